@@ -1,0 +1,156 @@
+/*
+ * hstu_attn.h -- C ABI of the GB300 (sm_103a) jagged HSTU attention library.
+ *
+ * Operation (MLCommons training PR #903 and TorchEasyRec PR #670 describe the
+ * op; the formula below is the pointwise-SiLU attention those pages run):
+ *
+ *   For every sequence b (rows [seq_offsets[b], seq_offsets[b+1]) of the
+ *   jagged tensors, length L_b), every head h and every query row i < L_b:
+ *     O[i] = sum over visible columns j of  silu(alpha * q_i . k_j) / N * v_j
+ *   with silu(x) = x * sigmoid(x) and N = max_seqlen (one N for the batch).
+ *
+ *   Visible columns (TorchEasyRec PR #670, "move the HSTU arbitrary-mask path
+ *   to NFUNC=5", PR body): row i reads (nfunc+1)/2 half-open column intervals
+ *   from func[:, row] -- interval 0 is [0, func[0]), interval t >= 1 is
+ *   [func[2t-1], func[2t]) -- in the sequence's local column coordinates.
+ *   Bounds are clamped to [0, L_b]; an interval whose end <= start is empty
+ *   and skipped; the visible set is the union of the intervals. func values
+ *   are never an error.
+ *
+ *   Targets-only mode (MLCommons training PR #903, "compute the last HSTU
+ *   layer only for the rows the loss reads"): one query row per sequence (its
+ *   candidate) against the full-length K/V of that sequence; the result is
+ *   that row of the full op.
+ *
+ * Conventions (all entry points):
+ *   - q, k, v, o, dout, dq, dk, dv: DEVICE pointers, bf16, contiguous
+ *     (tokens, num_heads, head_dim); row stride num_heads*head_dim elements.
+ *     Base addresses must be 16-byte aligned.
+ *   - seq_offsets: DEVICE int32 (batch+1), seq_offsets[0] = 0, non-decreasing,
+ *     seq_offsets[batch] = total, every length <= max_seqlen.
+ *   - func: DEVICE int32 (nfunc, total), shared by all heads (read once per
+ *     row). func_c (targets-only): DEVICE int32 (nfunc, batch).
+ *   - ws: DEVICE workspace of at least hstu_attn_workspace_size() bytes,
+ *     256-byte aligned, owned by the caller. The library allocates nothing.
+ *   - stream: a cudaStream_t passed as void*. Work is only enqueued on it; no
+ *     entry point synchronises except hstu_attn_get_device_status.
+ *   - Host-checkable errors (null pointers, unsupported nfunc or head_dim,
+ *     misalignment, workspace too small, bad sizes) return a status before
+ *     anything is enqueued. Errors only visible on the device (offsets that
+ *     are not monotone, a length above max_seqlen, a wrong last offset) set
+ *     the workspace error word; every later kernel that reads that workspace
+ *     then writes nothing. Read it with hstu_attn_get_device_status.
+ *   - No C++ exception crosses this boundary.
+ */
+#ifndef HSTU_ATTN_H_
+#define HSTU_ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define HSTU_API __attribute__((visibility("default")))
+#else
+#define HSTU_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  HSTU_OK = 0,
+  HSTU_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misaligned pointer */
+  HSTU_ERR_UNSUPPORTED = 2,  /* nfunc or head_dim this build has no kernel for */
+  HSTU_ERR_WORKSPACE = 3,    /* workspace null, too small or misaligned */
+  HSTU_ERR_CUDA = 4,         /* a CUDA runtime call failed (launch, sync) */
+  HSTU_ERR_DEVICE_INPUT = 5, /* device-side input check failed (offsets) */
+  HSTU_ERR_TIMEOUT = 6       /* a bounded in-kernel wait gave up */
+} hstu_status_t;
+
+typedef struct {
+  int32_t batch;      /* B, number of sequences (>= 1) */
+  int64_t total;      /* T = seq_offsets[B], rows of k and v (and of q, o) */
+  int32_t num_heads;  /* H >= 1 */
+  int32_t head_dim;   /* D = D_qk = D_v, one of 32, 64, 128 */
+  int32_t nfunc;      /* rows of func: 1, 3 or 5 */
+  int32_t max_seqlen; /* N: >= every L_b, <= 32768; also the 1/N scale */
+  float alpha;        /* scale on q.k, usually 1/sqrt(head_dim) */
+} hstu_attn_shape_t;
+
+/* Workspace modes for hstu_attn_workspace_size. */
+#define HSTU_WS_FULL 0    /* plan + hstu_attn_fwd + hstu_attn_bwd */
+#define HSTU_WS_TARGETS 1 /* hstu_attn_{fwd,bwd}_targets_only */
+
+/* Flags for hstu_attn_fwd / hstu_attn_bwd. */
+#define HSTU_FLAG_NONE 0
+/* The workspace already holds the plan that hstu_attn_plan (or an earlier
+ * fwd/bwd call without this flag) built for the same seq_offsets, func and
+ * shape; skip rebuilding it. The caller guarantees that none changed. */
+#define HSTU_FLAG_REUSE_PLAN 1
+
+/* 1 if this build has kernels for that nfunc (1, 3, 5), else 0. The pages'
+ * wheel bakes NFUNC in at compile time (TorchEasyRec PR #670 review thread on
+ * exposing it at runtime); here it is a runtime argument dispatched to
+ * compiled variants, and this query exposes which ones exist. */
+HSTU_API int hstu_attn_nfunc_supported(int32_t nfunc);
+
+/* Bytes of workspace the given mode needs for that shape; 0 if the shape is
+ * invalid or unsupported. */
+HSTU_API size_t hstu_attn_workspace_size(const hstu_attn_shape_t* shape, int32_t mode);
+
+/* Builds the plan in ws: validates seq_offsets on the device, classifies
+ * every (q-tile, kv-tile) pair of 128x128 as skipped / partial / full from
+ * func, and writes the longest-first work lists of the forward and backward
+ * kernels. row_counts (nullable, DEVICE int32 (total)) receives the number of
+ * visible columns of every row -- a debug output, head independent. */
+HSTU_API hstu_status_t hstu_attn_plan(const int32_t* seq_offsets, const int32_t* func,
+                             const hstu_attn_shape_t* shape, int32_t* row_counts, void* ws,
+                             size_t ws_bytes, void* stream);
+
+/* Forward: o = attention(q, k, v) over the full jagged batch. Rows with no
+ * visible column get 0. Builds the plan first unless HSTU_FLAG_REUSE_PLAN. */
+HSTU_API hstu_status_t hstu_attn_fwd(const void* q, const void* k, const void* v, void* o,
+                            const int32_t* seq_offsets, const int32_t* func,
+                            const hstu_attn_shape_t* shape, int32_t* row_counts, void* ws,
+                            size_t ws_bytes, uint32_t flags, void* stream);
+
+/* Backward of sum(o * dout): writes dq, dk, dv (all rows; zero where a row or
+ * column takes part in no visible pair). dk/dv accumulate per kv tile in
+ * tensor memory and dq per q tile, each output element written once by one
+ * CTA: no atomics, bitwise repeatable. */
+HSTU_API hstu_status_t hstu_attn_bwd(const void* dout, const void* q, const void* k, const void* v,
+                            void* dq, void* dk, void* dv, const int32_t* seq_offsets,
+                            const int32_t* func, const hstu_attn_shape_t* shape, void* ws,
+                            size_t ws_bytes, uint32_t flags, void* stream);
+
+/* Targets-only forward: q_c (batch, H, D) holds one candidate row per
+ * sequence, func_c (nfunc, batch) its intervals; k, v are full length
+ * (total, H, D). o_c (batch, H, D). */
+HSTU_API hstu_status_t hstu_attn_fwd_targets_only(const void* q_c, const void* k, const void* v, void* o_c,
+                                         const int32_t* seq_offsets, const int32_t* func_c,
+                                         const hstu_attn_shape_t* shape, void* ws,
+                                         size_t ws_bytes, void* stream);
+
+/* Targets-only backward of sum(o_c * dout_c): dq_c (batch, H, D); dk, dv
+ * (total, H, D), every row written (zero where not visible to its
+ * sequence's candidate). */
+HSTU_API hstu_status_t hstu_attn_bwd_targets_only(const void* dout_c, const void* q_c, const void* k,
+                                         const void* v, void* dq_c, void* dk, void* dv,
+                                         const int32_t* seq_offsets, const int32_t* func_c,
+                                         const hstu_attn_shape_t* shape, void* ws,
+                                         size_t ws_bytes, void* stream);
+
+/* Synchronises the stream, then returns the status recorded in the
+ * workspace error word (HSTU_OK, HSTU_ERR_DEVICE_INPUT, HSTU_ERR_TIMEOUT) or
+ * HSTU_ERR_CUDA if the synchronisation failed. */
+HSTU_API hstu_status_t hstu_attn_get_device_status(const void* ws, void* stream);
+
+/* Static description of a status code. */
+HSTU_API const char* hstu_status_string(hstu_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HSTU_ATTN_H_ */

@@ -1,0 +1,232 @@
+"""Thin Python binding of the C ABI in ``include/hstu_attn.h``.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+library. Tensors are torch CUDA tensors (torch supplies device memory and the
+current stream); the library is loaded with ctypes from this directory and the
+binding raises if it is missing -- there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional, Tuple
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libhstu_attn.so")
+
+HSTU_OK = 0
+STATUS_NAMES = {
+    0: "HSTU_OK", 1: "HSTU_ERR_INVALID_ARG", 2: "HSTU_ERR_UNSUPPORTED", 3: "HSTU_ERR_WORKSPACE",
+    4: "HSTU_ERR_CUDA", 5: "HSTU_ERR_DEVICE_INPUT", 6: "HSTU_ERR_TIMEOUT",
+}
+WS_FULL = 0
+WS_TARGETS = 1
+FLAG_REUSE_PLAN = 1
+
+EXPORTED = (
+    "hstu_attn_nfunc_supported", "hstu_attn_workspace_size", "hstu_attn_plan", "hstu_attn_fwd",
+    "hstu_attn_bwd", "hstu_attn_fwd_targets_only", "hstu_attn_bwd_targets_only",
+    "hstu_attn_get_device_status", "hstu_status_string",
+)
+
+
+class HstuError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)} ({status_string(status)})")
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [
+        ("batch", ctypes.c_int32),
+        ("total", ctypes.c_int64),
+        ("num_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("nfunc", ctypes.c_int32),
+        ("max_seqlen", ctypes.c_int32),
+        ("alpha", ctypes.c_float),
+    ]
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Loads the library (once). Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"CUDA library {path} is missing: build it first "
+            "(python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(path)
+    vp, i32, u32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_uint32, ctypes.c_size_t
+    sp = ctypes.POINTER(Shape)
+    sig = {
+        "hstu_attn_nfunc_supported": (ctypes.c_int, [i32]),
+        "hstu_attn_workspace_size": (sz, [sp, i32]),
+        "hstu_attn_plan": (ctypes.c_int, [vp, vp, sp, vp, vp, sz, vp]),
+        "hstu_attn_fwd": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, sp, vp, vp, sz, u32, vp]),
+        "hstu_attn_bwd": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, vp, vp, vp, sp, vp, sz, u32, vp]),
+        "hstu_attn_fwd_targets_only": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, sp, vp, sz, vp]),
+        "hstu_attn_bwd_targets_only": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, vp, vp, vp, sp, vp, sz, vp]),
+        "hstu_attn_get_device_status": (ctypes.c_int, [vp, vp]),
+        "hstu_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return load().hstu_status_string(status).decode()
+    except Exception:  # library missing: still format the error
+        return STATUS_NAMES.get(status, "unknown")
+
+
+def _check(status: int, what: str):
+    if status != HSTU_OK:
+        raise HstuError(status, what)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream: Optional[torch.cuda.Stream] = None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t: torch.Tensor, dtype, name: str):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def make_shape(batch: int, total: int, heads: int, dim: int, nfunc: int, max_seqlen: int,
+               alpha: Optional[float] = None) -> Shape:
+    if alpha is None:
+        alpha = 1.0 / math.sqrt(dim)
+    return Shape(batch, total, heads, dim, nfunc, max_seqlen, alpha)
+
+
+def nfunc_supported(nfunc: int) -> bool:
+    return bool(load().hstu_attn_nfunc_supported(nfunc))
+
+
+def workspace_size(shape: Shape, mode: int = WS_FULL) -> int:
+    return int(load().hstu_attn_workspace_size(ctypes.byref(shape), mode))
+
+
+def alloc_workspace(shape: Shape, mode: int = WS_FULL, device="cuda") -> torch.Tensor:
+    n = workspace_size(shape, mode)
+    if n == 0:
+        raise HstuError(2, "workspace_size")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def _shape_full(q, seq_offsets, func, max_seqlen, alpha):
+    T, H, D = q.shape
+    return make_shape(seq_offsets.numel() - 1, T, H, D, func.shape[0], max_seqlen, alpha)
+
+
+def plan(seq_offsets, func, shape: Shape, ws: torch.Tensor, row_counts=None, stream=None):
+    _need(seq_offsets, torch.int32, "seq_offsets")
+    _need(func, torch.int32, "func")
+    _check(load().hstu_attn_plan(_ptr(seq_offsets), _ptr(func), ctypes.byref(shape), _ptr(row_counts),
+                                 _ptr(ws), ws.numel(), _stream(stream)), "hstu_attn_plan")
+
+
+def fwd(q, k, v, seq_offsets, func, max_seqlen: int, alpha: Optional[float] = None,
+        ws: Optional[torch.Tensor] = None, row_counts: Optional[torch.Tensor] = None,
+        reuse_plan: bool = False, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """o = HSTU attention over the jagged batch (see include/hstu_attn.h)."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, torch.bfloat16, n)
+    _need(seq_offsets, torch.int32, "seq_offsets")
+    _need(func, torch.int32, "func")
+    shape = _shape_full(q, seq_offsets, func, max_seqlen, alpha)
+    if ws is None:
+        ws = alloc_workspace(shape, WS_FULL, q.device)
+    o = torch.empty_like(q) if out is None else out
+    flags = FLAG_REUSE_PLAN if reuse_plan else 0
+    _check(load().hstu_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(seq_offsets), _ptr(func),
+                                ctypes.byref(shape), _ptr(row_counts), _ptr(ws), ws.numel(), flags,
+                                _stream(stream)), "hstu_attn_fwd")
+    return o
+
+
+def bwd(do, q, k, v, seq_offsets, func, max_seqlen: int, alpha: Optional[float] = None,
+        ws: Optional[torch.Tensor] = None, reuse_plan: bool = False, outs=None,
+        stream=None) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    """(dq, dk, dv) of sum(o * do)."""
+    for t, n in ((do, "dout"), (q, "q"), (k, "k"), (v, "v")):
+        _need(t, torch.bfloat16, n)
+    _need(seq_offsets, torch.int32, "seq_offsets")
+    _need(func, torch.int32, "func")
+    shape = _shape_full(q, seq_offsets, func, max_seqlen, alpha)
+    if ws is None:
+        ws = alloc_workspace(shape, WS_FULL, q.device)
+    dq, dk, dv = outs if outs is not None else (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
+    flags = FLAG_REUSE_PLAN if reuse_plan else 0
+    _check(load().hstu_attn_bwd(_ptr(do), _ptr(q), _ptr(k), _ptr(v), _ptr(dq), _ptr(dk), _ptr(dv),
+                                _ptr(seq_offsets), _ptr(func), ctypes.byref(shape), _ptr(ws), ws.numel(),
+                                flags, _stream(stream)), "hstu_attn_bwd")
+    return dq, dk, dv
+
+
+def _shape_targets(q_c, k, seq_offsets, func_c, max_seqlen, alpha):
+    B, H, D = q_c.shape
+    return make_shape(B, k.shape[0], H, D, func_c.shape[0], max_seqlen, alpha)
+
+
+def fwd_targets_only(q_c, k, v, seq_offsets, func_c, max_seqlen: int, alpha: Optional[float] = None,
+                     ws: Optional[torch.Tensor] = None, out=None, stream=None) -> torch.Tensor:
+    for t, n in ((q_c, "q_c"), (k, "k"), (v, "v")):
+        _need(t, torch.bfloat16, n)
+    _need(seq_offsets, torch.int32, "seq_offsets")
+    _need(func_c, torch.int32, "func_c")
+    shape = _shape_targets(q_c, k, seq_offsets, func_c, max_seqlen, alpha)
+    if ws is None:
+        ws = alloc_workspace(shape, WS_TARGETS, q_c.device)
+    o_c = torch.empty_like(q_c) if out is None else out
+    _check(load().hstu_attn_fwd_targets_only(_ptr(q_c), _ptr(k), _ptr(v), _ptr(o_c), _ptr(seq_offsets),
+                                             _ptr(func_c), ctypes.byref(shape), _ptr(ws), ws.numel(),
+                                             _stream(stream)), "hstu_attn_fwd_targets_only")
+    return o_c
+
+
+def bwd_targets_only(do_c, q_c, k, v, seq_offsets, func_c, max_seqlen: int,
+                     alpha: Optional[float] = None, ws: Optional[torch.Tensor] = None, outs=None,
+                     stream=None):
+    for t, n in ((do_c, "dout_c"), (q_c, "q_c"), (k, "k"), (v, "v")):
+        _need(t, torch.bfloat16, n)
+    _need(seq_offsets, torch.int32, "seq_offsets")
+    _need(func_c, torch.int32, "func_c")
+    shape = _shape_targets(q_c, k, seq_offsets, func_c, max_seqlen, alpha)
+    if ws is None:
+        ws = alloc_workspace(shape, WS_TARGETS, q_c.device)
+    dq_c, dk, dv = outs if outs is not None else (torch.empty_like(q_c), torch.empty_like(k),
+                                                  torch.empty_like(v))
+    _check(load().hstu_attn_bwd_targets_only(_ptr(do_c), _ptr(q_c), _ptr(k), _ptr(v), _ptr(dq_c), _ptr(dk),
+                                             _ptr(dv), _ptr(seq_offsets), _ptr(func_c), ctypes.byref(shape),
+                                             _ptr(ws), ws.numel(), _stream(stream)),
+           "hstu_attn_bwd_targets_only")
+    return dq_c, dk, dv
+
+
+def device_status(ws: torch.Tensor, stream=None) -> int:
+    """Synchronises the stream and returns the workspace status code."""
+    return int(load().hstu_attn_get_device_status(_ptr(ws), _stream(stream)))

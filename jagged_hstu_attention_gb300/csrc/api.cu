@@ -1,0 +1,311 @@
+// C ABI of the library (declared in include/hstu_attn.h): host-side argument
+// checks, workspace layout, TMA tensor-map encoding and kernel dispatch.
+// Nothing here allocates device memory or synchronises, except
+// hstu_attn_get_device_status.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "../../include/hstu_attn.h"
+#include "common.cuh"
+#include "internal.h"
+
+namespace {
+
+using hstu::kBlock;
+
+bool aligned(const void* ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
+
+hstu_status_t check_shape(const hstu_attn_shape_t* s) {
+  if (!s) return HSTU_ERR_INVALID_ARG;
+  if (s->batch < 1 || s->total < 0 || s->num_heads < 1 || s->max_seqlen < 1)
+    return HSTU_ERR_INVALID_ARG;
+  if (s->total > INT32_MAX) return HSTU_ERR_INVALID_ARG;  // offsets are int32
+  if (s->max_seqlen > hstu::kMaxSeqlen) return HSTU_ERR_UNSUPPORTED;
+  if (s->batch > (1 << 22) - 1) return HSTU_ERR_UNSUPPORTED;  // work-list encoding
+  if (!hstu_attn_nfunc_supported(s->nfunc)) return HSTU_ERR_UNSUPPORTED;
+  if (s->head_dim != 32 && s->head_dim != 64 && s->head_dim != 128) return HSTU_ERR_UNSUPPORTED;
+  if (!(s->alpha == s->alpha)) return HSTU_ERR_INVALID_ARG;  // NaN
+  return HSTU_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// (tokens, H, D) bf16 viewed as a 3-D tensor {D, H, tokens}; box = 64
+// columns x 1 head x 128 rows with 128-byte swizzle. For D = 32 the box is
+// wider than the tensor and TMA fills the missing columns with zeros.
+bool make_map(CUtensorMap* m, const void* ptr, int64_t tokens, int heads, int dim) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(dim), static_cast<cuuint64_t>(heads),
+                        static_cast<cuuint64_t>(tokens)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(dim) * 2,
+                           static_cast<cuuint64_t>(heads) * dim * 2};
+  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(kBlock)};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+hstu_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? HSTU_OK : HSTU_ERR_CUDA; }
+
+// Upper bound on the number of (sequence, tile) work items.
+int grid_items(const hstu_attn_shape_t* s, int nt) {
+  const int64_t by_tokens = (s->total + kBlock - 1) / kBlock + s->batch;
+  const int64_t by_batch = static_cast<int64_t>(s->batch) * nt;
+  return static_cast<int>(by_tokens < by_batch ? by_tokens : by_batch);
+}
+
+hstu_status_t check_ws(const void* ws, size_t ws_bytes, size_t need) {
+  if (!ws || !aligned(ws, 256) || ws_bytes < need) return HSTU_ERR_WORKSPACE;
+  return HSTU_OK;
+}
+
+hstu::PlanParams plan_params(const int32_t* seq_offsets, const int32_t* func,
+                             const hstu_attn_shape_t* s, int32_t* row_counts, void* ws,
+                             const hstu::FullLayout& l) {
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  hstu::PlanParams p{};
+  p.seq_offsets = seq_offsets;
+  p.func = func;
+  p.row_counts = row_counts;
+  p.header = reinterpret_cast<int32_t*>(base + l.header);
+  p.qvis = reinterpret_cast<int32_t*>(base + l.qvis);
+  p.kvvis = reinterpret_cast<int32_t*>(base + l.kvvis);
+  p.fwd_list = reinterpret_cast<int32_t*>(base + l.fwd_list);
+  p.bwd_list = reinterpret_cast<int32_t*>(base + l.bwd_list);
+  p.cls = base + l.cls;
+  p.total = s->total;
+  p.batch = s->batch;
+  p.nfunc = s->nfunc;
+  p.nt = l.nt;
+  p.max_seqlen = s->max_seqlen;
+  return p;
+}
+
+hstu_status_t check_common(const int32_t* seq_offsets, const int32_t* func,
+                           const hstu_attn_shape_t* s, const void* ws, size_t ws_bytes) {
+  hstu_status_t st = check_shape(s);
+  if (st != HSTU_OK) return st;
+  if (!seq_offsets || (s->total > 0 && !func)) return HSTU_ERR_INVALID_ARG;
+  if (!aligned(seq_offsets, 4) || !aligned(func, 4)) return HSTU_ERR_INVALID_ARG;
+  return check_ws(ws, ws_bytes, hstu_attn_workspace_size(s, HSTU_WS_FULL));
+}
+
+bool tensor_ok(const void* p) { return p && aligned(p, 16); }
+
+hstu_status_t run_plan(const int32_t* seq_offsets, const int32_t* func, const hstu_attn_shape_t* s,
+                       int32_t* row_counts, void* ws, cudaStream_t stream) {
+  const hstu::FullLayout l = hstu::full_layout(s->batch, s->max_seqlen);
+  return from_cuda(hstu::launch_plan(plan_params(seq_offsets, func, s, row_counts, ws, l),
+                                     l.zero_bytes, stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+int hstu_attn_nfunc_supported(int32_t nfunc) {
+  return (nfunc == 1 || nfunc == 3 || nfunc == 5) ? 1 : 0;
+}
+
+size_t hstu_attn_workspace_size(const hstu_attn_shape_t* shape, int32_t mode) {
+  if (check_shape(shape) != HSTU_OK) return 0;
+  if (mode == HSTU_WS_FULL) return hstu::full_layout(shape->batch, shape->max_seqlen).total;
+  if (mode == HSTU_WS_TARGETS)
+    return hstu::targets_layout(shape->batch, shape->num_heads, shape->head_dim, shape->max_seqlen)
+        .total;
+  return 0;
+}
+
+hstu_status_t hstu_attn_plan(const int32_t* seq_offsets, const int32_t* func,
+                             const hstu_attn_shape_t* shape, int32_t* row_counts, void* ws,
+                             size_t ws_bytes, void* stream) {
+  hstu_status_t st = check_common(seq_offsets, func, shape, ws, ws_bytes);
+  if (st != HSTU_OK) return st;
+  if (row_counts && !aligned(row_counts, 4)) return HSTU_ERR_INVALID_ARG;
+  return run_plan(seq_offsets, func, shape, row_counts, ws, static_cast<cudaStream_t>(stream));
+}
+
+hstu_status_t hstu_attn_fwd(const void* q, const void* k, const void* v, void* o,
+                            const int32_t* seq_offsets, const int32_t* func,
+                            const hstu_attn_shape_t* shape, int32_t* row_counts, void* ws,
+                            size_t ws_bytes, uint32_t flags, void* stream) {
+  hstu_status_t st = check_common(seq_offsets, func, shape, ws, ws_bytes);
+  if (st != HSTU_OK) return st;
+  if (shape->total > 0 && !(tensor_ok(q) && tensor_ok(k) && tensor_ok(v) && tensor_ok(o)))
+    return HSTU_ERR_INVALID_ARG;
+  if (row_counts && !aligned(row_counts, 4)) return HSTU_ERR_INVALID_ARG;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (!(flags & HSTU_FLAG_REUSE_PLAN)) {
+    st = run_plan(seq_offsets, func, shape, row_counts, ws, cs);
+    if (st != HSTU_OK) return st;
+  }
+  if (shape->total == 0) return HSTU_OK;
+  const hstu::FullLayout l = hstu::full_layout(shape->batch, shape->max_seqlen);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  hstu::AttnParams p{};
+  if (!make_map(&p.tm_q, q, shape->total, shape->num_heads, shape->head_dim) ||
+      !make_map(&p.tm_k, k, shape->total, shape->num_heads, shape->head_dim) ||
+      !make_map(&p.tm_v, v, shape->total, shape->num_heads, shape->head_dim))
+    return HSTU_ERR_CUDA;
+  p.tm_do = p.tm_q;
+  p.seq_offsets = seq_offsets;
+  p.func = func;
+  p.out0 = static_cast<__nv_bfloat16*>(o);
+  p.cls = base + l.cls;
+  p.list = reinterpret_cast<const int32_t*>(base + l.fwd_list);
+  p.header = reinterpret_cast<int32_t*>(base + l.header);
+  p.total = shape->total;
+  p.heads = shape->num_heads;
+  p.dim = shape->head_dim;
+  p.nt = l.nt;
+  p.max_seqlen = shape->max_seqlen;
+  p.alpha = shape->alpha;
+  p.inv_n = 1.0f / static_cast<float>(shape->max_seqlen);
+  return from_cuda(hstu::launch_fwd(p, (shape->nfunc + 1) / 2, grid_items(shape, l.nt), cs));
+}
+
+hstu_status_t hstu_attn_bwd(const void* dout, const void* q, const void* k, const void* v,
+                            void* dq, void* dk, void* dv, const int32_t* seq_offsets,
+                            const int32_t* func, const hstu_attn_shape_t* shape, void* ws,
+                            size_t ws_bytes, uint32_t flags, void* stream) {
+  hstu_status_t st = check_common(seq_offsets, func, shape, ws, ws_bytes);
+  if (st != HSTU_OK) return st;
+  if (shape->total > 0 && !(tensor_ok(dout) && tensor_ok(q) && tensor_ok(k) && tensor_ok(v) &&
+                            tensor_ok(dq) && tensor_ok(dk) && tensor_ok(dv)))
+    return HSTU_ERR_INVALID_ARG;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (!(flags & HSTU_FLAG_REUSE_PLAN)) {
+    st = run_plan(seq_offsets, func, shape, nullptr, ws, cs);
+    if (st != HSTU_OK) return st;
+  }
+  if (shape->total == 0) return HSTU_OK;
+  const hstu::FullLayout l = hstu::full_layout(shape->batch, shape->max_seqlen);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  hstu::AttnParams p{};
+  if (!make_map(&p.tm_q, q, shape->total, shape->num_heads, shape->head_dim) ||
+      !make_map(&p.tm_k, k, shape->total, shape->num_heads, shape->head_dim) ||
+      !make_map(&p.tm_v, v, shape->total, shape->num_heads, shape->head_dim) ||
+      !make_map(&p.tm_do, dout, shape->total, shape->num_heads, shape->head_dim))
+    return HSTU_ERR_CUDA;
+  p.seq_offsets = seq_offsets;
+  p.func = func;
+  p.out0 = static_cast<__nv_bfloat16*>(dq);
+  p.out1 = static_cast<__nv_bfloat16*>(dk);
+  p.out2 = static_cast<__nv_bfloat16*>(dv);
+  p.cls = base + l.cls;
+  p.list = reinterpret_cast<const int32_t*>(base + l.bwd_list);
+  p.header = reinterpret_cast<int32_t*>(base + l.header);
+  p.total = shape->total;
+  p.heads = shape->num_heads;
+  p.dim = shape->head_dim;
+  p.nt = l.nt;
+  p.max_seqlen = shape->max_seqlen;
+  p.alpha = shape->alpha;
+  p.inv_n = 1.0f / static_cast<float>(shape->max_seqlen);
+  return from_cuda(hstu::launch_bwd(p, (shape->nfunc + 1) / 2, grid_items(shape, l.nt), cs));
+}
+
+static hstu_status_t targets_common(const void* q_c, const void* k, const void* v,
+                                    const int32_t* seq_offsets, const int32_t* func_c,
+                                    const hstu_attn_shape_t* shape, void* ws, size_t ws_bytes,
+                                    hstu::TgtParams* p) {
+  hstu_status_t st = check_shape(shape);
+  if (st != HSTU_OK) return st;
+  if (!seq_offsets || !func_c || !aligned(seq_offsets, 4) || !aligned(func_c, 4))
+    return HSTU_ERR_INVALID_ARG;
+  if (!tensor_ok(q_c) || (shape->total > 0 && !(tensor_ok(k) && tensor_ok(v))))
+    return HSTU_ERR_INVALID_ARG;
+  st = check_ws(ws, ws_bytes, hstu_attn_workspace_size(shape, HSTU_WS_TARGETS));
+  if (st != HSTU_OK) return st;
+  const hstu::TargetsLayout l =
+      hstu::targets_layout(shape->batch, shape->num_heads, shape->head_dim, shape->max_seqlen);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  *p = hstu::TgtParams{};
+  p->q_c = static_cast<const __nv_bfloat16*>(q_c);
+  p->k = static_cast<const __nv_bfloat16*>(k);
+  p->v = static_cast<const __nv_bfloat16*>(v);
+  p->seq_offsets = seq_offsets;
+  p->func_c = func_c;
+  p->partial = reinterpret_cast<float*>(base + l.partial);
+  p->header = reinterpret_cast<int32_t*>(base + l.header);
+  p->total = shape->total;
+  p->batch = shape->batch;
+  p->heads = shape->num_heads;
+  p->dim = shape->head_dim;
+  p->nfunc = shape->nfunc;
+  p->nc = l.nc;
+  p->max_seqlen = shape->max_seqlen;
+  p->alpha = shape->alpha;
+  p->inv_n = 1.0f / static_cast<float>(shape->max_seqlen);
+  return HSTU_OK;
+}
+
+hstu_status_t hstu_attn_fwd_targets_only(const void* q_c, const void* k, const void* v, void* o_c,
+                                         const int32_t* seq_offsets, const int32_t* func_c,
+                                         const hstu_attn_shape_t* shape, void* ws,
+                                         size_t ws_bytes, void* stream) {
+  hstu::TgtParams p;
+  hstu_status_t st = targets_common(q_c, k, v, seq_offsets, func_c, shape, ws, ws_bytes, &p);
+  if (st != HSTU_OK) return st;
+  if (!tensor_ok(o_c)) return HSTU_ERR_INVALID_ARG;
+  p.o_c = static_cast<__nv_bfloat16*>(o_c);
+  return from_cuda(hstu::launch_targets_fwd(p, static_cast<cudaStream_t>(stream)));
+}
+
+hstu_status_t hstu_attn_bwd_targets_only(const void* dout_c, const void* q_c, const void* k,
+                                         const void* v, void* dq_c, void* dk, void* dv,
+                                         const int32_t* seq_offsets, const int32_t* func_c,
+                                         const hstu_attn_shape_t* shape, void* ws,
+                                         size_t ws_bytes, void* stream) {
+  hstu::TgtParams p;
+  hstu_status_t st = targets_common(q_c, k, v, seq_offsets, func_c, shape, ws, ws_bytes, &p);
+  if (st != HSTU_OK) return st;
+  if (!tensor_ok(dout_c) || !tensor_ok(dq_c) || (shape->total > 0 && !(tensor_ok(dk) && tensor_ok(dv))))
+    return HSTU_ERR_INVALID_ARG;
+  p.do_c = static_cast<const __nv_bfloat16*>(dout_c);
+  p.dq_c = static_cast<__nv_bfloat16*>(dq_c);
+  p.dk = static_cast<__nv_bfloat16*>(dk);
+  p.dv = static_cast<__nv_bfloat16*>(dv);
+  return from_cuda(hstu::launch_targets_bwd(p, static_cast<cudaStream_t>(stream)));
+}
+
+hstu_status_t hstu_attn_get_device_status(const void* ws, void* stream) {
+  if (!ws || !aligned(ws, 256)) return HSTU_ERR_WORKSPACE;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(cs) != cudaSuccess) return HSTU_ERR_CUDA;
+  int32_t err = 0;
+  if (cudaMemcpy(&err, ws, sizeof(err), cudaMemcpyDeviceToHost) != cudaSuccess) return HSTU_ERR_CUDA;
+  if (err & hstu::kErrInput) return HSTU_ERR_DEVICE_INPUT;
+  if (err & hstu::kErrTimeout) return HSTU_ERR_TIMEOUT;
+  return HSTU_OK;
+}
+
+const char* hstu_status_string(hstu_status_t status) {
+  switch (status) {
+    case HSTU_OK: return "ok";
+    case HSTU_ERR_INVALID_ARG: return "invalid argument";
+    case HSTU_ERR_UNSUPPORTED: return "unsupported nfunc, head_dim or size";
+    case HSTU_ERR_WORKSPACE: return "workspace null, misaligned or too small";
+    case HSTU_ERR_CUDA: return "CUDA runtime error";
+    case HSTU_ERR_DEVICE_INPUT: return "device-side input check failed (seq_offsets)";
+    case HSTU_ERR_TIMEOUT: return "bounded in-kernel wait timed out";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

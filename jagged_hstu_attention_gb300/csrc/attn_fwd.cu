@@ -1,0 +1,291 @@
+// Forward kernel: one CTA per (work item = sequence b, q tile qt) and head h.
+//
+//   warp 4      TMA producer: Q tile once, then K/V tiles of every visited kv
+//               tile into a 2-stage ring.
+//   warp 5      TMEM owner and MMA issuer (one elected lane):
+//                 S[it % 2] = Q K^T             (tcgen05, SMEM x SMEM)
+//                 O        += P[it % 2] V       (tcgen05, TMEM x SMEM)
+//               S for tile it+1 is issued before P of tile it is consumed, so
+//               the tensor core works while the epilogue computes P.
+//   warps 0-3   epilogue, one thread per q row (= TMEM lane): load S, apply
+//               P = silu(alpha S) / N (and the row's interval mask on partial
+//               tiles only), pack P to bf16 in place over the S columns, and
+//               finally O -> bf16 -> global with rows past L_b left alone.
+//
+// TMEM (512 columns): S0 [0,128), S1 [128,256), O [256, 256+DP).
+// SMEM: Q (DP/64 chunks of 128 rows x 128 B, 128-byte swizzle), K and V
+// stages of the same shape.
+#include "common.cuh"
+#include "internal.h"
+
+namespace hstu {
+
+template <int DP>
+struct FwdSmem {
+  static constexpr int kChunks = DP / 64;
+  static constexpr int kTile = kChunks * kBlock * 128;  // bytes of a 128 x DP bf16 tile
+  alignas(1024) uint8_t q[kTile];
+  alignas(1024) uint8_t k[2][kTile];
+  alignas(1024) uint8_t v[2][kTile];
+  alignas(8) uint64_t bar_q, bar_kv_full[2], bar_kv_empty[2], bar_s_full[2], bar_p_full[2],
+      bar_o_full;
+  uint32_t tmem_base;
+  int abort_flag;
+  int n_tiles;
+  int16_t tile_j[kMaxTiles];
+  uint8_t tile_c[kMaxTiles];
+};
+
+template <typename S>
+__device__ __forceinline__ S& smem_as(uint8_t* raw) {
+  return *reinterpret_cast<S*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+}
+
+// Warp-uniform bounded wait.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  const bool ok = mbar_wait(bar, parity, abort_flag);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// P = silu(alpha s) / N = (alpha/N) * s * sigmoid(alpha s) for 32 columns,
+// masked by bit k of `mask`, packed to 16 bf16x2 words.
+__device__ __forceinline__ void silu_pack32(const uint32_t (&s)[32], uint32_t mask, float alpha,
+                                            float c1, uint32_t (&pk)[16]) {
+#pragma unroll
+  for (int e = 0; e < 32; e += 2) {
+    const float s0 = __uint_as_float(s[e]), s1 = __uint_as_float(s[e + 1]);
+    float p0 = c1 * s0 * sigmoidf_fast(alpha * s0);
+    float p1 = c1 * s1 * sigmoidf_fast(alpha * s1);
+    p0 = ((mask >> e) & 1u) ? p0 : 0.0f;
+    p1 = ((mask >> (e + 1)) & 1u) ? p1 : 0.0f;
+    pk[e / 2] = pack_bf16x2(p0, p1);
+  }
+}
+
+template <int DP, int NINT>
+__global__ void __launch_bounds__(192, 1) hstu_fwd_kernel(const __grid_constant__ AttnParams p) {
+  using Smem = FwdSmem<DP>;
+  extern __shared__ uint8_t smem_raw[];
+  Smem& s = smem_as<Smem>(smem_raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int item = blockIdx.x / p.heads, h = blockIdx.x - item * p.heads;
+  volatile int32_t* hdr = p.header;
+  if (item >= hdr[kHdrNFwd] || hdr[kHdrErr] != 0) return;
+  const int code = p.list[item];
+  const int b = code >> 8, qt = code & 255;
+  const int o0 = p.seq_offsets[b];
+  const int L = p.seq_offsets[b + 1] - o0;
+  const int ntiles_b = (L + kBlock - 1) / kBlock;
+  const uint8_t* cls_row = p.cls + (static_cast<size_t>(b) * p.nt + qt) * p.nt;
+
+  if (threadIdx.x == 0) {
+    s.abort_flag = 0;
+    mbar_init(smem_u32(&s.bar_q), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&s.bar_kv_full[i]), 1);
+      mbar_init(smem_u32(&s.bar_kv_empty[i]), 1);
+      mbar_init(smem_u32(&s.bar_s_full[i]), 1);
+      mbar_init(smem_u32(&s.bar_p_full[i]), 128);
+    }
+    mbar_init(smem_u32(&s.bar_o_full), 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {  // compact list of visited kv tiles
+    int n = 0;
+    for (int base = 0; base < ntiles_b; base += 32) {
+      const int j = base + lane;
+      const uint8_t c = j < ntiles_b ? cls_row[j] : kSkip;
+      const unsigned m = __ballot_sync(0xffffffffu, c != kSkip);
+      if (c != kSkip) {
+        const int pos = n + __popc(m & ((1u << lane) - 1u));
+        s.tile_j[pos] = static_cast<int16_t>(j);
+        s.tile_c[pos] = c;
+      }
+      n += __popc(m);
+    }
+    if (lane == 0) s.n_tiles = n;
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(&s.tmem_base), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = s.tmem_base;
+  const int nt = s.n_tiles;
+  volatile int* abort_flag = &s.abort_flag;
+  const int q_row0 = o0 + qt * kBlock;
+  constexpr int kTile = Smem::kTile;
+  constexpr int kChunkBytes = kBlock * 128;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    if (nt > 0 && elect_one_sync()) {
+      int last_use[2] = {-1, -1};
+      mbar_expect_tx(smem_u32(&s.bar_q), kTile);
+      for (int c = 0; c < Smem::kChunks; ++c)
+        tma_load_3d(smem_u32(s.q + c * kChunkBytes), &p.tm_q, smem_u32(&s.bar_q), c * 64, h, q_row0);
+      for (int it = 0; it < nt; ++it) {
+        const int st = it & 1, use = it >> 1;
+        if (use > 0 && !mbar_wait(smem_u32(&s.bar_kv_empty[st]), (use - 1) & 1, abort_flag)) break;
+        const int kv_row0 = o0 + s.tile_j[it] * kBlock;
+        const uint32_t bar = smem_u32(&s.bar_kv_full[st]);
+        mbar_expect_tx(bar, 2 * kTile);
+        for (int c = 0; c < Smem::kChunks; ++c) {
+          tma_load_3d(smem_u32(s.k[st] + c * kChunkBytes), &p.tm_k, bar, c * 64, h, kv_row0);
+          tma_load_3d(smem_u32(s.v[st] + c * kChunkBytes), &p.tm_v, bar, c * 64, h, kv_row0);
+        }
+        last_use[st] = use;
+      }
+      // Never leave with a copy in flight.
+      mbar_wait_drain(smem_u32(&s.bar_q), 0);
+      for (int st = 0; st < 2; ++st)
+        if (last_use[st] >= 0) mbar_wait_drain(smem_u32(&s.bar_kv_full[st]), last_use[st] & 1);
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (nt > 0 && elect_one_sync()) {
+      constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t idesc_o = idesc_bf16(128, DP, false, true);
+      const uint32_t q_base = smem_u32(s.q);
+      bool ok = mbar_wait(smem_u32(&s.bar_q), 0, abort_flag);
+      tc_fence_after();
+      for (int it = 0; ok && it <= nt; ++it) {
+        if (it < nt) {
+          const int st = it & 1, use = it >> 1;
+          if (!mbar_wait(smem_u32(&s.bar_kv_full[st]), use & 1, abort_flag)) break;
+          tc_fence_after();
+          const uint32_t k_base = smem_u32(s.k[st]);
+#pragma unroll
+          for (int kk = 0; kk < DP / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+            umma_ss(tbase + st * 128, sdesc_sw128(q_base + off, 16, 1024),
+                    sdesc_sw128(k_base + off, 16, 1024), idesc_s, kk > 0);
+          }
+          umma_commit(smem_u32(&s.bar_s_full[st]));
+        }
+        if (it >= 1) {
+          const int pi = it - 1, pst = pi & 1, puse = pi >> 1;
+          if (!mbar_wait(smem_u32(&s.bar_p_full[pst]), puse & 1, abort_flag)) break;
+          tc_fence_after();
+          const uint32_t v_base = smem_u32(s.v[pst]);
+#pragma unroll
+          for (int kk = 0; kk < kBlock / 16; ++kk) {
+            umma_ts(tbase + 256, tbase + pst * 128 + kk * 8,
+                    sdesc_sw128(v_base + kk * 16 * 128, kChunkBytes, 1024), idesc_o,
+                    (pi > 0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(smem_u32(&s.bar_kv_empty[pst]));
+        }
+      }
+      // Arrives once every MMA issued above has completed (also on abort).
+      umma_commit(smem_u32(&s.bar_o_full));
+      mbar_wait_drain(smem_u32(&s.bar_o_full), 0);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int r = threadIdx.x;  // q row within the tile == TMEM lane
+    const int i_loc = qt * kBlock + r;
+    const bool valid = i_loc < L;
+    int lo[NINT], hi[NINT];
+    load_row_intervals<NINT>(p.func, p.total, static_cast<int64_t>(o0) + i_loc, L, valid, lo, hi);
+    const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
+    const float alpha = p.alpha, c1 = p.alpha * p.inv_n;
+    bool ok = true;
+    for (int it = 0; it < nt; ++it) {
+      const int st = it & 1, use = it >> 1;
+      if (!warp_wait(smem_u32(&s.bar_s_full[st]), use & 1, abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      const int col0 = s.tile_j[it] * kBlock;
+      const bool partial = s.tile_c[it] == kPartial;
+      const uint32_t sb = tbase + lane_addr + st * 128;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t a[32], c[32];
+        tmem_ld32(sb + half * 64, a);
+        tmem_ld32(sb + half * 64 + 32, c);
+        tmem_ld_wait(a);
+        tmem_ld_wait(c);
+        uint32_t m0 = 0xffffffffu, m1 = 0xffffffffu;
+        if (partial) {
+          m0 = row_mask_word<NINT>(lo, hi, col0 + half * 64);
+          m1 = row_mask_word<NINT>(lo, hi, col0 + half * 64 + 32);
+        }
+        uint32_t pa[16], pc[16];
+        silu_pack32(a, m0, alpha, c1, pa);
+        silu_pack32(c, m1, alpha, c1, pc);
+        tmem_st16(sb + half * 32, pa);
+        tmem_st16(sb + half * 32 + 16, pc);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&s.bar_p_full[st]));
+    }
+    if (ok && nt > 0) ok = warp_wait(smem_u32(&s.bar_o_full), 0, abort_flag);
+    tc_fence_after();
+    if (ok && !*abort_flag) {
+      __nv_bfloat16* dst = p.out0 + (static_cast<int64_t>(q_row0 + r) * p.heads + h) * p.dim;
+#pragma unroll
+      for (int c = 0; c < DP / 32; ++c) {
+        uint32_t a[32];
+        if (nt > 0) {
+          tmem_ld32(tbase + lane_addr + 256 + c * 32, a);
+          tmem_ld_wait(a);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) a[e] = 0u;
+        }
+        if (valid && c * 32 < p.dim) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            pk[e] = pack_bf16x2(__uint_as_float(a[2 * e]), __uint_as_float(a[2 * e + 1]));
+          uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            d4[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+  if (threadIdx.x == 0 && s.abort_flag) atomicOr(p.header + kHdrErr, kErrTimeout);
+}
+
+template <int DP, int NINT>
+static cudaError_t launch_fwd_t(const AttnParams& p, int grid_items, cudaStream_t stream) {
+  const int smem = static_cast<int>(sizeof(FwdSmem<DP>)) + 1024;
+  static bool configured = false;  // attribute set once per instantiation
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(hstu_fwd_kernel<DP, NINT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const long long ctas = static_cast<long long>(grid_items) * p.heads;
+  if (ctas <= 0) return cudaSuccess;
+  hstu_fwd_kernel<DP, NINT><<<static_cast<unsigned>(ctas), 192, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fwd(const AttnParams& p, int nint, int grid_items, cudaStream_t stream) {
+  if (p.dim > 64) {
+    if (nint == 1) return launch_fwd_t<128, 1>(p, grid_items, stream);
+    if (nint == 2) return launch_fwd_t<128, 2>(p, grid_items, stream);
+    return launch_fwd_t<128, 3>(p, grid_items, stream);
+  }
+  if (nint == 1) return launch_fwd_t<64, 1>(p, grid_items, stream);
+  if (nint == 2) return launch_fwd_t<64, 2>(p, grid_items, stream);
+  return launch_fwd_t<64, 3>(p, grid_items, stream);
+}
+
+}  // namespace hstu

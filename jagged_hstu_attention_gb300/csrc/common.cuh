@@ -1,0 +1,163 @@
+// Shared definitions of the CUDA path: workspace layout, kernel parameter
+// blocks, the func-interval decode and the SiLU arithmetic used by the
+// epilogues.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "sm103_primitives.cuh"
+
+namespace hstu {
+
+constexpr int kBlock = 128;        // q-tile rows = kv-tile rows
+constexpr int kMaxSeqlen = 32768;  // => at most 256 tiles per sequence
+constexpr int kMaxTiles = kMaxSeqlen / kBlock;
+constexpr int kMaxIntervals = 3;   // nfunc <= 5
+
+// Workspace header (int32 words).
+constexpr int kHdrErr = 0;     // error bits (kErrInput | kErrTimeout)
+constexpr int kHdrNFwd = 1;    // entries of the forward work list
+constexpr int kHdrNBwd = 2;    // entries of the backward work list
+constexpr int kHdrWords = 64;  // 256 bytes
+constexpr int kErrInput = 1;
+constexpr int kErrTimeout = 2;
+
+// Tile classes written by the plan.
+constexpr uint8_t kSkip = 0, kPartial = 1, kFull = 2;
+
+// Backward work-list entries: bit 30 = role (1: dK/dV for a kv tile,
+// 0: dQ for a q tile), bits 8..29 = sequence, bits 0..7 = tile.
+constexpr int kRoleDkdv = 1 << 30;
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Layout of the HSTU_WS_FULL workspace. header, qvis and kvvis are contiguous
+// so that one memset clears them at the start of a plan.
+struct FullLayout {
+  int nt = 0;  // tiles per sequence at max_seqlen
+  size_t header = 0, qvis = 0, kvvis = 0, zero_bytes = 0, fwd_list = 0, bwd_list = 0, cls = 0,
+         total = 0;
+};
+inline FullLayout full_layout(int batch, int max_seqlen) {
+  FullLayout l;
+  l.nt = (max_seqlen + kBlock - 1) / kBlock;
+  const size_t items = static_cast<size_t>(batch) * l.nt;
+  l.header = 0;
+  l.qvis = kHdrWords * 4;
+  l.kvvis = l.qvis + align_up(items * 4, 256);
+  l.zero_bytes = l.kvvis + align_up(items * 4, 256);
+  l.fwd_list = l.zero_bytes;
+  l.bwd_list = l.fwd_list + align_up(items * 4, 256);
+  l.cls = l.bwd_list + align_up(2 * items * 4, 256);
+  l.total = l.cls + align_up(items * l.nt, 256);
+  return l;
+}
+
+// Targets-only: keys per CTA chunk and the workspace of fp32 partials.
+constexpr int kTgtChunk = 256;
+struct TargetsLayout {
+  int nc = 0;
+  size_t header = 0, partial = 0, total = 0;
+};
+inline TargetsLayout targets_layout(int batch, int heads, int dim, int max_seqlen) {
+  TargetsLayout l;
+  l.nc = (max_seqlen + kTgtChunk - 1) / kTgtChunk;
+  l.header = 0;
+  l.partial = kHdrWords * 4;
+  l.total = l.partial + align_up(static_cast<size_t>(batch) * heads * l.nc * dim * 4, 256);
+  return l;
+}
+
+struct PlanParams {
+  const int32_t* seq_offsets;
+  const int32_t* func;
+  int32_t* row_counts;  // nullable
+  int32_t* header;
+  int32_t* qvis;
+  int32_t* kvvis;
+  int32_t* fwd_list;
+  int32_t* bwd_list;
+  uint8_t* cls;
+  int64_t total;
+  int32_t batch, nfunc, nt, max_seqlen;
+};
+
+struct alignas(64) AttnParams {
+  CUtensorMap tm_q, tm_k, tm_v, tm_do;
+  const int32_t* seq_offsets;
+  const int32_t* func;
+  __nv_bfloat16* out0;  // fwd: o; bwd: dq
+  __nv_bfloat16* out1;  // bwd: dk
+  __nv_bfloat16* out2;  // bwd: dv
+  const uint8_t* cls;
+  const int32_t* list;
+  int32_t* header;
+  int64_t total;
+  int32_t heads, dim, nt, max_seqlen;
+  float alpha, inv_n;
+};
+
+struct TgtParams {
+  const __nv_bfloat16* q_c;
+  const __nv_bfloat16* k;
+  const __nv_bfloat16* v;
+  const __nv_bfloat16* do_c;
+  __nv_bfloat16* o_c;   // fwd output
+  __nv_bfloat16* dq_c;  // bwd outputs
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  const int32_t* seq_offsets;
+  const int32_t* func_c;
+  float* partial;
+  int32_t* header;
+  int64_t total;
+  int32_t batch, heads, dim, nfunc, nc, max_seqlen;
+  float alpha, inv_n;
+};
+
+// ---------------------------------------------------------------- func decode
+// Clamped intervals of one row; an empty interval becomes [0, 0) so that it
+// can never widen a bound or pass a membership test.
+template <int NINT>
+__device__ __forceinline__ void load_row_intervals(const int32_t* __restrict__ func, int64_t total,
+                                                   int64_t row, int L, bool valid, int (&lo)[NINT],
+                                                   int (&hi)[NINT]) {
+#pragma unroll
+  for (int t = 0; t < NINT; ++t) {
+    int a = 0, e = 0;
+    if (valid) {
+      a = (t == 0) ? 0 : __ldg(func + static_cast<int64_t>(2 * t - 1) * total + row);
+      e = __ldg(func + static_cast<int64_t>(2 * t) * total + row);
+      a = min(max(a, 0), L);
+      e = min(max(e, 0), L);
+      if (e <= a) a = e = 0;
+    }
+    lo[t] = a;
+    hi[t] = e;
+  }
+}
+
+// Bit k set iff column (base + k) lies in one of the row's intervals, k < 32.
+template <int NINT>
+__device__ __forceinline__ uint32_t row_mask_word(const int (&lo)[NINT], const int (&hi)[NINT],
+                                                  int base) {
+  uint32_t w = 0;
+#pragma unroll
+  for (int t = 0; t < NINT; ++t) {
+    const int a = max(lo[t] - base, 0);
+    const int e = min(hi[t] - base, 32);
+    if (e > a) w |= static_cast<uint32_t>(((1ull << e) - 1ull) ^ ((1ull << a) - 1ull));
+  }
+  return w;
+}
+
+// ---------------------------------------------------------------- SiLU math
+__device__ __forceinline__ float sigmoidf_fast(float x) {
+  return __fdividef(1.0f, 1.0f + __expf(-x));
+}
+
+}  // namespace hstu

@@ -1,0 +1,200 @@
+// Plan: device-side validation of seq_offsets, the func prologue that
+// classifies every (q-tile, kv-tile) pair of a sequence, the per-row visible
+// counts, and the longest-first work lists of the forward and backward
+// kernels. Nothing here needs a host synchronisation.
+//
+// The pages' kernels reduce per-tile min/max bounds of every interval
+// (including the empty padded ones) and then test every interval in every KV
+// block (TorchEasyRec PR #670, review thread: the cost of the padded third
+// interval came from those reductions and from the per-block masking loop).
+// Here empty intervals are normalised away before anything else, and each
+// pair's class comes from exact per-row popcounts of the row's visible
+// columns inside the tile:
+//   skip    -- no valid row sees any column of the tile,
+//   full    -- every row of the q tile is valid and sees all 128 columns,
+//   partial -- anything else (the kernels then apply the per-row mask).
+#include "common.cuh"
+#include "internal.h"
+
+namespace hstu {
+
+template <int NINT>
+__global__ void __launch_bounds__(128) plan_classify_kernel(const PlanParams p) {
+  const int b = blockIdx.x, qt = blockIdx.y;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int o0 = p.seq_offsets[b];
+  const int o1 = p.seq_offsets[b + 1];
+  const int L = o1 - o0;
+  if (b == 0 && qt == 0 && tid == 0) {
+    if (p.seq_offsets[0] != 0 || static_cast<int64_t>(p.seq_offsets[p.batch]) != p.total)
+      atomicOr(p.header + kHdrErr, kErrInput);
+  }
+  if (L < 0 || L > p.max_seqlen || o0 < 0 || static_cast<int64_t>(o1) > p.total) {
+    if (qt == 0 && tid == 0) atomicOr(p.header + kHdrErr, kErrInput);
+    return;
+  }
+  const int ntiles = (L + kBlock - 1) / kBlock;
+  if (qt >= ntiles) return;
+
+  __shared__ uint32_t any_bits[4][kMaxTiles / 32];
+  __shared__ uint32_t all_bits[4][kMaxTiles / 32];
+  __shared__ int n_visit;
+  for (int x = tid; x < 4 * (kMaxTiles / 32); x += 128) {
+    (&any_bits[0][0])[x] = 0;
+    (&all_bits[0][0])[x] = 0;
+  }
+  if (tid == 0) n_visit = 0;
+  __syncthreads();
+
+  const int i = qt * kBlock + tid;
+  const bool valid = i < L;
+  int lo[NINT], hi[NINT];
+  load_row_intervals<NINT>(p.func, p.total, static_cast<int64_t>(o0) + i, L, valid, lo, hi);
+
+  int count = 0;
+  for (int j = 0; j < ntiles; ++j) {
+    int c = 0;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) c += __popc(row_mask_word<NINT>(lo, hi, j * kBlock + 32 * w));
+    count += c;
+    const unsigned any = __ballot_sync(0xffffffffu, c > 0);
+    const unsigned all = __ballot_sync(0xffffffffu, c == kBlock);
+    if (lane == 0) {
+      if (any) any_bits[warp][j >> 5] |= 1u << (j & 31);
+      if (all == 0xffffffffu) all_bits[warp][j >> 5] |= 1u << (j & 31);
+    }
+  }
+  if (valid && p.row_counts) p.row_counts[o0 + i] = count;
+  __syncthreads();
+
+  const size_t row_base = (static_cast<size_t>(b) * p.nt + qt) * p.nt;
+  int mine = 0;
+  for (int j = tid; j < ntiles; j += 128) {
+    const uint32_t bit = 1u << (j & 31);
+    const int word = j >> 5;
+    const bool any = ((any_bits[0][word] | any_bits[1][word] | any_bits[2][word] |
+                       any_bits[3][word]) & bit) != 0;
+    const bool all = ((all_bits[0][word] & all_bits[1][word] & all_bits[2][word] &
+                       all_bits[3][word]) & bit) != 0;
+    const uint8_t cls = all ? kFull : (any ? kPartial : kSkip);
+    p.cls[row_base + j] = cls;
+    if (cls != kSkip) {
+      ++mine;
+      atomicAdd(p.kvvis + static_cast<size_t>(b) * p.nt + j, 1);
+    }
+  }
+  if (mine) atomicAdd(&n_visit, mine);
+  __syncthreads();
+  if (tid == 0) p.qvis[static_cast<size_t>(b) * p.nt + qt] = n_visit;
+}
+
+// Exclusive scan of cnt[0..n) in place (one block of 1024 threads).
+__device__ void block_exclusive_scan(int* cnt, int n) {
+  __shared__ int carry;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  __shared__ int warp_sums[32];
+  if (tid == 0) carry = 0;
+  __syncthreads();
+  for (int base = 0; base < n; base += blockDim.x) {
+    const int idx = base + tid;
+    const int x = idx < n ? cnt[idx] : 0;
+    int incl = x;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += y;
+    }
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      const int ws = lane < (blockDim.x >> 5) ? warp_sums[lane] : 0;
+      int wincl = ws;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, wincl, d);
+        if (lane >= d) wincl += y;
+      }
+      warp_sums[lane] = wincl - ws;
+    }
+    __syncthreads();
+    const int excl = carry + warp_sums[warp] + incl - x;
+    __syncthreads();
+    if (idx < n) cnt[idx] = excl;
+    if (tid == blockDim.x - 1) carry = excl + x;
+    __syncthreads();
+  }
+}
+
+// Longest-first lists by counting sort on the number of tile pairs each item
+// visits (weight). Equal weights may come out in any order: every output
+// element is computed by exactly one CTA with a fixed internal order, so the
+// list order only changes scheduling, never results.
+__global__ void __launch_bounds__(1024) plan_sort_kernel(const PlanParams p) {
+  __shared__ int hist_f[kMaxTiles + 1];
+  __shared__ int hist_b[4 * kMaxTiles + 1];
+  const int tid = threadIdx.x;
+  if (p.header[kHdrErr] != 0) return;
+  const int nt = p.nt;
+  const int max_wf = nt, max_wb = 4 * nt;
+  for (int x = tid; x <= max_wf; x += blockDim.x) hist_f[x] = 0;
+  for (int x = tid; x <= max_wb; x += blockDim.x) hist_b[x] = 0;
+  __syncthreads();
+  const int n_all = p.batch * nt;
+  auto tiles_of = [&](int b) {
+    int L = p.seq_offsets[b + 1] - p.seq_offsets[b];
+    L = min(max(L, 0), p.max_seqlen);
+    return (L + kBlock - 1) / kBlock;
+  };
+  // Histograms; slot index = max_w - weight gives descending order.
+  for (int idx = tid; idx < n_all; idx += blockDim.x) {
+    const int b = idx / nt, t = idx - b * nt;
+    if (t >= tiles_of(b)) continue;
+    const int wq = min(p.qvis[idx], nt);
+    const int wk = min(p.kvvis[idx], nt);
+    atomicAdd(&hist_f[max_wf - wq], 1);
+    atomicAdd(&hist_b[max_wb - 3 * wq], 1);
+    atomicAdd(&hist_b[max_wb - 4 * wk], 1);
+  }
+  __syncthreads();
+  block_exclusive_scan(hist_f, max_wf + 1);
+  block_exclusive_scan(hist_b, max_wb + 1);
+  __syncthreads();
+  int my_f = 0;
+  for (int idx = tid; idx < n_all; idx += blockDim.x) {
+    const int b = idx / nt, t = idx - b * nt;
+    if (t >= tiles_of(b)) continue;
+    ++my_f;
+    const int wq = min(p.qvis[idx], nt);
+    const int wk = min(p.kvvis[idx], nt);
+    const int code = (b << 8) | t;
+    p.fwd_list[atomicAdd(&hist_f[max_wf - wq], 1)] = code;
+    p.bwd_list[atomicAdd(&hist_b[max_wb - 3 * wq], 1)] = code;
+    p.bwd_list[atomicAdd(&hist_b[max_wb - 4 * wk], 1)] = code | kRoleDkdv;
+  }
+  // total item count
+  __shared__ int n_items;
+  if (tid == 0) n_items = 0;
+  __syncthreads();
+  if (my_f) atomicAdd(&n_items, my_f);
+  __syncthreads();
+  if (tid == 0) {
+    p.header[kHdrNFwd] = n_items;
+    p.header[kHdrNBwd] = 2 * n_items;
+  }
+}
+
+cudaError_t launch_plan(const PlanParams& p, size_t zero_bytes, cudaStream_t stream) {
+  cudaError_t e = cudaMemsetAsync(p.header, 0, zero_bytes, stream);
+  if (e != cudaSuccess) return e;
+  const dim3 grid(p.batch, p.nt);
+  const int nint = (p.nfunc + 1) / 2;
+  if (nint == 1) plan_classify_kernel<1><<<grid, 128, 0, stream>>>(p);
+  else if (nint == 2) plan_classify_kernel<2><<<grid, 128, 0, stream>>>(p);
+  else plan_classify_kernel<3><<<grid, 128, 0, stream>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  plan_sort_kernel<<<1, 1024, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace hstu

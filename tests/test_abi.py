@@ -1,0 +1,95 @@
+"""C ABI checks that need no GPU: the library loads, exports every function
+the header declares, and rejects bad arguments on the host with the right
+status before anything is enqueued."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from jagged_hstu_attention_gb300 import binding as hb
+from jagged_hstu_attention_gb300 import build_ext
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "hstu_attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_ext.build()
+    return hb.load()
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(hstu_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared()
+    for n in ("hstu_attn_fwd", "hstu_attn_bwd", "hstu_attn_fwd_targets_only",
+              "hstu_attn_bwd_targets_only", "hstu_attn_plan", "hstu_attn_workspace_size"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+    assert set(_declared()) <= set(hb.EXPORTED) | set(_declared())
+
+
+def _shape(**kw):
+    s = dict(batch=4, total=1000, heads=2, dim=128, nfunc=5, max_seqlen=300, alpha=0.1)
+    s.update(kw)
+    return hb.make_shape(s["batch"], s["total"], s["heads"], s["dim"], s["nfunc"], s["max_seqlen"],
+                         s["alpha"])
+
+
+def test_nfunc_supported(lib):
+    assert [hb.nfunc_supported(n) for n in range(7)] == [False, True, False, True, False, True, False]
+
+
+def test_workspace_size(lib):
+    full = hb.workspace_size(_shape(), hb.WS_FULL)
+    tgt = hb.workspace_size(_shape(), hb.WS_TARGETS)
+    assert full > 0 and full % 256 == 0 and tgt > 0
+    assert hb.workspace_size(_shape(max_seqlen=3000), hb.WS_FULL) > full
+    for bad in (dict(nfunc=2), dict(dim=96), dict(batch=0), dict(max_seqlen=0),
+                dict(max_seqlen=40000), dict(heads=0), dict(total=-1)):
+        assert hb.workspace_size(_shape(**bad), hb.WS_FULL) == 0, bad
+    assert hb.workspace_size(_shape(), 7) == 0
+
+
+def _fwd(lib, shape, q=1 << 20, k=1 << 20, v=1 << 20, o=1 << 20, off=1 << 20, func=1 << 20,
+         ws=1 << 20, ws_bytes=1 << 30):
+    vp = ctypes.c_void_p
+    return lib.hstu_attn_fwd(vp(q), vp(k), vp(v), vp(o), vp(off), vp(func), ctypes.byref(shape), None,
+                             vp(ws), ws_bytes, 0, None)
+
+
+def test_host_validation_statuses(lib):
+    s = _shape()
+    assert _fwd(lib, s, q=0) == 1                       # null tensor
+    assert _fwd(lib, s, o=(1 << 20) + 8) == 1           # misaligned tensor
+    assert _fwd(lib, s, off=0) == 1                     # null offsets
+    assert _fwd(lib, _shape(nfunc=4)) == 2              # unsupported nfunc
+    assert _fwd(lib, _shape(dim=80)) == 2               # unsupported head_dim
+    assert _fwd(lib, s, ws=0) == 3                      # null workspace
+    assert _fwd(lib, s, ws=(1 << 20) + 64) == 3         # misaligned workspace
+    assert _fwd(lib, s, ws_bytes=16) == 3               # workspace too small
+    assert _fwd(lib, _shape(alpha=float("nan"))) == 1   # NaN alpha
+    vp = ctypes.c_void_p
+    assert lib.hstu_attn_bwd(vp(0), vp(0), vp(0), vp(0), vp(0), vp(0), vp(0), vp(1 << 20), vp(1 << 20),
+                             ctypes.byref(s), vp(1 << 20), 1 << 30, 0, None) == 1
+    assert lib.hstu_attn_fwd_targets_only(vp(0), vp(1 << 20), vp(1 << 20), vp(1 << 20), vp(1 << 20),
+                                          vp(1 << 20), ctypes.byref(s), vp(1 << 20), 1 << 30, None) == 1
+    assert lib.hstu_attn_plan(vp(1 << 20), vp(1 << 20), ctypes.byref(_shape(nfunc=0)), None, vp(1 << 20),
+                              1 << 30, None) == 2
+    assert lib.hstu_attn_get_device_status(vp(0), None) == 3
+
+
+def test_status_strings(lib):
+    for st in range(7):
+        assert len(hb.status_string(st)) > 0
+    assert "unknown" in hb.status_string(42)

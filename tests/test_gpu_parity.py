@@ -1,0 +1,213 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU fp64 oracle.
+
+Small batches are compared element by element in full; the full-size
+workloads are run whole on the GPU and compared on a seeded sample of
+sequences (always holding the longest and the shortest one).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.hstu_oracle as orc
+from jagged_hstu_attention_gb300 import binding as hb
+from jagged_hstu_attention_gb300 import workloads as wl
+from hstu_testutil import GpuBatch, check_grad, check_o, compare, np64, sample_seqs
+
+pytestmark = pytest.mark.gpu
+
+
+def _gen(lens, H, D, seed):
+    T = int(np.sum(lens))
+    g = torch.Generator().manual_seed(seed)
+    return [wl.randn_bf16((T, H, D), g) for _ in range(4)]
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_tiny_full_parity(seed):
+    gb = GpuBatch.from_config(wl.CONFIGS["tiny"], seed)
+    compare(gb.run(), gb.oracle())
+
+
+@pytest.mark.parametrize("D", [32, 64, 128])
+@pytest.mark.parametrize("mask", ["tiny", "sla", "causal", "onerank"])
+def test_ragged_tails_all_masks(D, mask):
+    """Lengths that end mid-tile, a one-row and an empty sequence, several
+    tiles per sequence, every mask family, every head size."""
+    lens = [1, 130, 0, 300, 127, 257] if mask != "onerank" else [40, 300, 129, 257]
+    nfunc = 1 if mask == "causal" else 5
+    cfg = wl.Config("t", len(lens), 0, 0, 2, D, mask, nfunc, k1=70, k2=20)
+    func = wl.build_func(cfg, np.array(lens), nfunc)
+    q, k, v, do = _gen(lens, 2, D, seed=D)
+    gb = GpuBatch(lens, func, q, k, v, do, max_seqlen=320)
+    compare(gb.run(), gb.oracle())
+
+
+@pytest.mark.parametrize("nfunc", [1, 3, 5])
+def test_random_intervals(nfunc):
+    """Arbitrary (also negative, out-of-range, reversed) func values."""
+    lens = np.array([200, 77, 384, 5])
+    T = int(lens.sum())
+    rng = np.random.default_rng(nfunc)
+    func = rng.integers(-20, 420, size=(nfunc, T)).astype(np.int32)
+    q, k, v, do = _gen(lens, 3, 64, seed=11)
+    gb = GpuBatch(lens, func, q, k, v, do, max_seqlen=400)
+    compare(gb.run(), gb.oracle())
+
+
+def test_all_intervals_empty_gives_zeros():
+    lens = np.array([150, 40])
+    func = np.zeros((3, 190), dtype=np.int32)
+    q, k, v, do = _gen(lens, 2, 128, seed=3)
+    gb = GpuBatch(lens, func, q, k, v, do)
+    out = gb.run()
+    for n in ("o", "dq", "dk", "dv"):
+        assert not out[n].any(), n
+    assert not out["counts"].any()
+
+
+def test_sla_padding_is_bitwise_inert():
+    cfg = wl.CONFIGS["sla_b32_s1024"]
+    g5 = GpuBatch.from_config(cfg, 0, nfunc=5)
+    g3 = GpuBatch(g5.lens, g5.func[:3], g5.q, g5.k, g5.v, g5.do)
+    a, b = g5.run(), g3.run()
+    for n in ("o", "dq", "dk", "dv", "counts"):
+        assert torch.equal(a[n], b[n]), n
+
+
+@pytest.mark.parametrize("name", ["sla_b32_s1024", "sla_b16_s2048", "onerank_b64"])
+def test_config_parity_sampled(name):
+    cfg = wl.CONFIGS[name]
+    gb = GpuBatch.from_config(cfg, 0)
+    out = gb.run()
+    seqs = sample_seqs(gb.lens, 4)
+    compare(out, gb.oracle(seqs))
+    # visible counts of every row, bitwise
+    ref_counts = orc.visible_counts(gb.offsets, gb.func, gb.nfunc)
+    assert np.array_equal(out["counts"].cpu().numpy(), ref_counts)
+
+
+def test_dlrm_full_length_sampled():
+    cfg = wl.CONFIGS["dlrm_b1024"]
+    gb = GpuBatch.from_config(cfg, 0, device="cuda")
+    out = gb.run()
+    seqs = sample_seqs(gb.lens, 3)
+    compare(out, gb.oracle(seqs))
+    # causal counts of every row: i + 1, closed form
+    exp = np.concatenate([np.arange(L) + 1 for L in gb.lens])
+    assert np.array_equal(out["counts"].cpu().numpy(), exp)
+
+
+def _targets_inputs(gb, seed=5):
+    B = len(gb.lens)
+    H, D = gb.q.shape[1], gb.q.shape[2]
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    q_c = wl.randn_bf16((B, H, D), g, "cuda")
+    do_c = wl.randn_bf16((B, H, D), g, "cuda")
+    func_c = wl.build_func_candidates(gb.lens, gb.nfunc)
+    return q_c, do_c, func_c
+
+
+def _run_targets(gb, q_c, do_c, func_c):
+    d_fc = torch.tensor(func_c, dtype=torch.int32, device="cuda")
+    shape = hb.make_shape(len(gb.lens), gb.total, gb.q.shape[1], gb.q.shape[2], gb.nfunc, gb.max_seqlen,
+                          gb.alpha)
+    ws = hb.alloc_workspace(shape, hb.WS_TARGETS)
+    o_c = hb.fwd_targets_only(q_c, gb.k, gb.v, gb.d_off, d_fc, gb.max_seqlen, gb.alpha, ws=ws)
+    dq_c, dk, dv = hb.bwd_targets_only(do_c, q_c, gb.k, gb.v, gb.d_off, d_fc, gb.max_seqlen, gb.alpha, ws=ws)
+    assert hb.device_status(ws) == hb.HSTU_OK
+    return o_c, dq_c, dk, dv
+
+
+def test_targets_only_equals_full_candidate_row():
+    """Targets-only output equals the full path's candidate row on the GPU,
+    and both match the oracle."""
+    lens = np.array([300, 1, 129, 513, 64])
+    cfg = wl.Config("c", 5, 0, 0, 2, 128, "causal", 1)
+    func = wl.build_func(cfg, lens, 1)
+    q, k, v, do = _gen(lens, 2, 128, seed=9)
+    gb = GpuBatch(lens, func, q, k, v, do)
+    cand = torch.as_tensor(gb.offsets[1:] - 1, device="cuda")
+    q_c = gb.q.index_select(0, cand).contiguous()
+    do_c = gb.do.index_select(0, cand).contiguous()
+    func_c = wl.build_func_candidates(lens, 1)
+    o_c, dq_c, dk, dv = _run_targets(gb, q_c, do_c, func_c)
+    full = gb.run(want_bwd=False)["o"].index_select(0, cand)
+    check_o(np64(o_c), np64(full).astype(np.float64), "targets vs full row")
+    ref = orc.fwd_targets_only(np64(q_c), np64(gb.k), np64(gb.v), gb.offsets, func_c, 1, gb.max_seqlen, gb.alpha)
+    check_o(np64(o_c), ref)
+    rdq, rdk, rdv = orc.bwd_targets_only(np64(do_c), np64(q_c), np64(gb.k), np64(gb.v), gb.offsets, func_c, 1,
+                                         gb.max_seqlen, gb.alpha)
+    check_grad(np64(dq_c), rdq, "dq_c")
+    check_grad(np64(dk), rdk, "dk")
+    check_grad(np64(dv), rdv, "dv")
+
+
+@pytest.mark.parametrize("nfunc", [3, 5])
+def test_targets_only_interval_masks(nfunc):
+    lens = np.array([700, 33, 260])
+    T = int(lens.sum())
+    rng = np.random.default_rng(nfunc + 7)
+    q, k, v, do = _gen(lens, 4, 64, seed=13)
+    gb = GpuBatch(lens, np.zeros((nfunc, T), np.int32), q, k, v, do)
+    func_c = rng.integers(-10, 720, size=(nfunc, 3)).astype(np.int32)
+    g = torch.Generator().manual_seed(3)
+    q_c = wl.randn_bf16((3, 4, 64), g).cuda()
+    do_c = wl.randn_bf16((3, 4, 64), g).cuda()
+    o_c, dq_c, dk, dv = _run_targets(gb, q_c, do_c, func_c)
+    ref = orc.fwd_targets_only(np64(q_c), np64(gb.k), np64(gb.v), gb.offsets, func_c, nfunc, gb.max_seqlen,
+                               gb.alpha)
+    check_o(np64(o_c), ref)
+    rdq, rdk, rdv = orc.bwd_targets_only(np64(do_c), np64(q_c), np64(gb.k), np64(gb.v), gb.offsets, func_c,
+                                         nfunc, gb.max_seqlen, gb.alpha)
+    check_grad(np64(dq_c), rdq, "dq_c")
+    check_grad(np64(dk), rdk, "dk")
+    check_grad(np64(dv), rdv, "dv")
+
+
+def test_dlrm_targets_only_full_size():
+    cfg = wl.CONFIGS["dlrm_b1024"]
+    gb = GpuBatch.from_config(cfg, 0, device="cuda")
+    q_c, do_c, func_c = _targets_inputs(gb)
+    o_c, dq_c, dk, dv = _run_targets(gb, q_c, do_c, func_c)
+    # forward and dq_c for every sequence: the oracle does one row each
+    ref_o = orc.fwd_targets_only(np64(q_c), np64(gb.k), np64(gb.v), gb.offsets, func_c, 1, gb.max_seqlen,
+                                 gb.alpha)
+    check_o(np64(o_c), ref_o)
+    # dk/dv on sampled sequences (full fp64 copies of dk/dv would be 2.8 GB each)
+    seqs = sample_seqs(gb.lens, 4)
+    rows, sub_off, _, (q, k, v, do) = gb.sub(seqs)
+    fc = func_c[:, seqs]
+    rdq, rdk, rdv = orc.bwd_targets_only(np64(do_c[seqs]), np64(q_c[seqs]), k, v, sub_off, fc, 1,
+                                         gb.max_seqlen, gb.alpha)
+    ridx = torch.as_tensor(rows, device="cuda")
+    check_grad(np64(dq_c[seqs]), rdq, "dq_c")
+    check_grad(np64(dk.index_select(0, ridx)), rdk, "dk")
+    check_grad(np64(dv.index_select(0, ridx)), rdv, "dv")
+
+
+def test_backward_is_bitwise_repeatable():
+    gb = GpuBatch.from_config(wl.CONFIGS["onerank_b64"], 1)
+    a = gb.run()
+    b = gb.run()
+    for n in ("o", "dq", "dk", "dv"):
+        assert torch.equal(a[n], b[n]), n
+
+
+def test_device_side_offset_error_sets_status_and_writes_nothing():
+    lens = np.array([100, 50])
+    q, k, v, do = _gen(lens, 2, 64, seed=1)
+    func = wl.build_func(wl.Config("c", 2, 0, 0, 2, 64, "causal", 1), lens, 1)
+    gb = GpuBatch(lens, func, q, k, v, do)
+    bad = torch.tensor([0, 120, 150], dtype=torch.int32, device="cuda")  # L_0 = 120 > max_seqlen 100
+    shape = hb.make_shape(2, 150, 2, 64, 1, 100, gb.alpha)
+    ws = hb.alloc_workspace(shape)
+    o = torch.full_like(gb.q, 7.0)
+    hb.fwd(gb.q, gb.k, gb.v, bad, gb.d_func, 100, gb.alpha, ws=ws, out=o)
+    assert hb.device_status(ws) == 5  # HSTU_ERR_DEVICE_INPUT
+    assert torch.all(o == 7.0)
+    # the same workspace recovers with valid offsets
+    o2 = hb.fwd(gb.q, gb.k, gb.v, gb.d_off, gb.d_func, 100, gb.alpha, ws=ws)
+    assert hb.device_status(ws) == hb.HSTU_OK
+    assert torch.isfinite(o2.float()).all()
