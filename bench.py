@@ -1,0 +1,427 @@
+#!/usr/bin/env python3
+"""Benchmark: jagged HSTU masked attention fwd+bwd on one GB300 per rank.
+
+A step is one pass of the whole hot path over one synthetic batch: the plan
+(offset validation, tile classification, longest-first work lists), the
+forward kernel and the backward kernel, all through the C ABI. The headline
+workload is the SLA mask of TorchEasyRec PR #670 at B=32, S=1024, H=4, D=128
+with NFUNC=5 (third interval padded empty); the NFUNC=3 leg of the same batch
+runs interleaved with it to give the padding overhead.
+
+Metric: useful TFLOP/s = visible (row, column) pairs x heads x (4 D forward +
+10 D backward) / step time. Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+  python bench.py --config onerank_b64|sla_b16_s2048|dlrm_b1024 ...
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "HSTU masked attn fwd+bwd ms and useful TFLOP/s (% bf16 TC peak), 1xGB300"
+UNIT = "TFLOP/s"
+DEFAULT_CONFIG = "sla_b32_s1024"
+L2_FLUSH_BYTES = 512 << 20
+
+# DRAM bytes per launch of the backward kernel from an ncu capture, with the
+# hash of the kernel sources they were taken on (the value is reported only
+# while the sources are unchanged). Filled from profiles/.
+NCU_TRAFFIC = {"bwd": None, "sources_sha": None}
+
+
+def kernel_sources_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "jagged_hstu_attention_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"bf16_tflops": float(p["bf16_tflops"]), "hbm_gbs": float(p["hbm_gbs"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"hstu_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, val in zip(names, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- GPU legs
+class Leg:
+    """One jagged batch resident on the GPU with preallocated outputs."""
+
+    def __init__(self, cfg, seed, nfunc, device, shared=None):
+        import torch
+        from jagged_hstu_attention_gb300 import binding as hb
+        from jagged_hstu_attention_gb300 import workloads as wl
+        self.hb = hb
+        if shared is None:
+            gen_dev = "cuda" if cfg.name.startswith("dlrm") else "cpu"
+            b = wl.make_batch(cfg, seed, device=gen_dev, nfunc=nfunc)
+            self.lens, self.offsets, self.func = b.lens, b.offsets, b.func
+            self.q, self.k, self.v, self.do = (t.to(device) for t in (b.q, b.k, b.v, b.do))
+        else:  # same activations, another func width
+            self.lens, self.offsets = shared.lens, shared.offsets
+            self.func = wl.build_func(cfg, self.lens, nfunc)
+            self.q, self.k, self.v, self.do = shared.q, shared.k, shared.v, shared.do
+        self.cfg, self.nfunc = cfg, nfunc
+        self.T = int(self.offsets[-1])
+        self.N = int(self.lens.max())
+        self.alpha = 1.0 / math.sqrt(cfg.dim)
+        self.d_off = torch.tensor(self.offsets, dtype=torch.int32, device=device)
+        self.d_func = torch.tensor(self.func, dtype=torch.int32, device=device)
+        self.shape = hb.make_shape(len(self.lens), self.T, cfg.heads, cfg.dim, nfunc, self.N, self.alpha)
+        self.ws = hb.alloc_workspace(self.shape, hb.WS_FULL, device)
+        self.counts = torch.empty(self.T, dtype=torch.int32, device=device)
+        self.o = torch.empty_like(self.q)
+        self.dq, self.dk, self.dv = (torch.empty_like(self.q) for _ in range(3))
+        hb.plan(self.d_off, self.d_func, self.shape, self.ws, row_counts=self.counts)
+        torch.cuda.synchronize()
+        if hb.device_status(self.ws) != hb.HSTU_OK:
+            raise RuntimeError("plan reported a device-side error")
+        self.pairs = int(self.counts.sum().item())  # visible pairs per head
+
+    def flops(self):
+        H, D = self.cfg.heads, self.cfg.dim
+        return self.pairs * H * 4 * D, self.pairs * H * 10 * D
+
+    def step(self, ev):
+        hb = self.hb
+        ev[0].record()
+        hb.plan(self.d_off, self.d_func, self.shape, self.ws)
+        ev[1].record()
+        hb.fwd(self.q, self.k, self.v, self.d_off, self.d_func, self.N, self.alpha, ws=self.ws,
+               reuse_plan=True, out=self.o)
+        ev[2].record()
+        hb.bwd(self.do, self.q, self.k, self.v, self.d_off, self.d_func, self.N, self.alpha, ws=self.ws,
+               reuse_plan=True, outs=(self.dq, self.dk, self.dv))
+        ev[3].record()
+
+
+LAUNCHES_PER_STEP = 4  # plan classify + plan sort + forward + backward
+
+
+def time_legs(legs, steps, warmup, flush):
+    import torch
+    for _ in range(warmup):
+        for leg in legs:
+            leg.step([torch.cuda.Event(enable_timing=True) for _ in range(4)])
+    torch.cuda.synchronize()
+    rec = [[] for _ in legs]
+    for _ in range(steps):
+        for li, leg in enumerate(legs):
+            flush.zero_()
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            leg.step(ev)
+            rec[li].append(ev)
+    torch.cuda.synchronize()
+    out = []
+    for evs in rec:
+        plan = [e[0].elapsed_time(e[1]) for e in evs]
+        fwd = [e[1].elapsed_time(e[2]) for e in evs]
+        bwd = [e[2].elapsed_time(e[3]) for e in evs]
+        stp = [e[0].elapsed_time(e[3]) for e in evs]
+        out.append({"plan": plan, "fwd": fwd, "bwd": bwd, "step": stp})
+    return out
+
+
+def e2e_leg(leg, steps, warmup):
+    """Same step through the C ABI from pinned HOST buffers: copies of the
+    step's inputs in, of its outputs out, inside the timed region."""
+    import torch
+    hb = leg.hb
+    pin = lambda t: t.cpu().pin_memory()
+    h_in = [pin(t) for t in (leg.q, leg.k, leg.v, leg.do, leg.d_off, leg.d_func)]
+    h_out = [torch.empty(leg.q.shape, dtype=leg.q.dtype).pin_memory() for _ in range(4)]
+    d_in = [torch.empty_like(t, device="cuda") for t in h_in]
+    d_out = [torch.empty_like(leg.q) for _ in range(4)]
+    h2d = sum(t.numel() * t.element_size() for t in h_in)
+    d2h = sum(t.numel() * t.element_size() for t in h_out)
+
+    def one():
+        for d, h in zip(d_in, h_in):
+            d.copy_(h, non_blocking=True)
+        q, k, v, do, off, func = d_in
+        hb.plan(off, func, leg.shape, leg.ws)
+        hb.fwd(q, k, v, off, func, leg.N, leg.alpha, ws=leg.ws, reuse_plan=True, out=d_out[0])
+        hb.bwd(do, q, k, v, off, func, leg.N, leg.alpha, ws=leg.ws, reuse_plan=True, outs=tuple(d_out[1:]))
+        for h, d in zip(h_out, d_out):
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        one()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    return ms, h2d, d2h
+
+
+# ---------------------------------------------------------------- CPU oracle
+def oracle_sample(cfg, seed, budget_s, min_seqs=1, max_seqs=None):
+    """Times the fp64 oracle (as it stands) on whole sequences of the workload
+    until the time budget is spent; returns (useful flops, seconds, seqs)."""
+    import torch
+    import oracle.hstu_oracle as orc
+    from jagged_hstu_attention_gb300 import workloads as wl
+    lens = wl.lengths(cfg, seed)
+    N = int(lens.max())
+    alpha = 1.0 / math.sqrt(cfg.dim)
+    order = np.argsort(-lens, kind="stable")
+    g = torch.Generator().manual_seed(seed)
+    flops = 0.0
+    secs = 0.0
+    done = 0
+    limit = max_seqs if max_seqs is not None else len(lens)
+    for b in order[:limit]:
+        L = int(lens[b])
+        f = wl.func_rows(cfg, L)
+        shape = (L, cfg.heads, cfg.dim)
+        q, k, v, do = (wl.randn_bf16(shape, g).float().numpy().astype(np.float64) for _ in range(4))
+        off = np.array([0, L])
+        t0 = time.perf_counter()
+        orc.fwd_dense(q, k, v, off, f, cfg.nfunc, N, alpha)
+        orc.bwd_dense(do, q, k, v, off, f, cfg.nfunc, N, alpha)
+        secs += time.perf_counter() - t0
+        pairs = int(orc.visible_counts(off, f, cfg.nfunc).sum())
+        flops += pairs * cfg.heads * 14 * cfg.dim
+        done += 1
+        if done >= min_seqs and secs >= budget_s:
+            break
+    return flops, secs, done, len(lens)
+
+
+def cpu_cores():
+    try:
+        from threadpoolctl import threadpool_info
+        n = max((i.get("num_threads", 0) for i in threadpool_info()), default=0)
+        if n:
+            return int(n)
+    except Exception:
+        pass
+    return os.cpu_count()
+
+
+# ---------------------------------------------------------------- main
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def run_reference(args, cfg):
+    """The oracle as it stands on the host cores (bounded sample per step)."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    times, flops_all = [], []
+    per_step_budget = 4.0
+    for i in range(args.warmup + args.steps):
+        f, s, n, nb = oracle_sample(cfg, args.seed, per_step_budget, max_seqs=1)
+        if i >= args.warmup:
+            times.append(s)
+            flops_all.append(f)
+    value = sum(flops_all) / sum(times) / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": cfg.name, "batch": cfg.batch, "seq_len": cfg.len_hi,
+                                            "heads": cfg.heads, "head_dim": cfg.dim, "nfunc": cfg.nfunc},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                             "sample": f"1 of {cfg.batch} sequences (the longest) per step, all heads, "
+                                       "fwd+bwd, dense fp64 numpy"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default=DEFAULT_CONFIG)
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    from jagged_hstu_attention_gb300 import workloads as wl
+    cfg = wl.CONFIGS[args.config]
+    if args.impl == "reference":
+        run_reference(args, cfg)
+        return
+
+    import torch
+    import torch.distributed as dist
+    world, rank, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    from jagged_hstu_attention_gb300 import build_ext
+    build_ext.build()
+    from jagged_hstu_attention_gb300 import binding as hb
+    hb.load()
+
+    # Each rank runs its own batch (seed + rank): independent sequences, no
+    # data-path collective; weak scaling.
+    seed = args.seed + rank
+    leg_main = Leg(cfg, seed, cfg.nfunc, device)
+    legs = [leg_main]
+    if cfg.mask == "sla" and cfg.nfunc == 5:
+        legs.append(Leg(cfg, seed, 3, device, shared=leg_main))
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+
+    sampler = ClockSampler(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    wall0 = time.perf_counter()
+    res = time_legs(legs, args.steps, args.warmup, flush)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop()
+    if world > 1:
+        dist.barrier()
+
+    r = res[0]
+    ms_step = statistics.mean(r["step"])
+    ms_tensor = torch.tensor([ms_step], device=device)
+    if world > 1:
+        dist.all_reduce(ms_tensor, op=dist.ReduceOp.MAX)
+    ms_max = float(ms_tensor.item())
+    f_fwd, f_bwd = leg_main.flops()
+    useful = f_fwd + f_bwd
+    value = useful * world / (ms_max * 1e-3) / 1e12
+
+    e2e_ms, h2d, d2h = e2e_leg(leg_main, max(3, args.steps // 2), 2)
+    e2e_val = useful * world / (e2e_ms * 1e-3) / 1e12
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    peaks = load_peaks()
+    ms_bwd = statistics.mean(r["bwd"])
+    achieved = f_bwd / (ms_bwd * 1e-3) / 1e12
+    sha = kernel_sources_sha()
+    traffic = NCU_TRAFFIC["bwd"] if NCU_TRAFFIC["sources_sha"] == sha else None
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": cfg.name, "batch": cfg.batch, "seq_len": cfg.len_hi if cfg.len_lo == cfg.len_hi
+                   else f"U[{cfg.len_lo},{cfg.len_hi}]", "heads": cfg.heads, "head_dim": cfg.dim,
+                   "nfunc": cfg.nfunc, "mask": cfg.mask, "total_tokens": leg_main.T,
+                   "parallelism": f"replicas{world}" if world > 1 else "single", "l2": "flushed between steps"},
+        "pct_of_bf16_peak": 100.0 * value / world / peaks["bf16_tflops"],
+        "breakdown_ms": {k: statistics.mean(r[k]) for k in ("plan", "fwd", "bwd")},
+        "useful_gflop_per_step": useful / 1e9,
+        "gpu_launches": LAUNCHES_PER_STEP * args.steps * len(legs),
+        "roofline": {"kernel": "hstu_bwd_kernel", "bound": "tensor", "achieved": achieved,
+                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": achieved / peaks["bf16_tflops"], "traffic": traffic,
+                     "peak_source": peaks["source"] + " burst bf16"},
+        "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms},
+        "clocks": clocks,
+        "wall_s_timed_region": wall,
+    }
+    if len(legs) > 1:
+        ms3 = statistics.mean(res[1]["step"])
+        line["nfunc3"] = {"ms_per_step": ms3, "breakdown_ms": {k: statistics.mean(res[1][k])
+                                                               for k in ("plan", "fwd", "bwd")},
+                          "padding_overhead_pct": 100.0 * (ms_step - ms3) / ms3}
+    if not args.no_cpu_baseline:
+        f, s, n, nb = oracle_sample(cfg, seed, args.cpu_budget)
+        line["cpu_baseline"] = {"value": f / s / 1e12, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                                "sample": f"{n} of {nb} sequences (longest first), all heads, fwd+bwd, "
+                                          f"dense fp64 numpy, {s:.1f} s"}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -19,8 +19,16 @@
 // 10 D flops per pair) in exchange for a deterministic dQ with no fp32
 // workspace and no reduce-add traffic.
 //
-// Warps: 0-3 epilogue (one thread per TMEM lane), 4 TMA producer, 5 TMEM owner
-// and MMA issuer.
+// Warps: 0-7 epilogue (warp w: TMEM lanes 32(w%4).., column half w/4), 8 TMA
+// producer, 9 TMEM owner and MMA issuer. Each half packs its bf16 results in
+// place over the first 32 columns of its own 64 (K-steps 0-3 of the next MMA
+// read columns [0,32), K-steps 4-7 read [64,96)).
+//
+// Partial-tile masks of the dK/dV role are built by transposition: each warp
+// holds 32 q rows of the visiting q tile, computes each row's visible-column
+// bits over its 64 kv columns from the row's intervals, and one ballot per kv
+// column turns them into that column's 32-row word. The cost does not depend
+// on the number of intervals, so empty padded intervals stay free.
 #include "common.cuh"
 #include "internal.h"
 
@@ -43,9 +51,9 @@ struct BwdSmem {
   int n_tiles;
   int16_t tile_idx[kMaxTiles];
   uint8_t tile_c[kMaxTiles];
-  // dK/dV role: intervals of the current q tile's rows (double buffered).
-  int32_t flo[2][kMaxIntervals][kBlock];
-  int32_t fhi[2][kMaxIntervals][kBlock];
+  // dK/dV role: per partial q tile, colmask[c][j] bit e = q row 32c+e sees
+  // kv column j of the tile (double buffered).
+  uint32_t colmask[2][4][kBlock];
 };
 
 template <typename S>
@@ -69,22 +77,23 @@ __device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const uint32_t (
   for (int e = 0; e < 4; ++e) d4[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
 }
 
-// Writes TMEM columns [col, col + DP) of this thread's lane (or zeros) as a
-// bf16 row of `dim` elements.
+// Writes this warp's half of TMEM columns [taddr, taddr + DP) of its lane (or
+// zeros) into a bf16 row of `dim` elements.
 template <int DP>
-__device__ __forceinline__ void store_acc_row(uint32_t taddr, bool have, bool valid,
-                                              __nv_bfloat16* dst, int dim) {
+__device__ __forceinline__ void store_acc_half(uint32_t taddr, int half, bool have, bool valid,
+                                               __nv_bfloat16* dst, int dim) {
 #pragma unroll
-  for (int c = 0; c < DP / 32; ++c) {
+  for (int c = 0; c < DP / 64; ++c) {
+    const int col = half * (DP / 2) + c * 32;
     uint32_t a[32];
     if (have) {
-      tmem_ld32(taddr + c * 32, a);
+      tmem_ld32(taddr + col, a);
       tmem_ld_wait(a);
     } else {
 #pragma unroll
       for (int e = 0; e < 32; ++e) a[e] = 0u;
     }
-    if (valid && c * 32 < dim) store_row32(dst + c * 32, a);
+    if (valid && col < dim) store_row32(dst + col, a);
   }
 }
 
@@ -109,10 +118,10 @@ __device__ __forceinline__ void bwd_role(const AttnParams& p, BwdSmem<DP>& s, bo
       mbar_init(smem_u32(&s.bar_empty[i]), 1);
     }
     mbar_init(smem_u32(&s.bar_s_full), 1);
-    mbar_init(smem_u32(&s.bar_p_full), 128);
+    mbar_init(smem_u32(&s.bar_p_full), 256);
     mbar_init(smem_u32(&s.bar_acc), 1);
-    mbar_init(smem_u32(&s.bar_func[0]), 128);
-    mbar_init(smem_u32(&s.bar_func[1]), 128);
+    mbar_init(smem_u32(&s.bar_func[0]), 256);
+    mbar_init(smem_u32(&s.bar_func[1]), 256);
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -134,7 +143,7 @@ __device__ __forceinline__ void bwd_role(const AttnParams& p, BwdSmem<DP>& s, bo
     }
     if (lane == 0) s.n_tiles = n;
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(smem_u32(&s.tmem_base), 512);
     tmem_relinquish();
   }
@@ -161,7 +170,7 @@ __device__ __forceinline__ void bwd_role(const AttnParams& p, BwdSmem<DP>& s, bo
   const CUtensorMap* m_str0 = dkdv ? &p.tm_q : &p.tm_k;
   const CUtensorMap* m_str1 = dkdv ? &p.tm_do : &p.tm_v;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------------ producer
     if (nt > 0 && elect_one_sync()) {
       int last_use[2] = {-1, -1};
@@ -188,7 +197,7 @@ __device__ __forceinline__ void bwd_role(const AttnParams& p, BwdSmem<DP>& s, bo
         if (last_use[st] >= 0) mbar_wait_drain(smem_u32(&s.bar_full[st]), last_use[st] & 1);
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (nt > 0 && elect_one_sync()) {
       constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
@@ -222,17 +231,19 @@ __device__ __forceinline__ void bwd_role(const AttnParams& p, BwdSmem<DP>& s, bo
 #pragma unroll
           for (int kk = 0; kk < kBlock / 16; ++kk) {
             const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
-            umma_ts(t_acc0, tS + kk * 8, sdesc_sw128(s1 + kk * 16 * 128, kChunkBytes, 1024),
+            const uint32_t acol = (kk >> 2) * 64 + (kk & 3) * 8;
+            umma_ts(t_acc0, tS + acol, sdesc_sw128(s1 + kk * 16 * 128, kChunkBytes, 1024),
                     idesc_acc, acc);
-            umma_ts(t_acc1, tdP + kk * 8, sdesc_sw128(s0 + kk * 16 * 128, kChunkBytes, 1024),
+            umma_ts(t_acc1, tdP + acol, sdesc_sw128(s0 + kk * 16 * 128, kChunkBytes, 1024),
                     idesc_acc, acc);
           }
         } else {
           // dQ += dS K (K = str0, MN-major)
 #pragma unroll
           for (int kk = 0; kk < kBlock / 16; ++kk) {
-            umma_ts(t_dq, tS + kk * 8, sdesc_sw128(s0 + kk * 16 * 128, kChunkBytes, 1024),
-                    idesc_acc, (it > 0 || kk > 0) ? 1u : 0u);
+            umma_ts(t_dq, tS + (kk >> 2) * 64 + (kk & 3) * 8,
+                    sdesc_sw128(s0 + kk * 16 * 128, kChunkBytes, 1024), idesc_acc,
+                    (it > 0 || kk > 0) ? 1u : 0u);
           }
         }
         umma_commit(smem_u32(&s.bar_empty[st]));
@@ -243,32 +254,43 @@ __device__ __forceinline__ void bwd_role(const AttnParams& p, BwdSmem<DP>& s, bo
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    const int r = threadIdx.x;  // TMEM lane: kv row (dK/dV role) or q row (dQ role)
+    const int quarter = warp & 3, half = warp >> 2;
+    const int r = quarter * 32 + lane;  // TMEM lane: kv row (dK/dV role) or q row (dQ role)
     const int own_loc = tile * kBlock + r;
     const bool valid = own_loc < L;
-    const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
-    const float alpha = p.alpha, c1 = p.alpha * p.inv_n;  // c1: alpha/N
+    const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+    const SiluConsts kc(p.alpha, p.inv_n);
+    const int hc = half * 64;  // first S column of this warp's half
     int lo[NINT], hi[NINT];
     if (!dkdv)
       load_row_intervals<NINT>(p.func, p.total, static_cast<int64_t>(o0) + own_loc, L, valid, lo, hi);
     bool ok = true;
-    int fu = 0;  // partial tiles seen so far (dK/dV role): selects the interval buffer
+    int fu = 0;  // partial tiles seen so far (dK/dV role): selects the mask buffer
     for (int it = 0; it < nt; ++it) {
       const int other = s.tile_idx[it];
       const bool partial = s.tile_c[it] == kPartial;
       const int buf = fu & 1;
       if (dkdv && partial) {
-        // Intervals of the visiting q tile's rows, shared by the 128 threads.
-        int flo_r[NINT], fhi_r[NINT];
+        // This warp's 32 q rows of the visiting q tile; their visible bits
+        // over kv columns [hc, hc + 64) of tile `tile`, transposed by ballot.
+        int flo[NINT], fhi[NINT];
         const int qi = other * kBlock + r;
-        load_row_intervals<NINT>(p.func, p.total, static_cast<int64_t>(o0) + qi, L, qi < L, flo_r,
-                                 fhi_r);
+        load_row_intervals<NINT>(p.func, p.total, static_cast<int64_t>(o0) + qi, L, qi < L, flo, fhi);
+        const uint32_t w0 = row_mask_word<NINT>(flo, fhi, tile * kBlock + hc);
+        const uint32_t w1 = row_mask_word<NINT>(flo, fhi, tile * kBlock + hc + 32);
+        uint32_t mine0 = 0, mine1 = 0;
 #pragma unroll
-        for (int t = 0; t < NINT; ++t) {
-          s.flo[buf][t][r] = flo_r[t];
-          s.fhi[buf][t][r] = fhi_r[t];
+        for (int j = 0; j < 32; ++j) {
+          const uint32_t b0 = __ballot_sync(0xffffffffu, (w0 >> j) & 1u);
+          const uint32_t b1 = __ballot_sync(0xffffffffu, (w1 >> j) & 1u);
+          if (lane == j) {
+            mine0 = b0;
+            mine1 = b1;
+          }
         }
-        // Bounded hand-off between the 128 epilogue threads (an mbarrier, not
+        s.colmask[buf][quarter][hc + lane] = mine0;
+        s.colmask[buf][quarter][hc + 32 + lane] = mine1;
+        // Bounded hand-off between the 256 epilogue threads (an mbarrier, not
         // bar.sync, so that an aborting warp cannot strand the others).
         mbar_arrive(smem_u32(&s.bar_func[buf]));
         if (!warp_wait_b(smem_u32(&s.bar_func[buf]), (fu >> 1) & 1, abort_flag)) { ok = false; break; }
@@ -278,51 +300,35 @@ __device__ __forceinline__ void bwd_role(const AttnParams& p, BwdSmem<DP>& s, bo
       tc_fence_after();
       const int col0 = other * kBlock;  // dQ role: first kv column of the tile
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
+        const int chunk = 2 * half + c;  // 32-column chunk of S / dP
         uint32_t sv[32], dv[32];
-        tmem_ld32(tS + lane_addr + c * 32, sv);
-        tmem_ld32(tdP + lane_addr + c * 32, dv);
+        tmem_ld32(tS + lane_addr + chunk * 32, sv);
+        tmem_ld32(tdP + lane_addr + chunk * 32, dv);
         tmem_ld_wait(sv);
         tmem_ld_wait(dv);
         uint32_t mask = 0xffffffffu;
-        if (partial) {
-          if (dkdv) {
-            mask = 0;
-#pragma unroll 8
-            for (int e = 0; e < 32; ++e) {
-              const int qi = c * 32 + e;
-              bool vis = false;
-#pragma unroll
-              for (int t = 0; t < NINT; ++t)
-                vis |= (s.flo[buf][t][qi] <= own_loc) && (own_loc < s.fhi[buf][t][qi]);
-              mask |= static_cast<uint32_t>(vis) << e;
-            }
-          } else {
-            mask = row_mask_word<NINT>(lo, hi, col0 + c * 32);
-          }
-        }
+        if (partial) mask = dkdv ? s.colmask[buf][chunk][r] : row_mask_word<NINT>(lo, hi, col0 + chunk * 32);
         uint32_t pp[16], pd[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           float g[2], pv[2];
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
-            const float sc = __uint_as_float(sv[e + u]);
-            const float x = alpha * sc;
-            const float sg = sigmoidf_fast(x);
-            const float dsilu = sg * (1.0f + x * (1.0f - sg));
+            silu_p_g(__uint_as_float(sv[e + u]), __uint_as_float(dv[e + u]), kc, pv[u], g[u]);
             const bool on = (mask >> (e + u)) & 1u;
-            pv[u] = on ? c1 * sc * sg : 0.0f;
-            g[u] = on ? __uint_as_float(dv[e + u]) * dsilu * c1 : 0.0f;
+            pv[u] = on ? pv[u] : 0.0f;
+            g[u] = on ? g[u] : 0.0f;
           }
           pp[e / 2] = pack_bf16x2(pv[0], pv[1]);
           pd[e / 2] = pack_bf16x2(g[0], g[1]);
         }
+        const uint32_t dst = lane_addr + hc + c * 16;
         if (dkdv) {
-          tmem_st16(tS + lane_addr + c * 16, pp);
-          tmem_st16(tdP + lane_addr + c * 16, pd);
+          tmem_st16(tS + dst, pp);
+          tmem_st16(tdP + dst, pd);
         } else {
-          tmem_st16(tS + lane_addr + c * 16, pd);
+          tmem_st16(tS + dst, pd);
         }
       }
       tmem_st_wait();
@@ -334,17 +340,17 @@ __device__ __forceinline__ void bwd_role(const AttnParams& p, BwdSmem<DP>& s, bo
     if (ok && !*abort_flag) {
       const int64_t row = static_cast<int64_t>(row0 + r) * p.heads + h;
       if (dkdv) {
-        store_acc_row<DP>(t_acc0 + lane_addr, nt > 0, valid, p.out2 + row * p.dim, p.dim);  // dV
-        store_acc_row<DP>(t_acc1 + lane_addr, nt > 0, valid, p.out1 + row * p.dim, p.dim);  // dK
+        store_acc_half<DP>(t_acc0 + lane_addr, half, nt > 0, valid, p.out2 + row * p.dim, p.dim);  // dV
+        store_acc_half<DP>(t_acc1 + lane_addr, half, nt > 0, valid, p.out1 + row * p.dim, p.dim);  // dK
       } else {
-        store_acc_row<DP>(t_dq + lane_addr, nt > 0, valid, p.out0 + row * p.dim, p.dim);  // dQ
+        store_acc_half<DP>(t_dq + lane_addr, half, nt > 0, valid, p.out0 + row * p.dim, p.dim);  // dQ
       }
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tbase, 512);
   }
@@ -352,7 +358,7 @@ __device__ __forceinline__ void bwd_role(const AttnParams& p, BwdSmem<DP>& s, bo
 }
 
 template <int DP, int NINT>
-__global__ void __launch_bounds__(192, 1) hstu_bwd_kernel(const __grid_constant__ AttnParams p) {
+__global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant__ AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   BwdSmem<DP>& s = smem_as_b<BwdSmem<DP>>(smem_raw);
   const int item = blockIdx.x / p.heads, h = blockIdx.x - item * p.heads;
@@ -376,7 +382,7 @@ static cudaError_t launch_bwd_t(const AttnParams& p, int grid_items, cudaStream_
   }
   const long long ctas = 2LL * grid_items * p.heads;
   if (ctas <= 0) return cudaSuccess;
-  hstu_bwd_kernel<DP, NINT><<<static_cast<unsigned>(ctas), 192, smem, stream>>>(p);
+  hstu_bwd_kernel<DP, NINT><<<static_cast<unsigned>(ctas), 320, smem, stream>>>(p);
   return cudaGetLastError();
 }
 

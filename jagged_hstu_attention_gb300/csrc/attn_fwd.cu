@@ -1,18 +1,22 @@
 // Forward kernel: one CTA per (work item = sequence b, q tile qt) and head h.
 //
-//   warp 4      TMA producer: Q tile once, then K/V tiles of every visited kv
+//   warp 8      TMA producer: Q tile once, then K/V tiles of every visited kv
 //               tile into a 2-stage ring.
-//   warp 5      TMEM owner and MMA issuer (one elected lane):
+//   warp 9      TMEM owner and MMA issuer (one elected lane):
 //                 S[it % 2] = Q K^T             (tcgen05, SMEM x SMEM)
 //                 O        += P[it % 2] V       (tcgen05, TMEM x SMEM)
 //               S for tile it+1 is issued before P of tile it is consumed, so
 //               the tensor core works while the epilogue computes P.
-//   warps 0-3   epilogue, one thread per q row (= TMEM lane): load S, apply
-//               P = silu(alpha S) / N (and the row's interval mask on partial
-//               tiles only), pack P to bf16 in place over the S columns, and
-//               finally O -> bf16 -> global with rows past L_b left alone.
+//   warps 0-7   epilogue. Warp w reads TMEM lanes 32(w%4).. (q rows) and the
+//               column half w/4 of S: P = silu(alpha S) / N with the row's
+//               interval mask on partial tiles only, packed to bf16 in place
+//               over the first 32 columns of its own half (so the two halves
+//               never touch each other's columns); at the end O -> bf16 ->
+//               global, rows past L_b left alone. Two warps per SM
+//               sub-partition hide the MUFU and TMEM latencies.
 //
-// TMEM (512 columns): S0 [0,128), S1 [128,256), O [256, 256+DP).
+// TMEM (512 columns): S0 [0,128), S1 [128,256), O [256, 256+DP). Packed P of
+// buffer b: K-steps 0-3 at columns [128b, 128b+32), 4-7 at [128b+64, 128b+96).
 // SMEM: Q (DP/64 chunks of 128 rows x 128 B, 128-byte swizzle), K and V
 // stages of the same shape.
 #include "common.cuh"
@@ -47,15 +51,14 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
   return __all_sync(0xffffffffu, ok);
 }
 
-// P = silu(alpha s) / N = (alpha/N) * s * sigmoid(alpha s) for 32 columns,
-// masked by bit k of `mask`, packed to 16 bf16x2 words.
-__device__ __forceinline__ void silu_pack32(const uint32_t (&s)[32], uint32_t mask, float alpha,
-                                            float c1, uint32_t (&pk)[16]) {
+// P = silu(alpha s) / N for 32 columns, masked by bit k of `mask`, packed to
+// 16 bf16x2 words.
+__device__ __forceinline__ void silu_pack32(const uint32_t (&s)[32], uint32_t mask,
+                                            const SiluConsts& kc, uint32_t (&pk)[16]) {
 #pragma unroll
   for (int e = 0; e < 32; e += 2) {
-    const float s0 = __uint_as_float(s[e]), s1 = __uint_as_float(s[e + 1]);
-    float p0 = c1 * s0 * sigmoidf_fast(alpha * s0);
-    float p1 = c1 * s1 * sigmoidf_fast(alpha * s1);
+    float p0 = silu_p(__uint_as_float(s[e]), kc);
+    float p1 = silu_p(__uint_as_float(s[e + 1]), kc);
     p0 = ((mask >> e) & 1u) ? p0 : 0.0f;
     p1 = ((mask >> (e + 1)) & 1u) ? p1 : 0.0f;
     pk[e / 2] = pack_bf16x2(p0, p1);
@@ -63,7 +66,7 @@ __device__ __forceinline__ void silu_pack32(const uint32_t (&s)[32], uint32_t ma
 }
 
 template <int DP, int NINT>
-__global__ void __launch_bounds__(192, 1) hstu_fwd_kernel(const __grid_constant__ AttnParams p) {
+__global__ void __launch_bounds__(320, 1) hstu_fwd_kernel(const __grid_constant__ AttnParams p) {
   using Smem = FwdSmem<DP>;
   extern __shared__ uint8_t smem_raw[];
   Smem& s = smem_as<Smem>(smem_raw);
@@ -85,7 +88,7 @@ __global__ void __launch_bounds__(192, 1) hstu_fwd_kernel(const __grid_constant_
       mbar_init(smem_u32(&s.bar_kv_full[i]), 1);
       mbar_init(smem_u32(&s.bar_kv_empty[i]), 1);
       mbar_init(smem_u32(&s.bar_s_full[i]), 1);
-      mbar_init(smem_u32(&s.bar_p_full[i]), 128);
+      mbar_init(smem_u32(&s.bar_p_full[i]), 256);
     }
     mbar_init(smem_u32(&s.bar_o_full), 1);
     fence_mbar_init();
@@ -105,7 +108,7 @@ __global__ void __launch_bounds__(192, 1) hstu_fwd_kernel(const __grid_constant_
     }
     if (lane == 0) s.n_tiles = n;
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(smem_u32(&s.tmem_base), 512);
     tmem_relinquish();
   }
@@ -119,7 +122,7 @@ __global__ void __launch_bounds__(192, 1) hstu_fwd_kernel(const __grid_constant_
   constexpr int kTile = Smem::kTile;
   constexpr int kChunkBytes = kBlock * 128;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------------ producer
     if (nt > 0 && elect_one_sync()) {
       int last_use[2] = {-1, -1};
@@ -144,7 +147,7 @@ __global__ void __launch_bounds__(192, 1) hstu_fwd_kernel(const __grid_constant_
         if (last_use[st] >= 0) mbar_wait_drain(smem_u32(&s.bar_kv_full[st]), last_use[st] & 1);
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (nt > 0 && elect_one_sync()) {
       constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
@@ -173,7 +176,7 @@ __global__ void __launch_bounds__(192, 1) hstu_fwd_kernel(const __grid_constant_
           const uint32_t v_base = smem_u32(s.v[pst]);
 #pragma unroll
           for (int kk = 0; kk < kBlock / 16; ++kk) {
-            umma_ts(tbase + 256, tbase + pst * 128 + kk * 8,
+            umma_ts(tbase + 256, tbase + pst * 128 + (kk >> 2) * 64 + (kk & 3) * 8,
                     sdesc_sw128(v_base + kk * 16 * 128, kChunkBytes, 1024), idesc_o,
                     (pi > 0 || kk > 0) ? 1u : 0u);
           }
@@ -187,39 +190,38 @@ __global__ void __launch_bounds__(192, 1) hstu_fwd_kernel(const __grid_constant_
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    const int r = threadIdx.x;  // q row within the tile == TMEM lane
+    const int quarter = warp & 3, half = warp >> 2;
+    const int r = quarter * 32 + lane;  // q row within the tile == TMEM lane
     const int i_loc = qt * kBlock + r;
     const bool valid = i_loc < L;
     int lo[NINT], hi[NINT];
     load_row_intervals<NINT>(p.func, p.total, static_cast<int64_t>(o0) + i_loc, L, valid, lo, hi);
-    const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
-    const float alpha = p.alpha, c1 = p.alpha * p.inv_n;
+    const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+    const SiluConsts kc(p.alpha, p.inv_n);
+    const int hc = half * 64;  // first S column of this warp's half
     bool ok = true;
     for (int it = 0; it < nt; ++it) {
       const int st = it & 1, use = it >> 1;
       if (!warp_wait(smem_u32(&s.bar_s_full[st]), use & 1, abort_flag)) { ok = false; break; }
       tc_fence_after();
-      const int col0 = s.tile_j[it] * kBlock;
+      const int col0 = s.tile_j[it] * kBlock + hc;
       const bool partial = s.tile_c[it] == kPartial;
-      const uint32_t sb = tbase + lane_addr + st * 128;
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t a[32], c[32];
-        tmem_ld32(sb + half * 64, a);
-        tmem_ld32(sb + half * 64 + 32, c);
-        tmem_ld_wait(a);
-        tmem_ld_wait(c);
-        uint32_t m0 = 0xffffffffu, m1 = 0xffffffffu;
-        if (partial) {
-          m0 = row_mask_word<NINT>(lo, hi, col0 + half * 64);
-          m1 = row_mask_word<NINT>(lo, hi, col0 + half * 64 + 32);
-        }
-        uint32_t pa[16], pc[16];
-        silu_pack32(a, m0, alpha, c1, pa);
-        silu_pack32(c, m1, alpha, c1, pc);
-        tmem_st16(sb + half * 32, pa);
-        tmem_st16(sb + half * 32 + 16, pc);
+      const uint32_t sb = tbase + lane_addr + st * 128 + hc;
+      uint32_t a[32], c[32];
+      tmem_ld32(sb, a);
+      tmem_ld32(sb + 32, c);
+      tmem_ld_wait(a);
+      tmem_ld_wait(c);
+      uint32_t m0 = 0xffffffffu, m1 = 0xffffffffu;
+      if (partial) {
+        m0 = row_mask_word<NINT>(lo, hi, col0);
+        m1 = row_mask_word<NINT>(lo, hi, col0 + 32);
       }
+      uint32_t pa[16], pc[16];
+      silu_pack32(a, m0, kc, pa);
+      silu_pack32(c, m1, kc, pc);
+      tmem_st16(sb, pa);
+      tmem_st16(sb + 16, pc);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(smem_u32(&s.bar_p_full[st]));
@@ -227,23 +229,25 @@ __global__ void __launch_bounds__(192, 1) hstu_fwd_kernel(const __grid_constant_
     if (ok && nt > 0) ok = warp_wait(smem_u32(&s.bar_o_full), 0, abort_flag);
     tc_fence_after();
     if (ok && !*abort_flag) {
+      constexpr int kHalfCols = DP / 2;
       __nv_bfloat16* dst = p.out0 + (static_cast<int64_t>(q_row0 + r) * p.heads + h) * p.dim;
 #pragma unroll
-      for (int c = 0; c < DP / 32; ++c) {
-        uint32_t a[32];
+      for (int cc = 0; cc < kHalfCols / 32; ++cc) {
+        const int col = half * kHalfCols + cc * 32;
+        uint32_t v32[32];
         if (nt > 0) {
-          tmem_ld32(tbase + lane_addr + 256 + c * 32, a);
-          tmem_ld_wait(a);
+          tmem_ld32(tbase + lane_addr + 256 + col, v32);
+          tmem_ld_wait(v32);
         } else {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) a[e] = 0u;
+          for (int e = 0; e < 32; ++e) v32[e] = 0u;
         }
-        if (valid && c * 32 < p.dim) {
+        if (valid && col < p.dim) {
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e)
-            pk[e] = pack_bf16x2(__uint_as_float(a[2 * e]), __uint_as_float(a[2 * e + 1]));
-          uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+            pk[e] = pack_bf16x2(__uint_as_float(v32[2 * e]), __uint_as_float(v32[2 * e + 1]));
+          uint4* d4 = reinterpret_cast<uint4*>(dst + col);
 #pragma unroll
           for (int e = 0; e < 4; ++e)
             d4[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
@@ -254,7 +258,7 @@ __global__ void __launch_bounds__(192, 1) hstu_fwd_kernel(const __grid_constant_
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tbase, 512);
   }
@@ -273,7 +277,7 @@ static cudaError_t launch_fwd_t(const AttnParams& p, int grid_items, cudaStream_
   }
   const long long ctas = static_cast<long long>(grid_items) * p.heads;
   if (ctas <= 0) return cudaSuccess;
-  hstu_fwd_kernel<DP, NINT><<<static_cast<unsigned>(ctas), 192, smem, stream>>>(p);
+  hstu_fwd_kernel<DP, NINT><<<static_cast<unsigned>(ctas), 320, smem, stream>>>(p);
   return cudaGetLastError();
 }
 

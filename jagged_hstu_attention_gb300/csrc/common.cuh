@@ -86,7 +86,7 @@ struct PlanParams {
   int32_t batch, nfunc, nt, max_seqlen;
 };
 
-struct alignas(64) AttnParams {
+struct AttnParams {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;
   const int32_t* seq_offsets;
   const int32_t* func;
@@ -158,6 +158,43 @@ __device__ __forceinline__ uint32_t row_mask_word(const int (&lo)[NINT], const i
 // ---------------------------------------------------------------- SiLU math
 __device__ __forceinline__ float sigmoidf_fast(float x) {
   return __fdividef(1.0f, 1.0f + __expf(-x));
+}
+
+// Hardware tanh (one MUFU op, max relative error about 2^-11).
+__device__ __forceinline__ float tanh_approx(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Epilogue arithmetic on one S element s, with t = tanh(alpha s / 2) so that
+// sigmoid(alpha s) = (1 + t) / 2 (one MUFU op per element):
+//   p  = silu(alpha s) / N = u + u t,            u = s * alpha / (2N)
+//   silu'(x) = sigmoid(x) + x sigmoid(x)(1 - sigmoid(x))
+//            = (1 + t)/2 + (alpha s / 4)(1 - t^2)
+struct SiluConsts {
+  float half_alpha;     // alpha / 2
+  float quarter_alpha;  // alpha / 4
+  float half_c;         // alpha / (2N)
+  float c;              // alpha / N
+  __device__ __forceinline__ SiluConsts(float alpha, float inv_n)
+      : half_alpha(0.5f * alpha), quarter_alpha(0.25f * alpha), half_c(0.5f * alpha * inv_n),
+        c(alpha * inv_n) {}
+};
+__device__ __forceinline__ float silu_p(float s, const SiluConsts& k) {
+  const float t = tanh_approx(k.half_alpha * s);
+  const float u = k.half_c * s;
+  return fmaf(u, t, u);
+}
+// p and g = dp * silu'(alpha s) * alpha / N.
+__device__ __forceinline__ void silu_p_g(float s, float dp, const SiluConsts& k, float& p, float& g) {
+  const float t = tanh_approx(k.half_alpha * s);
+  const float u = k.half_c * s;
+  p = fmaf(u, t, u);
+  const float sg = fmaf(0.5f, t, 0.5f);
+  const float w = fmaf(-t, t, 1.0f);
+  const float dsilu = fmaf(k.quarter_alpha * s, w, sg);
+  g = (dp * k.c) * dsilu;
 }
 
 }  // namespace hstu
