@@ -141,6 +141,37 @@ HSTU_API hstu_status_t hstu_attn_bwd_targets_only(const void* dout_c, const void
                                          const hstu_attn_shape_t* shape, void* ws,
                                          size_t ws_bytes, void* stream);
 
+/* Scratch capacity of hstu_attn_fwd_noalloc, in bytes (8 MiB). */
+#define HSTU_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+
+/* Forward pass that allocates nothing and takes no workspace. The pages have
+ * no counterpart: it is an addition of this library for callers that cannot
+ * allocate device memory -- a serving runtime or host framework that reserves
+ * all device memory up front and forbids allocation on the request path, or
+ * a caller for whom cudaMalloc would synchronise the device or fail because
+ * the memory is already spoken for. Arguments and result are those of
+ * hstu_attn_fwd (the plan is always rebuilt). The plan's scratch is a fixed
+ * array of HSTU_NOALLOC_SCRATCH_BYTES compiled into the library; every GPU
+ * that loads the library holds it until the process exits.
+ *   - A shape whose plan needs more than HSTU_NOALLOC_SCRATCH_BYTES (see
+ *     hstu_attn_workspace_size with HSTU_WS_FULL) returns HSTU_ERR_WORKSPACE
+ *     and enqueues nothing.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - No cudaMalloc, cudaFree or allocating library routine is called.
+ *   - All calls on a device share the array, which keeps the last call's
+ *     contents; each call clears what must start at zero. Calls whose work
+ *     overlaps on the GPU (for example on two streams at once) race on it.
+ *   - Device-side input errors are read with
+ *     hstu_attn_get_device_status(ws) where ws is that array; there is no
+ *     handle to it, so this entry point is for callers that validate
+ *     seq_offsets themselves. */
+HSTU_API hstu_status_t hstu_attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o,
+                                             const int32_t* seq_offsets, const int32_t* func,
+                                             const hstu_attn_shape_t* shape, int32_t* row_counts,
+                                             void* stream);
+
 /* Synchronises the stream, then returns the status recorded in the
  * workspace error word (HSTU_OK, HSTU_ERR_DEVICE_INPUT, HSTU_ERR_TIMEOUT) or
  * HSTU_ERR_CUDA if the synchronisation failed. */

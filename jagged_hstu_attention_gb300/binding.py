@@ -29,8 +29,9 @@ FLAG_REUSE_PLAN = 1
 EXPORTED = (
     "hstu_attn_nfunc_supported", "hstu_attn_workspace_size", "hstu_attn_plan", "hstu_attn_fwd",
     "hstu_attn_bwd", "hstu_attn_fwd_targets_only", "hstu_attn_bwd_targets_only",
-    "hstu_attn_get_device_status", "hstu_status_string",
+    "hstu_attn_get_device_status", "hstu_status_string", "hstu_attn_fwd_noalloc",
 )
+NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
 class HstuError(RuntimeError):
@@ -76,6 +77,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "hstu_attn_bwd_targets_only": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, vp, vp, vp, sp, vp, sz, vp]),
         "hstu_attn_get_device_status": (ctypes.c_int, [vp, vp]),
         "hstu_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+        "hstu_attn_fwd_noalloc": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, sp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -230,3 +232,21 @@ def bwd_targets_only(do_c, q_c, k, v, seq_offsets, func_c, max_seqlen: int,
 def device_status(ws: torch.Tensor, stream=None) -> int:
     """Synchronises the stream and returns the workspace status code."""
     return int(load().hstu_attn_get_device_status(_ptr(ws), _stream(stream)))
+
+
+def fwd_noalloc(q, k, v, seq_offsets, func, max_seqlen: int, alpha: Optional[float] = None,
+                row_counts: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+                stream=None) -> torch.Tensor:
+    """Forward pass for callers that cannot allocate device memory: the plan's
+    scratch is a fixed array inside the library (hstu_attn_fwd_noalloc).
+    ``out`` lets the caller supply the output buffer too."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, torch.bfloat16, n)
+    _need(seq_offsets, torch.int32, "seq_offsets")
+    _need(func, torch.int32, "func")
+    shape = _shape_full(q, seq_offsets, func, max_seqlen, alpha)
+    o = torch.empty_like(q) if out is None else out
+    _check(load().hstu_attn_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(seq_offsets), _ptr(func),
+                                        ctypes.byref(shape), _ptr(row_counts), _stream(stream)),
+           "hstu_attn_fwd_noalloc")
+    return o
