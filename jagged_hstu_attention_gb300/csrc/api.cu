@@ -87,6 +87,8 @@ hstu::PlanParams plan_params(const int32_t* seq_offsets, const int32_t* func,
   p.kvvis = reinterpret_cast<int32_t*>(base + l.kvvis);
   p.fwd_list = reinterpret_cast<int32_t*>(base + l.fwd_list);
   p.bwd_list = reinterpret_cast<int32_t*>(base + l.bwd_list);
+  p.seq_order = reinterpret_cast<int32_t*>(base + l.seq_order);
+  p.seq_start = reinterpret_cast<int32_t*>(base + l.seq_start);
   p.cls = base + l.cls;
   p.total = s->total;
   p.batch = s->batch;

@@ -1,7 +1,7 @@
 // Forward kernel: one CTA per (work item = sequence b, q tile qt) and head h.
 //
 //   warp 8      TMA producer: Q tile once, then K/V tiles of every visited kv
-//               tile into a 2-stage ring.
+//               tile into a ring of kStages (3 at D=128, 4 at D<=64).
 //   warp 9      TMEM owner and MMA issuer (one elected lane):
 //                 S[it % 2] = Q K^T             (tcgen05, SMEM x SMEM)
 //                 O        += P[it % 2] V       (tcgen05, TMEM x SMEM)
@@ -28,11 +28,12 @@ template <int DP>
 struct FwdSmem {
   static constexpr int kChunks = DP / 64;
   static constexpr int kTile = kChunks * kBlock * 128;  // bytes of a 128 x DP bf16 tile
+  static constexpr int kStages = DP == 128 ? 3 : 4;     // K/V ring depth
   alignas(1024) uint8_t q[kTile];
-  alignas(1024) uint8_t k[2][kTile];
-  alignas(1024) uint8_t v[2][kTile];
-  alignas(8) uint64_t bar_q, bar_kv_full[2], bar_kv_empty[2], bar_s_full[2], bar_p_full[2],
-      bar_o_full;
+  alignas(1024) uint8_t k[kStages][kTile];
+  alignas(1024) uint8_t v[kStages][kTile];
+  alignas(8) uint64_t bar_q, bar_kv_full[kStages], bar_kv_empty[kStages], bar_s_full[2],
+      bar_p_full[2], bar_o_full;
   uint32_t tmem_base;
   int abort_flag;
   int n_tiles;
@@ -84,9 +85,11 @@ __global__ void __launch_bounds__(320, 1) hstu_fwd_kernel(const __grid_constant_
   if (threadIdx.x == 0) {
     s.abort_flag = 0;
     mbar_init(smem_u32(&s.bar_q), 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < Smem::kStages; ++i) {
       mbar_init(smem_u32(&s.bar_kv_full[i]), 1);
       mbar_init(smem_u32(&s.bar_kv_empty[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&s.bar_s_full[i]), 1);
       mbar_init(smem_u32(&s.bar_p_full[i]), 256);
     }
@@ -125,12 +128,13 @@ __global__ void __launch_bounds__(320, 1) hstu_fwd_kernel(const __grid_constant_
   if (warp == 8) {
     // ------------------------------------------------------------ producer
     if (nt > 0 && elect_one_sync()) {
-      int last_use[2] = {-1, -1};
+      int last_use[Smem::kStages];
+      for (int i = 0; i < Smem::kStages; ++i) last_use[i] = -1;
       mbar_expect_tx(smem_u32(&s.bar_q), kTile);
       for (int c = 0; c < Smem::kChunks; ++c)
         tma_load_3d(smem_u32(s.q + c * kChunkBytes), &p.tm_q, smem_u32(&s.bar_q), c * 64, h, q_row0);
       for (int it = 0; it < nt; ++it) {
-        const int st = it & 1, use = it >> 1;
+        const int st = it % Smem::kStages, use = it / Smem::kStages;
         if (use > 0 && !mbar_wait(smem_u32(&s.bar_kv_empty[st]), (use - 1) & 1, abort_flag)) break;
         const int kv_row0 = o0 + s.tile_j[it] * kBlock;
         const uint32_t bar = smem_u32(&s.bar_kv_full[st]);
@@ -143,7 +147,7 @@ __global__ void __launch_bounds__(320, 1) hstu_fwd_kernel(const __grid_constant_
       }
       // Never leave with a copy in flight.
       mbar_wait_drain(smem_u32(&s.bar_q), 0);
-      for (int st = 0; st < 2; ++st)
+      for (int st = 0; st < Smem::kStages; ++st)
         if (last_use[st] >= 0) mbar_wait_drain(smem_u32(&s.bar_kv_full[st]), last_use[st] & 1);
     }
     __syncwarp();
@@ -157,30 +161,30 @@ __global__ void __launch_bounds__(320, 1) hstu_fwd_kernel(const __grid_constant_
       tc_fence_after();
       for (int it = 0; ok && it <= nt; ++it) {
         if (it < nt) {
-          const int st = it & 1, use = it >> 1;
-          if (!mbar_wait(smem_u32(&s.bar_kv_full[st]), use & 1, abort_flag)) break;
+          const int kst = it % Smem::kStages, kuse = it / Smem::kStages, sb = it & 1;
+          if (!mbar_wait(smem_u32(&s.bar_kv_full[kst]), kuse & 1, abort_flag)) break;
           tc_fence_after();
-          const uint32_t k_base = smem_u32(s.k[st]);
+          const uint32_t k_base = smem_u32(s.k[kst]);
 #pragma unroll
           for (int kk = 0; kk < DP / 16; ++kk) {
             const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-            umma_ss(tbase + st * 128, sdesc_sw128(q_base + off, 16, 1024),
+            umma_ss(tbase + sb * 128, sdesc_sw128(q_base + off, 16, 1024),
                     sdesc_sw128(k_base + off, 16, 1024), idesc_s, kk > 0);
           }
-          umma_commit(smem_u32(&s.bar_s_full[st]));
+          umma_commit(smem_u32(&s.bar_s_full[sb]));
         }
         if (it >= 1) {
-          const int pi = it - 1, pst = pi & 1, puse = pi >> 1;
-          if (!mbar_wait(smem_u32(&s.bar_p_full[pst]), puse & 1, abort_flag)) break;
+          const int pi = it - 1, psb = pi & 1, puse = pi >> 1, pkst = pi % Smem::kStages;
+          if (!mbar_wait(smem_u32(&s.bar_p_full[psb]), puse & 1, abort_flag)) break;
           tc_fence_after();
-          const uint32_t v_base = smem_u32(s.v[pst]);
+          const uint32_t v_base = smem_u32(s.v[pkst]);
 #pragma unroll
           for (int kk = 0; kk < kBlock / 16; ++kk) {
-            umma_ts(tbase + 256, tbase + pst * 128 + (kk >> 2) * 64 + (kk & 3) * 8,
+            umma_ts(tbase + 256, tbase + psb * 128 + (kk >> 2) * 64 + (kk & 3) * 8,
                     sdesc_sw128(v_base + kk * 16 * 128, kChunkBytes, 1024), idesc_o,
                     (pi > 0 || kk > 0) ? 1u : 0u);
           }
-          umma_commit(smem_u32(&s.bar_kv_empty[pst]));
+          umma_commit(smem_u32(&s.bar_kv_empty[pkst]));
         }
       }
       // Arrives once every MMA issued above has completed (also on abort).

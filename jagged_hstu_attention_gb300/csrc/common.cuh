@@ -39,8 +39,8 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // so that one memset clears them at the start of a plan.
 struct FullLayout {
   int nt = 0;  // tiles per sequence at max_seqlen
-  size_t header = 0, qvis = 0, kvvis = 0, zero_bytes = 0, fwd_list = 0, bwd_list = 0, cls = 0,
-         total = 0;
+  size_t header = 0, qvis = 0, kvvis = 0, zero_bytes = 0, fwd_list = 0, bwd_list = 0, seq_order = 0,
+         seq_start = 0, cls = 0, total = 0;
 };
 inline FullLayout full_layout(int batch, int max_seqlen) {
   FullLayout l;
@@ -52,7 +52,9 @@ inline FullLayout full_layout(int batch, int max_seqlen) {
   l.zero_bytes = l.kvvis + align_up(items * 4, 256);
   l.fwd_list = l.zero_bytes;
   l.bwd_list = l.fwd_list + align_up(items * 4, 256);
-  l.cls = l.bwd_list + align_up(2 * items * 4, 256);
+  l.seq_order = l.bwd_list + align_up(2 * items * 4, 256);
+  l.seq_start = l.seq_order + align_up(static_cast<size_t>(batch) * 4, 256);
+  l.cls = l.seq_start + align_up(static_cast<size_t>(batch) * 4, 256);
   l.total = l.cls + align_up(items * l.nt, 256);
   return l;
 }
@@ -81,6 +83,8 @@ struct PlanParams {
   int32_t* kvvis;
   int32_t* fwd_list;
   int32_t* bwd_list;
+  int32_t* seq_order;  // sequences, longest first
+  int32_t* seq_start;  // first work item of each sorted sequence
   uint8_t* cls;
   int64_t total;
   int32_t batch, nfunc, nt, max_seqlen;

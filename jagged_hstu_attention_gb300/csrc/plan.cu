@@ -125,57 +125,51 @@ __device__ void block_exclusive_scan(int* cnt, int n) {
   }
 }
 
-// Longest-first lists by counting sort on the number of tile pairs each item
-// visits (weight). Equal weights may come out in any order: every output
-// element is computed by exactly one CTA with a fixed internal order, so the
-// list order only changes scheduling, never results.
+// Work lists. Sequences are ordered longest first (counting sort on their
+// tile count) and every sequence's items are contiguous, so the CTAs that
+// run at the same time work on one or two sequences and share their K/V (or
+// Q/dO) tiles in L2 instead of streaming every sequence's tiles from HBM at
+// once. Within a sequence the heaviest items come first: forward q tiles
+// last-first (the later rows of causal-like masks see the most columns);
+// backward dK/dV kv tiles first-first, then dQ q tiles last-first. Sequences
+// of equal length may come out in any order: every output element is
+// computed by exactly one CTA with a fixed internal order, so the order only
+// changes scheduling, never results.
 __global__ void __launch_bounds__(1024) plan_sort_kernel(const PlanParams p) {
-  __shared__ int hist_f[kMaxTiles + 1];
-  __shared__ int hist_b[4 * kMaxTiles + 1];
+  __shared__ int hist[kMaxTiles + 1];
+  __shared__ int n_items;
   const int tid = threadIdx.x;
   if (p.header[kHdrErr] != 0) return;
   const int nt = p.nt;
-  const int max_wf = nt, max_wb = 4 * nt;
-  for (int x = tid; x <= max_wf; x += blockDim.x) hist_f[x] = 0;
-  for (int x = tid; x <= max_wb; x += blockDim.x) hist_b[x] = 0;
-  __syncthreads();
-  const int n_all = p.batch * nt;
   auto tiles_of = [&](int b) {
     int L = p.seq_offsets[b + 1] - p.seq_offsets[b];
     L = min(max(L, 0), p.max_seqlen);
     return (L + kBlock - 1) / kBlock;
   };
-  // Histograms; slot index = max_w - weight gives descending order.
-  for (int idx = tid; idx < n_all; idx += blockDim.x) {
-    const int b = idx / nt, t = idx - b * nt;
-    if (t >= tiles_of(b)) continue;
-    const int wq = min(p.qvis[idx], nt);
-    const int wk = min(p.kvvis[idx], nt);
-    atomicAdd(&hist_f[max_wf - wq], 1);
-    atomicAdd(&hist_b[max_wb - 3 * wq], 1);
-    atomicAdd(&hist_b[max_wb - 4 * wk], 1);
+  for (int x = tid; x <= nt; x += blockDim.x) hist[x] = 0;
+  __syncthreads();
+  for (int b = tid; b < p.batch; b += blockDim.x) atomicAdd(&hist[nt - tiles_of(b)], 1);
+  __syncthreads();
+  block_exclusive_scan(hist, nt + 1);
+  __syncthreads();
+  for (int b = tid; b < p.batch; b += blockDim.x)
+    p.seq_order[atomicAdd(&hist[nt - tiles_of(b)], 1)] = b;
+  __syncthreads();
+  for (int pos = tid; pos < p.batch; pos += blockDim.x) p.seq_start[pos] = tiles_of(p.seq_order[pos]);
+  __syncthreads();
+  block_exclusive_scan(p.seq_start, p.batch);
+  __syncthreads();
+  for (int pos = tid; pos < p.batch; pos += blockDim.x) {
+    const int b = p.seq_order[pos];
+    const int n = tiles_of(b);
+    const int st = p.seq_start[pos];
+    for (int t = 0; t < n; ++t) {
+      p.fwd_list[st + t] = (b << 8) | (n - 1 - t);
+      p.bwd_list[2 * st + t] = (b << 8) | t | kRoleDkdv;
+      p.bwd_list[2 * st + n + t] = (b << 8) | (n - 1 - t);
+    }
   }
-  __syncthreads();
-  block_exclusive_scan(hist_f, max_wf + 1);
-  block_exclusive_scan(hist_b, max_wb + 1);
-  __syncthreads();
-  int my_f = 0;
-  for (int idx = tid; idx < n_all; idx += blockDim.x) {
-    const int b = idx / nt, t = idx - b * nt;
-    if (t >= tiles_of(b)) continue;
-    ++my_f;
-    const int wq = min(p.qvis[idx], nt);
-    const int wk = min(p.kvvis[idx], nt);
-    const int code = (b << 8) | t;
-    p.fwd_list[atomicAdd(&hist_f[max_wf - wq], 1)] = code;
-    p.bwd_list[atomicAdd(&hist_b[max_wb - 3 * wq], 1)] = code;
-    p.bwd_list[atomicAdd(&hist_b[max_wb - 4 * wk], 1)] = code | kRoleDkdv;
-  }
-  // total item count
-  __shared__ int n_items;
-  if (tid == 0) n_items = 0;
-  __syncthreads();
-  if (my_f) atomicAdd(&n_items, my_f);
+  if (tid == 0) n_items = p.seq_start[p.batch - 1] + tiles_of(p.seq_order[p.batch - 1]);
   __syncthreads();
   if (tid == 0) {
     p.header[kHdrNFwd] = n_items;
