@@ -6,7 +6,8 @@
 // through a 2-stage ring. Per q tile (TMEM lanes = kv rows):
 //     S^T  = K Q^T,  dP^T = V dO^T                      (SMEM x SMEM)
 //     P^T  = silu(alpha S^T)/N,  dS^T = dP^T * silu'(alpha S^T) * alpha/N
-//            (masked on partial tiles, packed bf16 in place over S^T, dP^T)
+//            (masked on partial tiles, packed bf16 in place over S^T, dP^T;
+//            the common factor alpha/(2N) is applied once at the stores)
 //     dV  += P^T dO,  dK += dS^T Q                       (TMEM x SMEM)
 // dK and dV accumulate in TMEM across the whole loop and are stored once:
 // no atomics, fixed order, bitwise repeatable.
@@ -19,10 +20,16 @@
 // 10 D flops per pair) in exchange for a deterministic dQ with no fp32
 // workspace and no reduce-add traffic.
 //
-// Warps: 0-7 epilogue (warp w: TMEM lanes 32(w%4).., column half w/4), 8 TMA
-// producer, 9 TMEM owner and MMA issuer. Each half packs its bf16 results in
-// place over the first 32 columns of its own 64 (K-steps 0-3 of the next MMA
-// read columns [0,32), K-steps 4-7 read [64,96)).
+// Warps: 0-7 epilogue, 8 TMA producer, 9 TMEM owner and MMA issuer.
+//
+// Half-tile pipeline: every 128-wide tile is handled as two 64-column halves.
+// S/dP of a half are N=64 MMAs into their own TMEM half. The epilogue warps
+// form two groups of four (TMEM lanes 32(w%4)..), and group h owns half h of
+// every tile, so both halves are converted at the same time while the tensor
+// core runs the accumulating MMAs of a finished half and S/dP of the next.
+// Each warp packs its bf16 results over the first 32 of its half's 64
+// columns, which it has read itself; the accumulating MMA's four K-steps of
+// half h read columns [64h, 64h+32).
 //
 // Partial-tile masks of the dK/dV role are built by transposition: each warp
 // holds 32 q rows of the visiting q tile, computes each row's visible-column
@@ -44,7 +51,7 @@ struct BwdSmem {
   alignas(1024) uint8_t res1[kTile];
   alignas(1024) uint8_t str0[2][kTile];
   alignas(1024) uint8_t str1[2][kTile];
-  alignas(8) uint64_t bar_res, bar_full[2], bar_empty[2], bar_s_full, bar_p_full, bar_acc,
+  alignas(8) uint64_t bar_res, bar_full[2], bar_empty[2], bar_s_full[2], bar_p_full[2], bar_acc,
       bar_func[2];
   uint32_t tmem_base;
   int abort_flag;
@@ -66,22 +73,22 @@ __device__ __forceinline__ bool warp_wait_b(uint32_t bar, uint32_t parity, volat
   return __all_sync(0xffffffffu, ok);
 }
 
-// Stores 32 fp32 accumulator columns of one row as bf16.
-__device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const uint32_t (&a)[32]) {
+// Stores 32 fp32 accumulator columns of one row, times `scale`, as bf16.
+__device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const uint32_t (&a)[32], float scale) {
   uint32_t pk[16];
 #pragma unroll
   for (int e = 0; e < 16; ++e)
-    pk[e] = pack_bf16x2(__uint_as_float(a[2 * e]), __uint_as_float(a[2 * e + 1]));
+    pk[e] = pack_bf16x2(scale * __uint_as_float(a[2 * e]), scale * __uint_as_float(a[2 * e + 1]));
   uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
   for (int e = 0; e < 4; ++e) d4[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
 }
 
 // Writes this warp's half of TMEM columns [taddr, taddr + DP) of its lane (or
-// zeros) into a bf16 row of `dim` elements.
+// zeros), times `scale`, into a bf16 row of `dim` elements.
 template <int DP>
 __device__ __forceinline__ void store_acc_half(uint32_t taddr, int half, bool have, bool valid,
-                                               __nv_bfloat16* dst, int dim) {
+                                               __nv_bfloat16* dst, int dim, float scale) {
 #pragma unroll
   for (int c = 0; c < DP / 64; ++c) {
     const int col = half * (DP / 2) + c * 32;
@@ -93,7 +100,35 @@ __device__ __forceinline__ void store_acc_half(uint32_t taddr, int half, bool ha
 #pragma unroll
       for (int e = 0; e < 32; ++e) a[e] = 0u;
     }
-    if (valid && col < dim) store_row32(dst + col, a);
+    if (valid && col < dim) store_row32(dst + col, a, scale);
+  }
+}
+
+// 32 columns of S and dP -> packed bf16 P' = s (1 + t) (when WANT_P) and
+// G' = dP (1 + t)(1 + h - h t), h = alpha s / 2, t = tanh(h): the backward
+// quantities up to the factor alpha / (2N) applied to dV, dK and dQ at their
+// store. MASKED zeroes the columns whose bit is clear.
+template <bool MASKED, bool WANT_P>
+__device__ __forceinline__ void epilogue32(const uint32_t (&sv)[32], const uint32_t (&dv)[32],
+                                           uint32_t mask, float half_alpha, uint32_t (&pp)[16],
+                                           uint32_t (&pd)[16]) {
+#pragma unroll
+  for (int e = 0; e < 32; e += 2) {
+    float g[2], pv[2];
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+      const float sc = __uint_as_float(sv[e + x]);
+      const float dp = __uint_as_float(dv[e + x]);
+      if (WANT_P) silu_pu_gu(sc, dp, half_alpha, pv[x], g[x]);
+      else g[x] = silu_gu(sc, dp, half_alpha);
+      if (MASKED) {
+        const bool on = (mask >> (e + x)) & 1u;
+        if (WANT_P) pv[x] = on ? pv[x] : 0.0f;
+        g[x] = on ? g[x] : 0.0f;
+      }
+    }
+    if (WANT_P) pp[e / 2] = pack_bf16x2(pv[0], pv[1]);
+    pd[e / 2] = pack_bf16x2(g[0], g[1]);
   }
 }
 
@@ -117,8 +152,10 @@ __device__ __forceinline__ void bwd_role(const AttnParams& p, BwdSmem<DP>& s, bo
       mbar_init(smem_u32(&s.bar_full[i]), 1);
       mbar_init(smem_u32(&s.bar_empty[i]), 1);
     }
-    mbar_init(smem_u32(&s.bar_s_full), 1);
-    mbar_init(smem_u32(&s.bar_p_full), 256);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&s.bar_s_full[i]), 1);
+      mbar_init(smem_u32(&s.bar_p_full[i]), 128);
+    }
     mbar_init(smem_u32(&s.bar_acc), 1);
     mbar_init(smem_u32(&s.bar_func[0]), 256);
     mbar_init(smem_u32(&s.bar_func[1]), 256);
@@ -200,53 +237,66 @@ __device__ __forceinline__ void bwd_role(const AttnParams& p, BwdSmem<DP>& s, bo
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (nt > 0 && elect_one_sync()) {
-      constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
+      // Half-tile pipeline: step u covers the 64-column half (u & 1) of tile
+      // u >> 1. S/dP of step u go into TMEM half (u & 1) while the epilogue
+      // works on step u - 1 in the other half; the accumulating MMAs of step
+      // u - 1 follow as soon as its packed P/dS are in place.
+      constexpr uint32_t idesc_s = idesc_bf16(128, 64, false, false);
       constexpr uint32_t idesc_acc = idesc_bf16(128, DP, false, true);
-      const uint32_t r0 = smem_u32(s.res0), r1 = smem_u32(s.res1);
+      // Descriptors are built once; each MMA only advances a start address.
+      const uint64_t dr0 = sdesc_sw128(smem_u32(s.res0), 16, 1024);
+      const uint64_t dr1 = sdesc_sw128(smem_u32(s.res1), 16, 1024);
+      const uint64_t ds0 = sdesc_sw128(smem_u32(s.str0[0]), 16, 1024);
+      const uint64_t ds1 = sdesc_sw128(smem_u32(s.str1[0]), 16, 1024);
+      const uint64_t ds0_mn = sdesc_sw128(smem_u32(s.str0[0]), kChunkBytes, 1024);
+      const uint64_t ds1_mn = sdesc_sw128(smem_u32(s.str1[0]), kChunkBytes, 1024);
       bool ok = mbar_wait(smem_u32(&s.bar_res), 0, abort_flag);
       tc_fence_after();
-      for (int it = 0; ok && it < nt; ++it) {
-        const int st = it & 1, use = it >> 1;
-        if (!mbar_wait(smem_u32(&s.bar_full[st]), use & 1, abort_flag)) break;
-        tc_fence_after();
-        const uint32_t s0 = smem_u32(s.str0[st]), s1 = smem_u32(s.str1[st]);
-        // S (or S^T) = res0 . str0^T ; dP (or dP^T) = res1 . str1^T
-#pragma unroll
-        for (int kk = 0; kk < DP / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-          umma_ss(tS, sdesc_sw128(r0 + off, 16, 1024), sdesc_sw128(s0 + off, 16, 1024), idesc_s,
-                  kk > 0);
-        }
-#pragma unroll
-        for (int kk = 0; kk < DP / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-          umma_ss(tdP, sdesc_sw128(r1 + off, 16, 1024), sdesc_sw128(s1 + off, 16, 1024), idesc_s,
-                  kk > 0);
-        }
-        umma_commit(smem_u32(&s.bar_s_full));
-        if (!mbar_wait(smem_u32(&s.bar_p_full), it & 1, abort_flag)) break;
-        tc_fence_after();
-        if (dkdv) {
-          // dV += P^T dO (dO = str1, MN-major); dK += dS^T Q (Q = str0, MN-major)
-#pragma unroll
-          for (int kk = 0; kk < kBlock / 16; ++kk) {
-            const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
-            const uint32_t acol = (kk >> 2) * 64 + (kk & 3) * 8;
-            umma_ts(t_acc0, tS + acol, sdesc_sw128(s1 + kk * 16 * 128, kChunkBytes, 1024),
-                    idesc_acc, acc);
-            umma_ts(t_acc1, tdP + acol, sdesc_sw128(s0 + kk * 16 * 128, kChunkBytes, 1024),
-                    idesc_acc, acc);
+      const int nsteps = 2 * nt;
+      for (int u = 0; ok && u <= nsteps; ++u) {
+        if (u < nsteps) {
+          const int it = u >> 1, hh = u & 1, st = it & 1;
+          if (hh == 0) {
+            if (!mbar_wait(smem_u32(&s.bar_full[st]), (it >> 1) & 1, abort_flag)) break;
+            tc_fence_after();
           }
-        } else {
-          // dQ += dS K (K = str0, MN-major)
+          // S (or S^T) = res0 . str0_h^T ; dP (or dP^T) = res1 . str1_h^T, N = 64
+          const uint32_t hoff = st * kTile + hh * 64 * 128;
+          const uint64_t b0 = sdesc_advance(ds0, hoff), b1 = sdesc_advance(ds1, hoff);
 #pragma unroll
-          for (int kk = 0; kk < kBlock / 16; ++kk) {
-            umma_ts(t_dq, tS + (kk >> 2) * 64 + (kk & 3) * 8,
-                    sdesc_sw128(s0 + kk * 16 * 128, kChunkBytes, 1024), idesc_acc,
-                    (it > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < DP / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+            umma_ss(tS + hh * 64, sdesc_advance(dr0, off), sdesc_advance(b0, off), idesc_s, kk > 0);
           }
+#pragma unroll
+          for (int kk = 0; kk < DP / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+            umma_ss(tdP + hh * 64, sdesc_advance(dr1, off), sdesc_advance(b1, off), idesc_s, kk > 0);
+          }
+          umma_commit(smem_u32(&s.bar_s_full[hh]));
         }
-        umma_commit(smem_u32(&s.bar_empty[st]));
+        if (u >= 1) {
+          const int pu = u - 1, pit = pu >> 1, ph = pu & 1, pst = pit & 1;
+          if (!mbar_wait(smem_u32(&s.bar_p_full[ph]), pit & 1, abort_flag)) break;
+          tc_fence_after();
+          const uint32_t boff0 = pst * kTile + ph * 64 * 128;
+          const uint64_t m0 = sdesc_advance(ds0_mn, boff0), m1 = sdesc_advance(ds1_mn, boff0);
+          const uint32_t first = (pit > 0 || ph > 0) ? 1u : 0u;
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {  // K = the 64 rows of this half
+            const uint32_t acol = ph * 64 + ks * 8;
+            const uint32_t acc = ks > 0 ? 1u : first;
+            if (dkdv) {
+              // dV += P^T dO (dO = str1, MN-major); dK += dS^T Q (Q = str0, MN-major)
+              umma_ts(t_acc0, tS + acol, sdesc_advance(m1, ks * 16 * 128), idesc_acc, acc);
+              umma_ts(t_acc1, tdP + acol, sdesc_advance(m0, ks * 16 * 128), idesc_acc, acc);
+            } else {
+              // dQ += dS K (K = str0, MN-major)
+              umma_ts(t_dq, tS + acol, sdesc_advance(m0, ks * 16 * 128), idesc_acc, acc);
+            }
+          }
+          if (ph == 1) umma_commit(smem_u32(&s.bar_empty[pst]));
+        }
       }
       umma_commit(smem_u32(&s.bar_acc));
       mbar_wait_drain(smem_u32(&s.bar_acc), 0);
@@ -259,18 +309,21 @@ __device__ __forceinline__ void bwd_role(const AttnParams& p, BwdSmem<DP>& s, bo
     const int own_loc = tile * kBlock + r;
     const bool valid = own_loc < L;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
-    const SiluConsts kc(p.alpha, p.inv_n);
+    const float half_alpha = 0.5f * p.alpha;
+    const float out_scale = 0.5f * p.alpha * p.inv_n;  // hc = alpha / (2N)
     const int hc = half * 64;  // first S column of this warp's half
     int lo[NINT], hi[NINT];
     if (!dkdv)
       load_row_intervals<NINT>(p.func, p.total, static_cast<int64_t>(o0) + own_loc, L, valid, lo, hi);
     bool ok = true;
     int fu = 0;  // partial tiles seen so far (dK/dV role): selects the mask buffer
+    int buf = 0;
+    const int hh = half;  // ping-pong: this warp group owns TMEM half `half` of every tile
     for (int it = 0; it < nt; ++it) {
       const int other = s.tile_idx[it];
       const bool partial = s.tile_c[it] == kPartial;
-      const int buf = fu & 1;
       if (dkdv && partial) {
+        buf = fu & 1;
         // This warp's 32 q rows of the visiting q tile; their visible bits
         // over kv columns [hc, hc + 64) of tile `tile`, transposed by ballot.
         int flo[NINT], fhi[NINT];
@@ -296,34 +349,30 @@ __device__ __forceinline__ void bwd_role(const AttnParams& p, BwdSmem<DP>& s, bo
         if (!warp_wait_b(smem_u32(&s.bar_func[buf]), (fu >> 1) & 1, abort_flag)) { ok = false; break; }
         ++fu;
       }
-      if (!warp_wait_b(smem_u32(&s.bar_s_full), it & 1, abort_flag)) { ok = false; break; }
+      if (!warp_wait_b(smem_u32(&s.bar_s_full[hh]), it & 1, abort_flag)) { ok = false; break; }
       tc_fence_after();
-      const int col0 = other * kBlock;  // dQ role: first kv column of the tile
 #pragma unroll 1
       for (int c = 0; c < 2; ++c) {
-        const int chunk = 2 * half + c;  // 32-column chunk of S / dP
+        const int chunk = 2 * hh + c;  // 32-column chunk of S / dP (of the 128)
         uint32_t sv[32], dv[32];
         tmem_ld32(tS + lane_addr + chunk * 32, sv);
         tmem_ld32(tdP + lane_addr + chunk * 32, dv);
         tmem_ld_wait(sv);
         tmem_ld_wait(dv);
-        uint32_t mask = 0xffffffffu;
-        if (partial) mask = dkdv ? s.colmask[buf][chunk][r] : row_mask_word<NINT>(lo, hi, col0 + chunk * 32);
         uint32_t pp[16], pd[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float g[2], pv[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            silu_p_g(__uint_as_float(sv[e + u]), __uint_as_float(dv[e + u]), kc, pv[u], g[u]);
-            const bool on = (mask >> (e + u)) & 1u;
-            pv[u] = on ? pv[u] : 0.0f;
-            g[u] = on ? g[u] : 0.0f;
-          }
-          pp[e / 2] = pack_bf16x2(pv[0], pv[1]);
-          pd[e / 2] = pack_bf16x2(g[0], g[1]);
+        if (partial) {  // CTA-uniform: full tiles run no mask arithmetic
+          const uint32_t mask =
+              dkdv ? s.colmask[buf][chunk][r] : row_mask_word<NINT>(lo, hi, other * kBlock + chunk * 32);
+          if (dkdv) epilogue32<true, true>(sv, dv, mask, half_alpha, pp, pd);
+          else epilogue32<true, false>(sv, dv, mask, half_alpha, pp, pd);
+        } else {
+          if (dkdv) epilogue32<false, true>(sv, dv, 0u, half_alpha, pp, pd);
+          else epilogue32<false, false>(sv, dv, 0u, half_alpha, pp, pd);
         }
-        const uint32_t dst = lane_addr + hc + c * 16;
+        // Packed over columns [64h + 16c, 64h + 16c + 16), which this warp
+        // has already read: K-step ks of the half's accumulating MMA reads
+        // columns [64h + 8ks, 64h + 8ks + 8).
+        const uint32_t dst = lane_addr + hh * 64 + c * 16;
         if (dkdv) {
           tmem_st16(tS + dst, pp);
           tmem_st16(tdP + dst, pd);
@@ -333,17 +382,20 @@ __device__ __forceinline__ void bwd_role(const AttnParams& p, BwdSmem<DP>& s, bo
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(smem_u32(&s.bar_p_full));
+      mbar_arrive(smem_u32(&s.bar_p_full[hh]));
     }
     if (ok && nt > 0) ok = warp_wait_b(smem_u32(&s.bar_acc), 0, abort_flag);
     tc_fence_after();
     if (ok && !*abort_flag) {
       const int64_t row = static_cast<int64_t>(row0 + r) * p.heads + h;
       if (dkdv) {
-        store_acc_half<DP>(t_acc0 + lane_addr, half, nt > 0, valid, p.out2 + row * p.dim, p.dim);  // dV
-        store_acc_half<DP>(t_acc1 + lane_addr, half, nt > 0, valid, p.out1 + row * p.dim, p.dim);  // dK
+        store_acc_half<DP>(t_acc0 + lane_addr, half, nt > 0, valid, p.out2 + row * p.dim, p.dim,
+                           out_scale);  // dV
+        store_acc_half<DP>(t_acc1 + lane_addr, half, nt > 0, valid, p.out1 + row * p.dim, p.dim,
+                           out_scale);  // dK
       } else {
-        store_acc_half<DP>(t_dq + lane_addr, half, nt > 0, valid, p.out0 + row * p.dim, p.dim);  // dQ
+        store_acc_half<DP>(t_dq + lane_addr, half, nt > 0, valid, p.out0 + row * p.dim, p.dim,
+                           out_scale);  // dQ
       }
     }
   }

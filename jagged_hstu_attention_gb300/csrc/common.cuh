@@ -172,33 +172,32 @@ __device__ __forceinline__ float tanh_approx(float x) {
 }
 
 // Epilogue arithmetic on one S element s, with t = tanh(alpha s / 2) so that
-// sigmoid(alpha s) = (1 + t) / 2 (one MUFU op per element):
-//   p  = silu(alpha s) / N = u + u t,            u = s * alpha / (2N)
-//   silu'(x) = sigmoid(x) + x sigmoid(x)(1 - sigmoid(x))
-//            = (1 + t)/2 + (alpha s / 4)(1 - t^2)
-struct SiluConsts {
-  float half_alpha;     // alpha / 2
-  float quarter_alpha;  // alpha / 4
-  float half_c;         // alpha / (2N)
-  float c;              // alpha / N
-  __device__ __forceinline__ SiluConsts(float alpha, float inv_n)
-      : half_alpha(0.5f * alpha), quarter_alpha(0.25f * alpha), half_c(0.5f * alpha * inv_n),
-        c(alpha * inv_n) {}
-};
-__device__ __forceinline__ float silu_p(float s, const SiluConsts& k) {
-  const float t = tanh_approx(k.half_alpha * s);
-  const float u = k.half_c * s;
-  return fmaf(u, t, u);
+// sigmoid(alpha s) = (1 + t) / 2 (one MUFU op per element). The common factor
+// hc = alpha / (2N) is left out of every element and applied once to the fp32
+// accumulators at their store:
+//   silu(alpha s) / N  = hc * s (1 + t)                           -> P' = s (1 + t)
+//   silu'(alpha s)     = (1 + t) / 2 + (alpha s / 4)(1 - t^2)
+//                      = (1 + t)(1 + h (1 - t)) / 2,  h = alpha s / 2
+//   dP silu'(alpha s) alpha / N = hc * dP (1 + t)(1 + h (1 - t))   -> G' = dP (1 + t)(1 + h - h t)
+// so O = hc sum P' V, dV = hc sum P'^T dO, dK = hc sum G'^T Q, dQ = hc sum G' K.
+__device__ __forceinline__ float silu_pu(float s, float half_alpha) {
+  const float t = tanh_approx(half_alpha * s);
+  return fmaf(s, t, s);
 }
-// p and g = dp * silu'(alpha s) * alpha / N.
-__device__ __forceinline__ void silu_p_g(float s, float dp, const SiluConsts& k, float& p, float& g) {
-  const float t = tanh_approx(k.half_alpha * s);
-  const float u = k.half_c * s;
-  p = fmaf(u, t, u);
-  const float sg = fmaf(0.5f, t, 0.5f);
-  const float w = fmaf(-t, t, 1.0f);
-  const float dsilu = fmaf(k.quarter_alpha * s, w, sg);
-  g = (dp * k.c) * dsilu;
+__device__ __forceinline__ void silu_pu_gu(float s, float dp, float half_alpha, float& p, float& g) {
+  const float h = half_alpha * s;
+  const float t = tanh_approx(h);
+  p = fmaf(s, t, s);
+  const float a = 1.0f + t;
+  const float f = fmaf(-h, t, h + 1.0f);
+  g = (dp * a) * f;
+}
+__device__ __forceinline__ float silu_gu(float s, float dp, float half_alpha) {
+  const float h = half_alpha * s;
+  const float t = tanh_approx(h);
+  const float a = 1.0f + t;
+  const float f = fmaf(-h, t, h + 1.0f);
+  return (dp * a) * f;
 }
 
 }  // namespace hstu

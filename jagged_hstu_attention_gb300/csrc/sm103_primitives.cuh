@@ -182,6 +182,13 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
   return d;
 }
 
+// Moves a descriptor's start address by `byte_off` bytes (a multiple of 16).
+// The start-address field holds address >> 4 in 14 bits and shared memory is
+// below 256 KB, so the add never carries out of the field.
+__device__ __forceinline__ uint64_t sdesc_advance(uint64_t desc, uint32_t byte_off) {
+  return desc + static_cast<uint64_t>(byte_off >> 4);
+}
+
 // Instruction descriptor, kind::f16: bf16 A and B, fp32 accumulator,
 // a_mn / b_mn select MN-major operands.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool b_mn) {
