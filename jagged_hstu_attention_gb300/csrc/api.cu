@@ -89,6 +89,7 @@ hstu::PlanParams plan_params(const int32_t* seq_offsets, const int32_t* func,
   p.bwd_list = reinterpret_cast<int32_t*>(base + l.bwd_list);
   p.seq_order = reinterpret_cast<int32_t*>(base + l.seq_order);
   p.seq_start = reinterpret_cast<int32_t*>(base + l.seq_start);
+  p.ivmask = base + l.ivmask;
   p.cls = base + l.cls;
   p.total = s->total;
   p.batch = s->batch;
@@ -169,6 +170,7 @@ hstu_status_t hstu_attn_fwd(const void* q, const void* k, const void* v, void* o
   p.func = func;
   p.out0 = static_cast<__nv_bfloat16*>(o);
   p.cls = base + l.cls;
+  p.ivmask = base + l.ivmask;
   p.list = reinterpret_cast<const int32_t*>(base + l.fwd_list);
   p.header = reinterpret_cast<int32_t*>(base + l.header);
   p.total = shape->total;
@@ -210,6 +212,7 @@ hstu_status_t hstu_attn_bwd(const void* dout, const void* q, const void* k, cons
   p.out1 = static_cast<__nv_bfloat16*>(dk);
   p.out2 = static_cast<__nv_bfloat16*>(dv);
   p.cls = base + l.cls;
+  p.ivmask = base + l.ivmask;
   p.list = reinterpret_cast<const int32_t*>(base + l.bwd_list);
   p.header = reinterpret_cast<int32_t*>(base + l.header);
   p.total = shape->total;

@@ -1,26 +1,33 @@
-// Backward kernel: one launch, two CTA roles taken from one longest-first
-// work list (entries carry the role bit), so both run side by side.
+// Backward kernel, persistent: one CTA per SM walks one longest-first work
+// list whose entries carry a role bit, so both roles run side by side and a
+// CTA keeps its pipelines running across items of either role.
 //
-// dK/dV role -- one CTA per (sequence b, kv tile kt, head h). K and V of the
-// tile stay in SMEM; the Q and dO tiles of every q tile that visits kt stream
+// dK/dV role -- item (sequence b, kv tile kt, head h). K and V of the tile
+// stay in SMEM; the Q and dO tiles of every q tile that visits kt stream
 // through a 2-stage ring. Per q tile (TMEM lanes = kv rows):
 //     S^T  = K Q^T,  dP^T = V dO^T                      (SMEM x SMEM)
 //     P^T  = silu(alpha S^T)/N,  dS^T = dP^T * silu'(alpha S^T) * alpha/N
 //            (masked on partial tiles, packed bf16 in place over S^T, dP^T;
 //            the common factor alpha/(2N) is applied once at the stores)
 //     dV  += P^T dO,  dK += dS^T Q                       (TMEM x SMEM)
-// dK and dV accumulate in TMEM across the whole loop and are stored once:
+// dK and dV accumulate in TMEM across the whole item and are stored once:
 // no atomics, fixed order, bitwise repeatable.
 //
-// dQ role -- one CTA per (sequence b, q tile qt, head h). Q and dO stay in
-// SMEM; K and V of every visited kv tile stream. Per kv tile (lanes = q rows):
+// dQ role -- item (sequence b, q tile qt, head h). Q and dO stay in SMEM; K
+// and V of every visited kv tile stream. Per kv tile (lanes = q rows):
 //     S = Q K^T,  dP = dO V^T;  dS = dP * silu'(alpha S) * alpha/N (packed
 //     over S);  dQ += dS K.
 // This recomputes S and dP once more per visible tile pair (14 D instead of
 // 10 D flops per pair) in exchange for a deterministic dQ with no fp32
 // workspace and no reduce-add traffic.
 //
-// Warps: 0-7 epilogue, 8 TMA producer, 9 TMEM owner and MMA issuer.
+// Warps: 0-7 epilogue, 8 producer (tile lists into two item slots, TMA
+// loads), 9 TMEM owner and MMA issuer. The next item's lists and resident
+// tiles are fetched while the current item finishes; its first accumulating
+// MMA waits until the epilogue has read out the previous item's accumulators.
+//
+// TMEM (512 columns, the same for both roles): acc0 [0,128) (dV or dQ),
+// acc1 [128,256) (dK), S [256,384), dP [384,512).
 //
 // Half-tile pipeline: every 128-wide tile is handled as two 64-column halves.
 // S/dP of a half are N=64 MMAs into their own TMEM half. The epilogue warps
@@ -41,6 +48,12 @@
 
 namespace hstu {
 
+// One work item as the producer publishes it to the other roles.
+struct BwdItem {
+  int dkdv, b, tile, h, o0, L, nt;
+  uint16_t idx[kMaxTiles];  // visiting (dK/dV) or visited (dQ) tile | 0x100 if partial
+};
+
 template <int DP>
 struct BwdSmem {
   static constexpr int kChunks = DP / 64;
@@ -51,16 +64,15 @@ struct BwdSmem {
   alignas(1024) uint8_t res1[kTile];
   alignas(1024) uint8_t str0[2][kTile];
   alignas(1024) uint8_t str1[2][kTile];
-  alignas(8) uint64_t bar_res, bar_full[2], bar_empty[2], bar_s_full[2], bar_p_full[2], bar_acc,
-      bar_func[2];
+  alignas(8) uint64_t bar_res_full, bar_res_empty, bar_full[2], bar_empty[2], bar_s_full[2],
+      bar_p_full[2], bar_acc_full, bar_acc_empty, bar_func[2], bar_item_full[2], bar_item_empty[2],
+      bar_drain;
   uint32_t tmem_base;
   int abort_flag;
-  int n_tiles;
-  int16_t tile_idx[kMaxTiles];
-  uint8_t tile_c[kMaxTiles];
   // dK/dV role: per partial q tile, colmask[c][j] bit e = q row 32c+e sees
   // kv column j of the tile (double buffered).
   uint32_t colmask[2][4][kBlock];
+  BwdItem item[2];
 };
 
 template <typename S>
@@ -133,52 +145,35 @@ __device__ __forceinline__ void epilogue32(const uint32_t (&sv)[32], const uint3
 }
 
 template <int DP, int NINT>
-__device__ __forceinline__ void bwd_role(const AttnParams& p, BwdSmem<DP>& s, bool dkdv, int b,
-                                         int tile, int h) {
+__global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant__ AttnParams p) {
   using Smem = BwdSmem<DP>;
   constexpr int kTile = Smem::kTile;
   constexpr int kChunkBytes = kBlock * 128;
+  extern __shared__ uint8_t smem_raw[];
+  Smem& s = smem_as_b<Smem>(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int o0 = p.seq_offsets[b];
-  const int L = p.seq_offsets[b + 1] - o0;
-  const int ntiles_b = (L + kBlock - 1) / kBlock;
-  const size_t nt_all = static_cast<size_t>(p.nt);
-  const uint8_t* cls_b = p.cls + static_cast<size_t>(b) * nt_all * nt_all;
+  volatile int32_t* hdr = p.header;
+  if (hdr[kHdrErr] != 0) return;
+  const int n_work = hdr[kHdrNBwd] * p.heads;
+  if (static_cast<int>(blockIdx.x) >= n_work) return;
 
   if (threadIdx.x == 0) {
     s.abort_flag = 0;
-    mbar_init(smem_u32(&s.bar_res), 1);
+    mbar_init(smem_u32(&s.bar_res_full), 1);
+    mbar_init(smem_u32(&s.bar_res_empty), 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&s.bar_full[i]), 1);
       mbar_init(smem_u32(&s.bar_empty[i]), 1);
-    }
-    for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&s.bar_s_full[i]), 1);
       mbar_init(smem_u32(&s.bar_p_full[i]), 128);
+      mbar_init(smem_u32(&s.bar_func[i]), 256);
+      mbar_init(smem_u32(&s.bar_item_full[i]), 1);
+      mbar_init(smem_u32(&s.bar_item_empty[i]), 1 + 256);  // MMA issuer + epilogue threads
     }
-    mbar_init(smem_u32(&s.bar_acc), 1);
-    mbar_init(smem_u32(&s.bar_func[0]), 256);
-    mbar_init(smem_u32(&s.bar_func[1]), 256);
+    mbar_init(smem_u32(&s.bar_acc_full), 1);
+    mbar_init(smem_u32(&s.bar_acc_empty), 256);
+    mbar_init(smem_u32(&s.bar_drain), 1);
     fence_mbar_init();
-  }
-  if (warp == 0) {
-    // dK/dV: q tiles i visiting kv tile `tile` (column of the class matrix);
-    // dQ: kv tiles j visited by q tile `tile` (row of the class matrix).
-    int n = 0;
-    for (int base = 0; base < ntiles_b; base += 32) {
-      const int x = base + lane;
-      uint8_t c = kSkip;
-      if (x < ntiles_b) c = dkdv ? cls_b[static_cast<size_t>(x) * nt_all + tile]
-                                 : cls_b[static_cast<size_t>(tile) * nt_all + x];
-      const unsigned m = __ballot_sync(0xffffffffu, c != kSkip);
-      if (c != kSkip) {
-        const int pos = n + __popc(m & ((1u << lane) - 1u));
-        s.tile_idx[pos] = static_cast<int16_t>(x);
-        s.tile_c[pos] = c;
-      }
-      n += __popc(m);
-    }
-    if (lane == 0) s.n_tiles = n;
   }
   if (warp == 9) {
     tmem_alloc(smem_u32(&s.tmem_base), 512);
@@ -188,55 +183,110 @@ __device__ __forceinline__ void bwd_role(const AttnParams& p, BwdSmem<DP>& s, bo
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = s.tmem_base;
-  const int nt = s.n_tiles;
+  const uint32_t t_acc0 = tbase;        // dV (dK/dV role) or dQ (dQ role)
+  const uint32_t t_acc1 = tbase + 128;  // dK (dK/dV role)
+  const uint32_t tS = tbase + 256;
+  const uint32_t tdP = tbase + 384;
   volatile int* abort_flag = &s.abort_flag;
-  const int row0 = o0 + tile * kBlock;  // rows of the resident tiles
-  // TMEM columns.
-  const uint32_t t_acc0 = tbase;        // dK/dV role: dV;  dQ role: dQ
-  const uint32_t t_acc1 = tbase + DP;   // dK/dV role: dK
-  const uint32_t t_s = dkdv ? tbase + 2 * DP : tbase + 256;
-  const uint32_t t_dp = t_s + 128;
-  // dQ role keeps dQ at column 256 and S/dP at 0/128.
-  const uint32_t t_dq = tbase + 256;
-  const uint32_t t_s_q = tbase, t_dp_q = tbase + 128;
-  const uint32_t tS = dkdv ? t_s : t_s_q;
-  const uint32_t tdP = dkdv ? t_dp : t_dp_q;
-
-  const CUtensorMap* m_res0 = dkdv ? &p.tm_k : &p.tm_q;
-  const CUtensorMap* m_res1 = dkdv ? &p.tm_v : &p.tm_do;
-  const CUtensorMap* m_str0 = dkdv ? &p.tm_q : &p.tm_k;
-  const CUtensorMap* m_str1 = dkdv ? &p.tm_do : &p.tm_v;
+  const int stride = gridDim.x;
+  const size_t nt_all = static_cast<size_t>(p.nt);
 
   if (warp == 8) {
     // ------------------------------------------------------------ producer
-    if (nt > 0 && elect_one_sync()) {
-      int last_use[2] = {-1, -1};
-      const uint32_t br = smem_u32(&s.bar_res);
-      mbar_expect_tx(br, 2 * kTile);
-      for (int c = 0; c < Smem::kChunks; ++c) {
-        tma_load_3d(smem_u32(s.res0 + c * kChunkBytes), m_res0, br, c * 64, h, row0);
-        tma_load_3d(smem_u32(s.res1 + c * kChunkBytes), m_res1, br, c * 64, h, row0);
+    int str_last[2] = {-1, -1};
+    int res_uses = 0;  // items with at least one tile (one resident load each)
+    int gs = 0;        // streamed tiles over all items
+    bool ok = true;
+    int i = 0;
+    for (int w = blockIdx.x; ok && w < n_work; w += stride, ++i) {
+      const int slot = i & 1;
+      if (i >= 2 && !warp_wait_b(smem_u32(&s.bar_item_empty[slot]), ((i >> 1) - 1) & 1, abort_flag)) {
+        ok = false;
+        break;
       }
-      for (int it = 0; it < nt; ++it) {
-        const int st = it & 1, use = it >> 1;
-        if (use > 0 && !mbar_wait(smem_u32(&s.bar_empty[st]), (use - 1) & 1, abort_flag)) break;
-        const int srow0 = o0 + s.tile_idx[it] * kBlock;
-        const uint32_t bar = smem_u32(&s.bar_full[st]);
-        mbar_expect_tx(bar, 2 * kTile);
-        for (int c = 0; c < Smem::kChunks; ++c) {
-          tma_load_3d(smem_u32(s.str0[st] + c * kChunkBytes), m_str0, bar, c * 64, h, srow0);
-          tma_load_3d(smem_u32(s.str1[st] + c * kChunkBytes), m_str1, bar, c * 64, h, srow0);
+      const int code = p.list[w / p.heads];
+      const int h = w % p.heads;
+      const bool dkdv = (code & kRoleDkdv) != 0;
+      const int b = (code & ~kRoleDkdv) >> 8, tile = code & 255;
+      const int o0 = p.seq_offsets[b];
+      const int L = p.seq_offsets[b + 1] - o0;
+      const int ntiles_b = (L + kBlock - 1) / kBlock;
+      const uint8_t* cls_b = p.cls + static_cast<size_t>(b) * nt_all * nt_all;
+      BwdItem& it_slot = s.item[slot];
+      // dK/dV: q tiles visiting kv tile `tile` (a column of the class matrix);
+      // dQ: kv tiles visited by q tile `tile` (a row of it).
+      int n = 0;
+      for (int base = 0; base < ntiles_b; base += 32) {
+        const int x = base + lane;
+        uint8_t c = kSkip;
+        if (x < ntiles_b)
+          c = dkdv ? cls_b[static_cast<size_t>(x) * nt_all + tile] : cls_b[static_cast<size_t>(tile) * nt_all + x];
+        const unsigned m = __ballot_sync(0xffffffffu, c != kSkip);
+        if (c != kSkip)
+          it_slot.idx[n + __popc(m & ((1u << lane) - 1u))] =
+              static_cast<uint16_t>(x | (c == kPartial ? 0x100 : 0));
+        n += __popc(m);
+      }
+      if (lane == 0) {
+        it_slot.dkdv = dkdv ? 1 : 0;
+        it_slot.b = b;
+        it_slot.tile = tile;
+        it_slot.h = h;
+        it_slot.o0 = o0;
+        it_slot.L = L;
+        it_slot.nt = n;
+      }
+      __threadfence_block();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_u32(&s.bar_item_full[slot]));
+        if (n > 0) {
+          const CUtensorMap* m_res0 = dkdv ? &p.tm_k : &p.tm_q;
+          const CUtensorMap* m_res1 = dkdv ? &p.tm_v : &p.tm_do;
+          const CUtensorMap* m_str0 = dkdv ? &p.tm_q : &p.tm_k;
+          const CUtensorMap* m_str1 = dkdv ? &p.tm_do : &p.tm_v;
+          if (res_uses > 0 && !mbar_wait(smem_u32(&s.bar_res_empty), (res_uses - 1) & 1, abort_flag))
+            ok = false;
+          if (ok) {
+            const uint32_t br = smem_u32(&s.bar_res_full);
+            mbar_expect_tx(br, 2 * kTile);
+            const int row0 = o0 + tile * kBlock;
+            for (int c = 0; c < Smem::kChunks; ++c) {
+              tma_load_3d(smem_u32(s.res0 + c * kChunkBytes), m_res0, br, c * 64, h, row0);
+              tma_load_3d(smem_u32(s.res1 + c * kChunkBytes), m_res1, br, c * 64, h, row0);
+            }
+            ++res_uses;
+          }
+          for (int t = 0; ok && t < n; ++t) {
+            const int g = gs + t, st = g & 1, use = g >> 1;
+            if (use > 0 && !mbar_wait(smem_u32(&s.bar_empty[st]), (use - 1) & 1, abort_flag)) {
+              ok = false;
+              break;
+            }
+            const int srow0 = o0 + (it_slot.idx[t] & 0xff) * kBlock;
+            const uint32_t bar = smem_u32(&s.bar_full[st]);
+            mbar_expect_tx(bar, 2 * kTile);
+            for (int c = 0; c < Smem::kChunks; ++c) {
+              tma_load_3d(smem_u32(s.str0[st] + c * kChunkBytes), m_str0, bar, c * 64, h, srow0);
+              tma_load_3d(smem_u32(s.str1[st] + c * kChunkBytes), m_str1, bar, c * 64, h, srow0);
+            }
+            str_last[st] = use;
+          }
+          gs += n;
         }
-        last_use[st] = use;
       }
-      mbar_wait_drain(br, 0);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    }
+    // Never leave with a copy in flight.
+    if (lane == 0) {
+      if (res_uses > 0) mbar_wait_drain(smem_u32(&s.bar_res_full), (res_uses - 1) & 1);
       for (int st = 0; st < 2; ++st)
-        if (last_use[st] >= 0) mbar_wait_drain(smem_u32(&s.bar_full[st]), last_use[st] & 1);
+        if (str_last[st] >= 0) mbar_wait_drain(smem_u32(&s.bar_full[st]), str_last[st] & 1);
     }
     __syncwarp();
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    if (nt > 0 && elect_one_sync()) {
+    if (elect_one_sync()) {
       // Half-tile pipeline: step u covers the 64-column half (u & 1) of tile
       // u >> 1. S/dP of step u go into TMEM half (u & 1) while the epilogue
       // works on step u - 1 in the other half; the accumulating MMAs of step
@@ -250,153 +300,199 @@ __device__ __forceinline__ void bwd_role(const AttnParams& p, BwdSmem<DP>& s, bo
       const uint64_t ds1 = sdesc_sw128(smem_u32(s.str1[0]), 16, 1024);
       const uint64_t ds0_mn = sdesc_sw128(smem_u32(s.str0[0]), kChunkBytes, 1024);
       const uint64_t ds1_mn = sdesc_sw128(smem_u32(s.str1[0]), kChunkBytes, 1024);
-      bool ok = mbar_wait(smem_u32(&s.bar_res), 0, abort_flag);
-      tc_fence_after();
-      const int nsteps = 2 * nt;
-      for (int u = 0; ok && u <= nsteps; ++u) {
-        if (u < nsteps) {
-          const int it = u >> 1, hh = u & 1, st = it & 1;
-          if (hh == 0) {
-            if (!mbar_wait(smem_u32(&s.bar_full[st]), (it >> 1) & 1, abort_flag)) break;
-            tc_fence_after();
-          }
-          // S (or S^T) = res0 . str0_h^T ; dP (or dP^T) = res1 . str1_h^T, N = 64
-          const uint32_t hoff = st * kTile + hh * 64 * 128;
-          const uint64_t b0 = sdesc_advance(ds0, hoff), b1 = sdesc_advance(ds1, hoff);
-#pragma unroll
-          for (int kk = 0; kk < DP / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-            umma_ss(tS + hh * 64, sdesc_advance(dr0, off), sdesc_advance(b0, off), idesc_s, kk > 0);
-          }
-#pragma unroll
-          for (int kk = 0; kk < DP / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-            umma_ss(tdP + hh * 64, sdesc_advance(dr1, off), sdesc_advance(b1, off), idesc_s, kk > 0);
-          }
-          umma_commit(smem_u32(&s.bar_s_full[hh]));
-        }
-        if (u >= 1) {
-          const int pu = u - 1, pit = pu >> 1, ph = pu & 1, pst = pit & 1;
-          if (!mbar_wait(smem_u32(&s.bar_p_full[ph]), pit & 1, abort_flag)) break;
-          tc_fence_after();
-          const uint32_t boff0 = pst * kTile + ph * 64 * 128;
-          const uint64_t m0 = sdesc_advance(ds0_mn, boff0), m1 = sdesc_advance(ds1_mn, boff0);
-          const uint32_t first = (pit > 0 || ph > 0) ? 1u : 0u;
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {  // K = the 64 rows of this half
-            const uint32_t acol = ph * 64 + ks * 8;
-            const uint32_t acc = ks > 0 ? 1u : first;
-            if (dkdv) {
-              // dV += P^T dO (dO = str1, MN-major); dK += dS^T Q (Q = str0, MN-major)
-              umma_ts(t_acc0, tS + acol, sdesc_advance(m1, ks * 16 * 128), idesc_acc, acc);
-              umma_ts(t_acc1, tdP + acol, sdesc_advance(m0, ks * 16 * 128), idesc_acc, acc);
-            } else {
-              // dQ += dS K (K = str0, MN-major)
-              umma_ts(t_dq, tS + acol, sdesc_advance(m0, ks * 16 * 128), idesc_acc, acc);
+      int gs = 0;        // streamed tiles over all items
+      int res_uses = 0;  // items with at least one tile
+      bool ok = true;
+      int i = 0;
+      for (int w = blockIdx.x; ok && w < n_work; w += stride, ++i) {
+        const int slot = i & 1;
+        if (!mbar_wait(smem_u32(&s.bar_item_full[slot]), (i >> 1) & 1, abort_flag)) break;
+        const int nt = s.item[slot].nt;
+        const bool dkdv = s.item[slot].dkdv != 0;
+        mbar_arrive(smem_u32(&s.bar_item_empty[slot]));
+        if (nt == 0) continue;
+        if (!mbar_wait(smem_u32(&s.bar_res_full), res_uses & 1, abort_flag)) break;
+        tc_fence_after();
+        const int nsteps = 2 * nt;
+        for (int u = 0; u <= nsteps; ++u) {
+          if (u < nsteps) {
+            const int g = gs + (u >> 1), hh = u & 1, st = g & 1;
+            if (hh == 0) {
+              if (!mbar_wait(smem_u32(&s.bar_full[st]), (g >> 1) & 1, abort_flag)) { ok = false; break; }
+              tc_fence_after();
             }
+            // S (or S^T) = res0 . str0_h^T ; dP (or dP^T) = res1 . str1_h^T, N = 64
+            const uint32_t hoff = st * kTile + hh * 64 * 128;
+            const uint64_t b0 = sdesc_advance(ds0, hoff), b1 = sdesc_advance(ds1, hoff);
+#pragma unroll
+            for (int kk = 0; kk < DP / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+              umma_ss(tS + hh * 64, sdesc_advance(dr0, off), sdesc_advance(b0, off), idesc_s, kk > 0);
+            }
+#pragma unroll
+            for (int kk = 0; kk < DP / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+              umma_ss(tdP + hh * 64, sdesc_advance(dr1, off), sdesc_advance(b1, off), idesc_s, kk > 0);
+            }
+            umma_commit(smem_u32(&s.bar_s_full[hh]));
+            if (u == nsteps - 1) umma_commit(smem_u32(&s.bar_res_empty));  // residents free
           }
-          if (ph == 1) umma_commit(smem_u32(&s.bar_empty[pst]));
+          if (u >= 1) {
+            const int pu = u - 1, pit = pu >> 1, ph = pu & 1, g = gs + pit, pst = g & 1;
+            if (pu == 0 && res_uses > 0 &&
+                !mbar_wait(smem_u32(&s.bar_acc_empty), (res_uses - 1) & 1, abort_flag)) {
+              ok = false;  // the previous item's accumulators have not been read out
+              break;
+            }
+            if (!mbar_wait(smem_u32(&s.bar_p_full[ph]), g & 1, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t boff0 = pst * kTile + ph * 64 * 128;
+            const uint64_t m0 = sdesc_advance(ds0_mn, boff0), m1 = sdesc_advance(ds1_mn, boff0);
+            const uint32_t first = (pit > 0 || ph > 0) ? 1u : 0u;
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {  // K = the 64 rows of this half
+              const uint32_t acol = ph * 64 + ks * 8;
+              const uint32_t acc = ks > 0 ? 1u : first;
+              if (dkdv) {
+                // dV += P^T dO (dO = str1, MN-major); dK += dS^T Q (Q = str0, MN-major)
+                umma_ts(t_acc0, tS + acol, sdesc_advance(m1, ks * 16 * 128), idesc_acc, acc);
+                umma_ts(t_acc1, tdP + acol, sdesc_advance(m0, ks * 16 * 128), idesc_acc, acc);
+              } else {
+                // dQ += dS K (K = str0, MN-major)
+                umma_ts(t_acc0, tS + acol, sdesc_advance(m0, ks * 16 * 128), idesc_acc, acc);
+              }
+            }
+            if (ph == 1) umma_commit(smem_u32(&s.bar_empty[pst]));
+          }
         }
+        if (!ok) break;
+        umma_commit(smem_u32(&s.bar_acc_full));
+        gs += nt;
+        ++res_uses;
       }
-      umma_commit(smem_u32(&s.bar_acc));
-      mbar_wait_drain(smem_u32(&s.bar_acc), 0);
+      // Arrives once every MMA issued above has completed (also on abort).
+      umma_commit(smem_u32(&s.bar_drain));
+      mbar_wait_drain(smem_u32(&s.bar_drain), 0);
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3, half = warp >> 2;
     const int r = quarter * 32 + lane;  // TMEM lane: kv row (dK/dV role) or q row (dQ role)
-    const int own_loc = tile * kBlock + r;
-    const bool valid = own_loc < L;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     const float half_alpha = 0.5f * p.alpha;
     const float out_scale = 0.5f * p.alpha * p.inv_n;  // hc = alpha / (2N)
     const int hc = half * 64;  // first S column of this warp's half
-    int lo[NINT], hi[NINT];
-    if (!dkdv)
-      load_row_intervals<NINT>(p.func, p.total, static_cast<int64_t>(o0) + own_loc, L, valid, lo, hi);
+    const int hh = half;       // this warp group owns TMEM half `half` of every tile
+    int g0 = 0;                // tiles over all items
+    int fu = 0;                // partial dK/dV tiles over all items: selects the mask buffer
+    int acc_uses = 0;
     bool ok = true;
-    int fu = 0;  // partial tiles seen so far (dK/dV role): selects the mask buffer
-    int buf = 0;
-    const int hh = half;  // ping-pong: this warp group owns TMEM half `half` of every tile
-    for (int it = 0; it < nt; ++it) {
-      const int other = s.tile_idx[it];
-      const bool partial = s.tile_c[it] == kPartial;
-      if (dkdv && partial) {
-        buf = fu & 1;
-        // This warp's 32 q rows of the visiting q tile; their visible bits
-        // over kv columns [hc, hc + 64) of tile `tile`, transposed by ballot.
-        int flo[NINT], fhi[NINT];
-        const int qi = other * kBlock + r;
-        load_row_intervals<NINT>(p.func, p.total, static_cast<int64_t>(o0) + qi, L, qi < L, flo, fhi);
-        const uint32_t w0 = row_mask_word<NINT>(flo, fhi, tile * kBlock + hc);
-        const uint32_t w1 = row_mask_word<NINT>(flo, fhi, tile * kBlock + hc + 32);
-        uint32_t mine0 = 0, mine1 = 0;
+    int i = 0;
+    for (int w = blockIdx.x; ok && w < n_work; w += stride, ++i) {
+      const int slot = i & 1;
+      if (!warp_wait_b(smem_u32(&s.bar_item_full[slot]), (i >> 1) & 1, abort_flag)) break;
+      const BwdItem& item = s.item[slot];
+      const bool dkdv = item.dkdv != 0;
+      const int nt = item.nt, tile = item.tile, h = item.h, o0 = item.o0, L = item.L;
+      const int own_loc = tile * kBlock + r;
+      const bool valid = own_loc < L;
+      int lo[NINT], hi[NINT];
+      const uint8_t* iv_b = p.ivmask + static_cast<size_t>(item.b) * nt_all;
+      if (!dkdv)
+        load_row_intervals<NINT>(p.func, p.total, static_cast<int64_t>(o0) + own_loc, L, valid, lo, hi,
+                                 iv_b[tile]);
+      int buf = 0;
+      for (int it = 0; it < nt; ++it) {
+        const int other = item.idx[it] & 0xff;
+        const bool partial = (item.idx[it] & 0x100) != 0;
+        if (dkdv && partial) {
+          buf = fu & 1;
+          // This warp's 32 q rows of the visiting q tile; their visible bits
+          // over kv columns [hc, hc + 64) of tile `tile`, transposed by ballot.
+          int flo[NINT], fhi[NINT];
+          const int qi = other * kBlock + r;
+          load_row_intervals<NINT>(p.func, p.total, static_cast<int64_t>(o0) + qi, L, qi < L, flo, fhi,
+                                   iv_b[other]);
+          const uint32_t w0 = row_mask_word<NINT>(flo, fhi, tile * kBlock + hc);
+          const uint32_t w1 = row_mask_word<NINT>(flo, fhi, tile * kBlock + hc + 32);
+          uint32_t mine0 = 0, mine1 = 0;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const uint32_t b0 = __ballot_sync(0xffffffffu, (w0 >> j) & 1u);
-          const uint32_t b1 = __ballot_sync(0xffffffffu, (w1 >> j) & 1u);
-          if (lane == j) {
-            mine0 = b0;
-            mine1 = b1;
+          for (int j = 0; j < 32; ++j) {
+            const uint32_t b0 = __ballot_sync(0xffffffffu, (w0 >> j) & 1u);
+            const uint32_t b1 = __ballot_sync(0xffffffffu, (w1 >> j) & 1u);
+            if (lane == j) {
+              mine0 = b0;
+              mine1 = b1;
+            }
+          }
+          s.colmask[buf][quarter][hc + lane] = mine0;
+          s.colmask[buf][quarter][hc + 32 + lane] = mine1;
+          // Bounded hand-off between the 256 epilogue threads (an mbarrier, not
+          // bar.sync, so that an aborting warp cannot strand the others).
+          mbar_arrive(smem_u32(&s.bar_func[buf]));
+          if (!warp_wait_b(smem_u32(&s.bar_func[buf]), (fu >> 1) & 1, abort_flag)) { ok = false; break; }
+          ++fu;
+        }
+        const int g = g0 + it;
+        if (!warp_wait_b(smem_u32(&s.bar_s_full[hh]), g & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < 2; ++c) {
+          const int chunk = 2 * hh + c;  // 32-column chunk of S / dP (of the 128)
+          uint32_t sv[32], dv[32];
+          tmem_ld32(tS + lane_addr + chunk * 32, sv);
+          tmem_ld32(tdP + lane_addr + chunk * 32, dv);
+          tmem_ld_wait(sv);
+          tmem_ld_wait(dv);
+          uint32_t pp[16], pd[16];
+          if (partial) {  // item-uniform: full tiles run no mask arithmetic
+            const uint32_t mask =
+                dkdv ? s.colmask[buf][chunk][r] : row_mask_word<NINT>(lo, hi, other * kBlock + chunk * 32);
+            if (dkdv) epilogue32<true, true>(sv, dv, mask, half_alpha, pp, pd);
+            else epilogue32<true, false>(sv, dv, mask, half_alpha, pp, pd);
+          } else {
+            if (dkdv) epilogue32<false, true>(sv, dv, 0u, half_alpha, pp, pd);
+            else epilogue32<false, false>(sv, dv, 0u, half_alpha, pp, pd);
+          }
+          // Packed over columns [64h + 16c, 64h + 16c + 16), which this warp
+          // has already read: K-step ks of the half's accumulating MMA reads
+          // columns [64h + 8ks, 64h + 8ks + 8).
+          const uint32_t dst = lane_addr + hh * 64 + c * 16;
+          if (dkdv) {
+            tmem_st16(tS + dst, pp);
+            tmem_st16(tdP + dst, pd);
+          } else {
+            tmem_st16(tS + dst, pd);
           }
         }
-        s.colmask[buf][quarter][hc + lane] = mine0;
-        s.colmask[buf][quarter][hc + 32 + lane] = mine1;
-        // Bounded hand-off between the 256 epilogue threads (an mbarrier, not
-        // bar.sync, so that an aborting warp cannot strand the others).
-        mbar_arrive(smem_u32(&s.bar_func[buf]));
-        if (!warp_wait_b(smem_u32(&s.bar_func[buf]), (fu >> 1) & 1, abort_flag)) { ok = false; break; }
-        ++fu;
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&s.bar_p_full[hh]));
       }
-      if (!warp_wait_b(smem_u32(&s.bar_s_full[hh]), it & 1, abort_flag)) { ok = false; break; }
-      tc_fence_after();
-#pragma unroll 1
-      for (int c = 0; c < 2; ++c) {
-        const int chunk = 2 * hh + c;  // 32-column chunk of S / dP (of the 128)
-        uint32_t sv[32], dv[32];
-        tmem_ld32(tS + lane_addr + chunk * 32, sv);
-        tmem_ld32(tdP + lane_addr + chunk * 32, dv);
-        tmem_ld_wait(sv);
-        tmem_ld_wait(dv);
-        uint32_t pp[16], pd[16];
-        if (partial) {  // CTA-uniform: full tiles run no mask arithmetic
-          const uint32_t mask =
-              dkdv ? s.colmask[buf][chunk][r] : row_mask_word<NINT>(lo, hi, other * kBlock + chunk * 32);
-          if (dkdv) epilogue32<true, true>(sv, dv, mask, half_alpha, pp, pd);
-          else epilogue32<true, false>(sv, dv, mask, half_alpha, pp, pd);
-        } else {
-          if (dkdv) epilogue32<false, true>(sv, dv, 0u, half_alpha, pp, pd);
-          else epilogue32<false, false>(sv, dv, 0u, half_alpha, pp, pd);
-        }
-        // Packed over columns [64h + 16c, 64h + 16c + 16), which this warp
-        // has already read: K-step ks of the half's accumulating MMA reads
-        // columns [64h + 8ks, 64h + 8ks + 8).
-        const uint32_t dst = lane_addr + hh * 64 + c * 16;
-        if (dkdv) {
-          tmem_st16(tS + dst, pp);
-          tmem_st16(tdP + dst, pd);
-        } else {
-          tmem_st16(tS + dst, pd);
-        }
+      if (!ok) break;
+      if (nt > 0) {
+        if (!warp_wait_b(smem_u32(&s.bar_acc_full), acc_uses & 1, abort_flag)) break;
+        tc_fence_after();
       }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(smem_u32(&s.bar_p_full[hh]));
-    }
-    if (ok && nt > 0) ok = warp_wait_b(smem_u32(&s.bar_acc), 0, abort_flag);
-    tc_fence_after();
-    if (ok && !*abort_flag) {
-      const int64_t row = static_cast<int64_t>(row0 + r) * p.heads + h;
+      if (*abort_flag) break;
+      const int64_t row = static_cast<int64_t>(o0 + own_loc) * p.heads + h;
       if (dkdv) {
         store_acc_half<DP>(t_acc0 + lane_addr, half, nt > 0, valid, p.out2 + row * p.dim, p.dim,
                            out_scale);  // dV
         store_acc_half<DP>(t_acc1 + lane_addr, half, nt > 0, valid, p.out1 + row * p.dim, p.dim,
                            out_scale);  // dK
       } else {
-        store_acc_half<DP>(t_dq + lane_addr, half, nt > 0, valid, p.out0 + row * p.dim, p.dim,
+        store_acc_half<DP>(t_acc0 + lane_addr, half, nt > 0, valid, p.out0 + row * p.dim, p.dim,
                            out_scale);  // dQ
       }
+      if (nt > 0) {
+        tc_fence_before();
+        mbar_arrive(smem_u32(&s.bar_acc_empty));
+        ++acc_uses;
+      }
+      mbar_arrive(smem_u32(&s.bar_item_empty[slot]));
+      g0 += nt;
     }
   }
 
@@ -410,19 +506,6 @@ __device__ __forceinline__ void bwd_role(const AttnParams& p, BwdSmem<DP>& s, bo
 }
 
 template <int DP, int NINT>
-__global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant__ AttnParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  BwdSmem<DP>& s = smem_as_b<BwdSmem<DP>>(smem_raw);
-  const int item = blockIdx.x / p.heads, h = blockIdx.x - item * p.heads;
-  volatile int32_t* hdr = p.header;
-  if (item >= hdr[kHdrNBwd] || hdr[kHdrErr] != 0) return;
-  const int code = p.list[item];
-  const bool dkdv = (code & kRoleDkdv) != 0;
-  const int b = (code & ~kRoleDkdv) >> 8, tile = code & 255;
-  bwd_role<DP, NINT>(p, s, dkdv, b, tile, h);
-}
-
-template <int DP, int NINT>
 static cudaError_t launch_bwd_t(const AttnParams& p, int grid_items, cudaStream_t stream) {
   const int smem = static_cast<int>(sizeof(BwdSmem<DP>)) + 1024;
   static bool configured = false;
@@ -432,8 +515,13 @@ static cudaError_t launch_bwd_t(const AttnParams& p, int grid_items, cudaStream_
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  const long long ctas = 2LL * grid_items * p.heads;
-  if (ctas <= 0) return cudaSuccess;
+  const long long work = 2LL * grid_items * p.heads;
+  if (work <= 0) return cudaSuccess;
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const long long ctas = work < sms ? work : sms;  // persistent: one CTA per SM
   hstu_bwd_kernel<DP, NINT><<<static_cast<unsigned>(ctas), 320, smem, stream>>>(p);
   return cudaGetLastError();
 }

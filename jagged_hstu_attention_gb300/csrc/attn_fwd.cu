@@ -1,35 +1,47 @@
-// Forward kernel: one CTA per (work item = sequence b, q tile qt) and head h.
+// Forward kernel, persistent: one CTA per SM walks the work list (sequence
+// b, q tile qt, head h; longest sequences first) with a stride of the grid
+// size, and keeps every pipeline running across work items.
 //
-//   warp 8      TMA producer: Q tile once, then the K and V tiles of every
-//               visited kv tile into two rings of kStages (3 at D=128, 4 at
-//               D<=64); K runs one tile ahead and frees after QK^T, V after
-//               PV, which keeps the load latency off the critical path.
+//   warp 8      producer. All 32 lanes build the next item's list of visited
+//               kv tiles (from the plan's tile classes) into one of two item
+//               slots; lane 0 then loads the item's Q tile and the K and V
+//               tiles of every visited kv tile by TMA into two rings of
+//               kStages (3 at D=128, 4 at D<=64). K frees after QK^T, V after
+//               PV, so the next item's Q and K arrive while the current item
+//               finishes.
 //   warp 9      TMEM owner and MMA issuer (one elected lane):
-//                 S[it % 3] = Q K^T             (tcgen05, SMEM x SMEM)
-//                 O        += P[it % 3] V       (tcgen05, TMEM x SMEM)
-//               S runs two tiles ahead of PV, so the tensor core fills one S
-//               buffer while the epilogue groups work on the other two.
-//   warps 0-7   epilogue, two groups of four warps that ping-pong over the kv
-//               tiles: group g (warps 4g..4g+3, TMEM lanes 32(w%4)..) takes
-//               the tiles it with it % 2 == g (S buffer it % 3). Per
-//               tile: P' = S (1 + tanh(alpha S / 2)) (that is silu(alpha S)/N
-//               up to the factor alpha / (2N), applied once to O at the
-//               store), with the row's interval mask on partial tiles only
-//               (full tiles run no mask arithmetic), packed to bf16 in place
-//               over the first 64 columns of the buffer. While one group
-//               works on tile it the other works on tile it+1, so two tiles'
-//               TMEM-load / MUFU / TMEM-store latency chains overlap. At the
-//               end each group stores half of O's columns (bf16, rows past
-//               L_b left alone).
+//                 S[g % 3] = Q K^T             (tcgen05, SMEM x SMEM)
+//                 O       += P[g % 3] V        (tcgen05, TMEM x SMEM)
+//               with g the tile index counted over all items of the CTA. S
+//               runs two tiles ahead of PV, so the tensor core fills one S
+//               buffer while the epilogue groups work on the other two. The
+//               first PV of an item waits until the epilogue has read out the
+//               previous item's O.
+//   warps 0-7   epilogue, two groups of four warps that ping-pong over the
+//               tiles: group gr (warps 4gr..4gr+3, TMEM lanes 32(w%4)..) takes
+//               the tiles with g % 2 == gr. Per tile: P' = S (1 + tanh(alpha
+//               S / 2)) (that is silu(alpha S) / N up to the factor
+//               alpha / (2N), applied once to O at the store), with the row's
+//               interval mask on partial tiles only (full tiles run no mask
+//               arithmetic), packed to bf16 in place over the first 64
+//               columns of the buffer. At the end of an item each group
+//               stores half of O's columns (bf16, rows past L_b untouched;
+//               rows that see no column get zeros).
 //
 // TMEM (512 columns): S0 [0,128), S1 [128,256), S2 [256,384), O [384, 384+DP).
 // Packed P of buffer b occupies columns [128b, 128b+64).
 // SMEM: Q (DP/64 chunks of 128 rows x 128 B, 128-byte swizzle), K and V
-// stages of the same shape.
+// stages of the same shape, two item slots.
 #include "common.cuh"
 #include "internal.h"
 
 namespace hstu {
+
+// One work item as the producer publishes it to the other roles.
+struct FwdItem {
+  int b, qt, h, o0, L, nt;
+  uint16_t tile[kMaxTiles];  // visited kv tile index | 0x100 if partial
+};
 
 template <int DP>
 struct FwdSmem {
@@ -39,13 +51,12 @@ struct FwdSmem {
   alignas(1024) uint8_t q[kTile];
   alignas(1024) uint8_t k[kStages][kTile];
   alignas(1024) uint8_t v[kStages][kTile];
-  alignas(8) uint64_t bar_q, bar_k_full[kStages], bar_k_empty[kStages], bar_v_full[kStages],
-      bar_v_empty[kStages], bar_s_full[3], bar_p_full[3], bar_o_full;
+  alignas(8) uint64_t bar_q_full, bar_q_empty, bar_k_full[kStages], bar_k_empty[kStages],
+      bar_v_full[kStages], bar_v_empty[kStages], bar_s_full[3], bar_p_full[3], bar_o_full,
+      bar_o_empty, bar_item_full[2], bar_item_empty[2], bar_drain;
   uint32_t tmem_base;
   int abort_flag;
-  int n_tiles;
-  int16_t tile_j[kMaxTiles];
-  uint8_t tile_c[kMaxTiles];
+  FwdItem item[2];
 };
 
 template <typename S>
@@ -76,26 +87,47 @@ __device__ __forceinline__ void silu_pack32(const uint32_t (&s)[32], uint32_t ma
   }
 }
 
+// Epilogue of one 128 x 128 S tile for this warp's 32 rows (all 128 columns).
+template <int NINT, bool MASKED>
+__device__ __forceinline__ void fwd_tile_epilogue(uint32_t sb, int col0, const int (&lo)[NINT],
+                                                  const int (&hi)[NINT], float half_alpha) {
+#pragma unroll
+  for (int hf = 0; hf < 2; ++hf) {
+    uint32_t a[32], c[32];
+    tmem_ld32(sb + hf * 64, a);
+    tmem_ld32(sb + hf * 64 + 32, c);
+    tmem_ld_wait(a);
+    tmem_ld_wait(c);
+    uint32_t pa[16], pc[16];
+    silu_pack32<MASKED>(a, MASKED ? row_mask_word<NINT>(lo, hi, col0 + hf * 64) : 0u, half_alpha, pa);
+    silu_pack32<MASKED>(c, MASKED ? row_mask_word<NINT>(lo, hi, col0 + hf * 64 + 32) : 0u, half_alpha,
+                        pc);
+    // Packed over columns [32 hf, 32 hf + 32) of the buffer, which this warp
+    // has already read: K-step kk of the PV MMA reads [8kk, 8kk+8).
+    tmem_st16(sb + hf * 32, pa);
+    tmem_st16(sb + hf * 32 + 16, pc);
+  }
+}
+
 template <int DP, int NINT>
 __global__ void __launch_bounds__(320, 1) hstu_fwd_kernel(const __grid_constant__ AttnParams p) {
   using Smem = FwdSmem<DP>;
+  constexpr int NS = Smem::kStages;
+  constexpr int kTile = Smem::kTile;
+  constexpr int kChunkBytes = kBlock * 128;
   extern __shared__ uint8_t smem_raw[];
   Smem& s = smem_as<Smem>(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int item = blockIdx.x / p.heads, h = blockIdx.x - item * p.heads;
   volatile int32_t* hdr = p.header;
-  if (item >= hdr[kHdrNFwd] || hdr[kHdrErr] != 0) return;
-  const int code = p.list[item];
-  const int b = code >> 8, qt = code & 255;
-  const int o0 = p.seq_offsets[b];
-  const int L = p.seq_offsets[b + 1] - o0;
-  const int ntiles_b = (L + kBlock - 1) / kBlock;
-  const uint8_t* cls_row = p.cls + (static_cast<size_t>(b) * p.nt + qt) * p.nt;
+  if (hdr[kHdrErr] != 0) return;
+  const int n_work = hdr[kHdrNFwd] * p.heads;
+  if (static_cast<int>(blockIdx.x) >= n_work) return;
 
   if (threadIdx.x == 0) {
     s.abort_flag = 0;
-    mbar_init(smem_u32(&s.bar_q), 1);
-    for (int i = 0; i < Smem::kStages; ++i) {
+    mbar_init(smem_u32(&s.bar_q_full), 1);
+    mbar_init(smem_u32(&s.bar_q_empty), 1);
+    for (int i = 0; i < NS; ++i) {
       mbar_init(smem_u32(&s.bar_k_full[i]), 1);
       mbar_init(smem_u32(&s.bar_k_empty[i]), 1);
       mbar_init(smem_u32(&s.bar_v_full[i]), 1);
@@ -106,22 +138,13 @@ __global__ void __launch_bounds__(320, 1) hstu_fwd_kernel(const __grid_constant_
       mbar_init(smem_u32(&s.bar_p_full[i]), 128);
     }
     mbar_init(smem_u32(&s.bar_o_full), 1);
-    fence_mbar_init();
-  }
-  if (warp == 0) {  // compact list of visited kv tiles
-    int n = 0;
-    for (int base = 0; base < ntiles_b; base += 32) {
-      const int j = base + lane;
-      const uint8_t c = j < ntiles_b ? cls_row[j] : kSkip;
-      const unsigned m = __ballot_sync(0xffffffffu, c != kSkip);
-      if (c != kSkip) {
-        const int pos = n + __popc(m & ((1u << lane) - 1u));
-        s.tile_j[pos] = static_cast<int16_t>(j);
-        s.tile_c[pos] = c;
-      }
-      n += __popc(m);
+    mbar_init(smem_u32(&s.bar_o_empty), 256);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&s.bar_item_full[i]), 1);
+      mbar_init(smem_u32(&s.bar_item_empty[i]), 1 + 256);  // MMA issuer + epilogue threads
     }
-    if (lane == 0) s.n_tiles = n;
+    mbar_init(smem_u32(&s.bar_drain), 1);
+    fence_mbar_init();
   }
   if (warp == 9) {
     tmem_alloc(smem_u32(&s.tmem_base), 512);
@@ -132,55 +155,99 @@ __global__ void __launch_bounds__(320, 1) hstu_fwd_kernel(const __grid_constant_
   tc_fence_after();
   const uint32_t tbase = s.tmem_base;
   const uint32_t tO = tbase + 384;  // O accumulator columns [384, 384 + DP)
-  const int nt = s.n_tiles;
   volatile int* abort_flag = &s.abort_flag;
-  const int q_row0 = o0 + qt * kBlock;
-  constexpr int kTile = Smem::kTile;
-  constexpr int kChunkBytes = kBlock * 128;
+  const int stride = gridDim.x;
 
   if (warp == 8) {
     // ------------------------------------------------------------ producer
-    if (nt > 0 && elect_one_sync()) {
-      // K runs one tile ahead of V: a K stage frees as soon as its QK^T has
-      // completed, a V stage only after its PV, so the K load of a later
-      // tile never waits behind a V slot.
-      constexpr int NS = Smem::kStages;
-      int k_last[NS], v_last[NS];
-      for (int i = 0; i < NS; ++i) k_last[i] = v_last[i] = -1;
-      mbar_expect_tx(smem_u32(&s.bar_q), kTile);
-      for (int c = 0; c < Smem::kChunks; ++c)
-        tma_load_3d(smem_u32(s.q + c * kChunkBytes), &p.tm_q, smem_u32(&s.bar_q), c * 64, h, q_row0);
-      bool ok = true;
-      for (int it = 0; ok && it <= nt; ++it) {
-        if (it < nt) {  // K of tile it
-          const int st = it % NS, use = it / NS;
-          if (use > 0 && !mbar_wait(smem_u32(&s.bar_k_empty[st]), (use - 1) & 1, abort_flag)) {
-            ok = false;
-            break;
+    int k_last[NS], v_last[NS];
+    for (int i = 0; i < NS; ++i) k_last[i] = v_last[i] = -1;
+    int q_uses = 0;  // items with at least one tile (one Q load each)
+    int g = 0;       // tiles issued over all items
+    bool ok = true;
+    int i = 0;
+    for (int w = blockIdx.x; ok && w < n_work; w += stride, ++i) {
+      const int slot = i & 1;
+      if (i >= 2 && !warp_wait(smem_u32(&s.bar_item_empty[slot]), ((i >> 1) - 1) & 1, abort_flag)) {
+        ok = false;
+        break;
+      }
+      const int code = p.list[w / p.heads];
+      const int h = w % p.heads;
+      const int b = code >> 8, qt = code & 255;
+      const int o0 = p.seq_offsets[b];
+      const int L = p.seq_offsets[b + 1] - o0;
+      const int ntiles_b = (L + kBlock - 1) / kBlock;
+      const uint8_t* cls_row = p.cls + (static_cast<size_t>(b) * p.nt + qt) * p.nt;
+      FwdItem& it_slot = s.item[slot];
+      int n = 0;
+      for (int base = 0; base < ntiles_b; base += 32) {
+        const int j = base + lane;
+        const uint8_t c = j < ntiles_b ? cls_row[j] : kSkip;
+        const unsigned m = __ballot_sync(0xffffffffu, c != kSkip);
+        if (c != kSkip)
+          it_slot.tile[n + __popc(m & ((1u << lane) - 1u))] =
+              static_cast<uint16_t>(j | (c == kPartial ? 0x100 : 0));
+        n += __popc(m);
+      }
+      if (lane == 0) {
+        it_slot.b = b;
+        it_slot.qt = qt;
+        it_slot.h = h;
+        it_slot.o0 = o0;
+        it_slot.L = L;
+        it_slot.nt = n;
+      }
+      __threadfence_block();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_u32(&s.bar_item_full[slot]));
+        if (n > 0) {
+          if (q_uses > 0 && !mbar_wait(smem_u32(&s.bar_q_empty), (q_uses - 1) & 1, abort_flag)) ok = false;
+          if (ok) {
+            mbar_expect_tx(smem_u32(&s.bar_q_full), kTile);
+            for (int c = 0; c < Smem::kChunks; ++c)
+              tma_load_3d(smem_u32(s.q + c * kChunkBytes), &p.tm_q, smem_u32(&s.bar_q_full), c * 64, h,
+                          o0 + qt * kBlock);
+            ++q_uses;
           }
-          const uint32_t bar = smem_u32(&s.bar_k_full[st]);
-          mbar_expect_tx(bar, kTile);
-          const int kv_row0 = o0 + s.tile_j[it] * kBlock;
-          for (int c = 0; c < Smem::kChunks; ++c)
-            tma_load_3d(smem_u32(s.k[st] + c * kChunkBytes), &p.tm_k, bar, c * 64, h, kv_row0);
-          k_last[st] = use;
-        }
-        if (it >= 1) {  // V of tile it - 1
-          const int vi = it - 1, st = vi % NS, use = vi / NS;
-          if (use > 0 && !mbar_wait(smem_u32(&s.bar_v_empty[st]), (use - 1) & 1, abort_flag)) {
-            ok = false;
-            break;
+          // K runs one tile ahead of V within the item.
+          for (int t = 0; ok && t <= n; ++t) {
+            if (t < n) {
+              const int gg = g + t, st = gg % NS, use = gg / NS;
+              if (use > 0 && !mbar_wait(smem_u32(&s.bar_k_empty[st]), (use - 1) & 1, abort_flag)) {
+                ok = false;
+                break;
+              }
+              const uint32_t bar = smem_u32(&s.bar_k_full[st]);
+              mbar_expect_tx(bar, kTile);
+              const int row = o0 + (it_slot.tile[t] & 0xff) * kBlock;
+              for (int c = 0; c < Smem::kChunks; ++c)
+                tma_load_3d(smem_u32(s.k[st] + c * kChunkBytes), &p.tm_k, bar, c * 64, h, row);
+              k_last[st] = use;
+            }
+            if (t >= 1) {
+              const int gg = g + t - 1, st = gg % NS, use = gg / NS;
+              if (use > 0 && !mbar_wait(smem_u32(&s.bar_v_empty[st]), (use - 1) & 1, abort_flag)) {
+                ok = false;
+                break;
+              }
+              const uint32_t bar = smem_u32(&s.bar_v_full[st]);
+              mbar_expect_tx(bar, kTile);
+              const int row = o0 + (it_slot.tile[t - 1] & 0xff) * kBlock;
+              for (int c = 0; c < Smem::kChunks; ++c)
+                tma_load_3d(smem_u32(s.v[st] + c * kChunkBytes), &p.tm_v, bar, c * 64, h, row);
+              v_last[st] = use;
+            }
           }
-          const uint32_t bar = smem_u32(&s.bar_v_full[st]);
-          mbar_expect_tx(bar, kTile);
-          const int kv_row0 = o0 + s.tile_j[vi] * kBlock;
-          for (int c = 0; c < Smem::kChunks; ++c)
-            tma_load_3d(smem_u32(s.v[st] + c * kChunkBytes), &p.tm_v, bar, c * 64, h, kv_row0);
-          v_last[st] = use;
+          g += n;
         }
       }
-      // Never leave with a copy in flight.
-      mbar_wait_drain(smem_u32(&s.bar_q), 0);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    }
+    // Never leave with a copy in flight.
+    if (lane == 0) {
+      if (q_uses > 0) mbar_wait_drain(smem_u32(&s.bar_q_full), (q_uses - 1) & 1);
       for (int st = 0; st < NS; ++st) {
         if (k_last[st] >= 0) mbar_wait_drain(smem_u32(&s.bar_k_full[st]), k_last[st] & 1);
         if (v_last[st] >= 0) mbar_wait_drain(smem_u32(&s.bar_v_full[st]), v_last[st] & 1);
@@ -189,106 +256,120 @@ __global__ void __launch_bounds__(320, 1) hstu_fwd_kernel(const __grid_constant_
     __syncwarp();
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    if (nt > 0 && elect_one_sync()) {
+    if (elect_one_sync()) {
       constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
       constexpr uint32_t idesc_o = idesc_bf16(128, DP, false, true);
       // Descriptors are built once; each MMA only advances a start address.
       const uint64_t dq = sdesc_sw128(smem_u32(s.q), 16, 1024);
       const uint64_t dk0 = sdesc_sw128(smem_u32(s.k[0]), 16, 1024);
       const uint64_t dv0 = sdesc_sw128(smem_u32(s.v[0]), kChunkBytes, 1024);
-      bool ok = mbar_wait(smem_u32(&s.bar_q), 0, abort_flag);
-      tc_fence_after();
-      // S runs two tiles ahead of PV: S(it) goes into buffer it % 3, whose
-      // previous tile it - 3 was consumed by a PV issued before it.
-      for (int it = 0; ok && it <= nt + 1; ++it) {
-        if (it < nt) {
-          const int kst = it % Smem::kStages, kuse = it / Smem::kStages, sb = it % 3;
-          if (!mbar_wait(smem_u32(&s.bar_k_full[kst]), kuse & 1, abort_flag)) break;
-          tc_fence_after();
-          const uint64_t dk = sdesc_advance(dk0, kst * kTile);
-          const uint32_t d_tmem = tbase + sb * 128;
+      int g = 0;       // tiles over all items
+      int q_uses = 0;  // items with at least one tile
+      bool ok = true;
+      int i = 0;
+      for (int w = blockIdx.x; ok && w < n_work; w += stride, ++i) {
+        const int slot = i & 1;
+        if (!mbar_wait(smem_u32(&s.bar_item_full[slot]), (i >> 1) & 1, abort_flag)) break;
+        const int nt = s.item[slot].nt;
+        mbar_arrive(smem_u32(&s.bar_item_empty[slot]));
+        if (nt == 0) continue;
+        if (!mbar_wait(smem_u32(&s.bar_q_full), q_uses & 1, abort_flag)) break;
+        tc_fence_after();
+        // S runs two tiles ahead of PV: S(g) goes into buffer g % 3, whose
+        // previous tile g - 3 was consumed by a PV issued before it.
+        for (int t = 0; t <= nt + 1; ++t) {
+          if (t < nt) {
+            const int gg = g + t, kst = gg % NS, sb = gg % 3;
+            if (!mbar_wait(smem_u32(&s.bar_k_full[kst]), (gg / NS) & 1, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            const uint64_t dk = sdesc_advance(dk0, kst * kTile);
+            const uint32_t d_tmem = tbase + sb * 128;
 #pragma unroll
-          for (int kk = 0; kk < DP / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-            umma_ss(d_tmem, sdesc_advance(dq, off), sdesc_advance(dk, off), idesc_s, kk > 0);
+            for (int kk = 0; kk < DP / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+              umma_ss(d_tmem, sdesc_advance(dq, off), sdesc_advance(dk, off), idesc_s, kk > 0);
+            }
+            umma_commit(smem_u32(&s.bar_s_full[sb]));
+            umma_commit(smem_u32(&s.bar_k_empty[kst]));  // K stage free once QK^T is done
+            if (t == nt - 1) umma_commit(smem_u32(&s.bar_q_empty));  // Q free for the next item
           }
-          umma_commit(smem_u32(&s.bar_s_full[sb]));
-          umma_commit(smem_u32(&s.bar_k_empty[kst]));  // K stage free once QK^T is done
-        }
-        if (it >= 2 && it - 2 < nt) {
-          const int pi = it - 2, psb = pi % 3, puse = pi / 3, pkst = pi % Smem::kStages;
-          if (!mbar_wait(smem_u32(&s.bar_v_full[pkst]), (pi / Smem::kStages) & 1, abort_flag)) break;
-          if (!mbar_wait(smem_u32(&s.bar_p_full[psb]), puse & 1, abort_flag)) break;
-          tc_fence_after();
-          const uint64_t dv = sdesc_advance(dv0, pkst * kTile);
-          const uint32_t a_tmem = tbase + psb * 128;
-          const uint32_t first = pi > 0 ? 1u : 0u;
-          umma_ts(tO, a_tmem, dv, idesc_o, first);
+          if (t >= 2) {
+            const int pt = t - 2, gg = g + pt, psb = gg % 3, pkst = gg % NS;
+            if (pt == 0 && q_uses > 0 &&
+                !mbar_wait(smem_u32(&s.bar_o_empty), (q_uses - 1) & 1, abort_flag)) {
+              ok = false;  // the previous item's O has not been read out
+              break;
+            }
+            if (!mbar_wait(smem_u32(&s.bar_v_full[pkst]), (gg / NS) & 1, abort_flag) ||
+                !mbar_wait(smem_u32(&s.bar_p_full[psb]), (gg / 3) & 1, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t dv = sdesc_advance(dv0, pkst * kTile);
+            const uint32_t a_tmem = tbase + psb * 128;
+            umma_ts(tO, a_tmem, dv, idesc_o, pt > 0 ? 1u : 0u);
 #pragma unroll
-          for (int kk = 1; kk < kBlock / 16; ++kk)
-            umma_ts(tO, a_tmem + kk * 8, sdesc_advance(dv, kk * 16 * 128), idesc_o, 1u);
-          umma_commit(smem_u32(&s.bar_v_empty[pkst]));
+            for (int kk = 1; kk < kBlock / 16; ++kk)
+              umma_ts(tO, a_tmem + kk * 8, sdesc_advance(dv, kk * 16 * 128), idesc_o, 1u);
+            umma_commit(smem_u32(&s.bar_v_empty[pkst]));
+          }
         }
+        if (!ok) break;
+        umma_commit(smem_u32(&s.bar_o_full));
+        g += nt;
+        ++q_uses;
       }
       // Arrives once every MMA issued above has completed (also on abort).
-      umma_commit(smem_u32(&s.bar_o_full));
-      mbar_wait_drain(smem_u32(&s.bar_o_full), 0);
+      umma_commit(smem_u32(&s.bar_drain));
+      mbar_wait_drain(smem_u32(&s.bar_drain), 0);
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    const int quarter = warp & 3, half = warp >> 2;
-    const int r = quarter * 32 + lane;  // q row within the tile == TMEM lane
-    const int i_loc = qt * kBlock + r;
-    const bool valid = i_loc < L;
-    int lo[NINT], hi[NINT];
-    load_row_intervals<NINT>(p.func, p.total, static_cast<int64_t>(o0) + i_loc, L, valid, lo, hi);
+    const int quarter = warp & 3, grp = warp >> 2;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     const float half_alpha = 0.5f * p.alpha;
     const float out_scale = 0.5f * p.alpha * p.inv_n;  // hc = alpha / (2N)
+    const int r = quarter * 32 + lane;                 // q row within the tile == TMEM lane
+    int g = 0, o_uses = 0;
     bool ok = true;
-    // Ping-pong: warp group `half` takes the tiles it with it % 2 == half;
-    // tile it lives in S buffer it % 3, so two tiles' epilogues run at the
-    // same time while the tensor core fills the third buffer.
-    for (int it = half; it < nt; it += 2) {
-      const int sbuf = it % 3, use = it / 3;
-      if (!warp_wait(smem_u32(&s.bar_s_full[sbuf]), use & 1, abort_flag)) { ok = false; break; }
-      tc_fence_after();
-      const int col0 = s.tile_j[it] * kBlock;
-      const bool partial = s.tile_c[it] == kPartial;
-      const uint32_t sb = tbase + lane_addr + sbuf * 128;
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        uint32_t a[32], c[32];
-        tmem_ld32(sb + hf * 64, a);
-        tmem_ld32(sb + hf * 64 + 32, c);
-        tmem_ld_wait(a);
-        tmem_ld_wait(c);
-        uint32_t pa[16], pc[16];
-        if (partial) {  // CTA-uniform: full tiles run no mask arithmetic
-          silu_pack32<true>(a, row_mask_word<NINT>(lo, hi, col0 + hf * 64), half_alpha, pa);
-          silu_pack32<true>(c, row_mask_word<NINT>(lo, hi, col0 + hf * 64 + 32), half_alpha, pc);
-        } else {
-          silu_pack32<false>(a, 0u, half_alpha, pa);
-          silu_pack32<false>(c, 0u, half_alpha, pc);
-        }
-        // Packed over columns [32 hf, 32 hf + 32) of the buffer, which this
-        // warp has already read: K-step kk of the PV MMA reads [8kk, 8kk+8).
-        tmem_st16(sb + hf * 32, pa);
-        tmem_st16(sb + hf * 32 + 16, pc);
+    int i = 0;
+    for (int w = blockIdx.x; ok && w < n_work; w += stride, ++i) {
+      const int slot = i & 1;
+      if (!warp_wait(smem_u32(&s.bar_item_full[slot]), (i >> 1) & 1, abort_flag)) break;
+      const FwdItem& item = s.item[slot];
+      const int nt = item.nt, qt = item.qt, h = item.h, o0 = item.o0, L = item.L;
+      const int i_loc = qt * kBlock + r;
+      const bool valid = i_loc < L;
+      int lo[NINT], hi[NINT];
+      const uint32_t active = p.ivmask[static_cast<size_t>(item.b) * p.nt + qt];
+      load_row_intervals<NINT>(p.func, p.total, static_cast<int64_t>(o0) + i_loc, L, valid, lo, hi, active);
+      // Ping-pong: this group takes the tiles with g % 2 == grp.
+      for (int t = (g & 1) == grp ? 0 : 1; t < nt; t += 2) {
+        const int gg = g + t, sbuf = gg % 3;
+        if (!warp_wait(smem_u32(&s.bar_s_full[sbuf]), (gg / 3) & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        const int tile = item.tile[t];
+        const uint32_t sb = tbase + lane_addr + sbuf * 128;
+        if (tile & 0x100) fwd_tile_epilogue<NINT, true>(sb, (tile & 0xff) * kBlock, lo, hi, half_alpha);
+        else fwd_tile_epilogue<NINT, false>(sb, (tile & 0xff) * kBlock, lo, hi, half_alpha);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&s.bar_p_full[sbuf]));
       }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(smem_u32(&s.bar_p_full[sbuf]));
-    }
-    if (ok && nt > 0) ok = warp_wait(smem_u32(&s.bar_o_full), 0, abort_flag);
-    tc_fence_after();
-    if (ok && !*abort_flag) {
+      if (!ok) break;
+      if (nt > 0) {
+        if (!warp_wait(smem_u32(&s.bar_o_full), o_uses & 1, abort_flag)) break;
+        tc_fence_after();
+      }
+      if (*abort_flag) break;
       constexpr int kHalfCols = DP / 2;
-      __nv_bfloat16* dst = p.out0 + (static_cast<int64_t>(q_row0 + r) * p.heads + h) * p.dim;
+      __nv_bfloat16* dst =
+          p.out0 + (static_cast<int64_t>(o0 + qt * kBlock + r) * p.heads + h) * p.dim;
 #pragma unroll
       for (int cc = 0; cc < kHalfCols / 32; ++cc) {
-        const int col = half * kHalfCols + cc * 32;
+        const int col = grp * kHalfCols + cc * 32;
         uint32_t v32[32];
         if (nt > 0) {
           tmem_ld32(tO + lane_addr + col, v32);
@@ -309,6 +390,13 @@ __global__ void __launch_bounds__(320, 1) hstu_fwd_kernel(const __grid_constant_
             d4[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
         }
       }
+      if (nt > 0) {
+        tc_fence_before();
+        mbar_arrive(smem_u32(&s.bar_o_empty));
+        ++o_uses;
+      }
+      mbar_arrive(smem_u32(&s.bar_item_empty[slot]));
+      g += nt;
     }
   }
 
@@ -321,6 +409,14 @@ __global__ void __launch_bounds__(320, 1) hstu_fwd_kernel(const __grid_constant_
   if (threadIdx.x == 0 && s.abort_flag) atomicOr(p.header + kHdrErr, kErrTimeout);
 }
 
+// Number of SMs of the current device (looked up per call; cheap).
+static cudaError_t sm_count(int* sms) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  return cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev);
+}
+
 template <int DP, int NINT>
 static cudaError_t launch_fwd_t(const AttnParams& p, int grid_items, cudaStream_t stream) {
   const int smem = static_cast<int>(sizeof(FwdSmem<DP>)) + 1024;
@@ -331,8 +427,12 @@ static cudaError_t launch_fwd_t(const AttnParams& p, int grid_items, cudaStream_
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  const long long ctas = static_cast<long long>(grid_items) * p.heads;
-  if (ctas <= 0) return cudaSuccess;
+  const long long work = static_cast<long long>(grid_items) * p.heads;
+  if (work <= 0) return cudaSuccess;
+  int sms = 0;
+  cudaError_t e = sm_count(&sms);
+  if (e != cudaSuccess) return e;
+  const long long ctas = work < sms ? work : sms;  // persistent: one CTA per SM
   hstu_fwd_kernel<DP, NINT><<<static_cast<unsigned>(ctas), 320, smem, stream>>>(p);
   return cudaGetLastError();
 }

@@ -40,7 +40,7 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 struct FullLayout {
   int nt = 0;  // tiles per sequence at max_seqlen
   size_t header = 0, qvis = 0, kvvis = 0, zero_bytes = 0, fwd_list = 0, bwd_list = 0, seq_order = 0,
-         seq_start = 0, cls = 0, total = 0;
+         seq_start = 0, ivmask = 0, cls = 0, total = 0;
 };
 inline FullLayout full_layout(int batch, int max_seqlen) {
   FullLayout l;
@@ -54,7 +54,8 @@ inline FullLayout full_layout(int batch, int max_seqlen) {
   l.bwd_list = l.fwd_list + align_up(items * 4, 256);
   l.seq_order = l.bwd_list + align_up(2 * items * 4, 256);
   l.seq_start = l.seq_order + align_up(static_cast<size_t>(batch) * 4, 256);
-  l.cls = l.seq_start + align_up(static_cast<size_t>(batch) * 4, 256);
+  l.ivmask = l.seq_start + align_up(static_cast<size_t>(batch) * 4, 256);
+  l.cls = l.ivmask + align_up(items, 256);
   l.total = l.cls + align_up(items * l.nt, 256);
   return l;
 }
@@ -85,6 +86,7 @@ struct PlanParams {
   int32_t* bwd_list;
   int32_t* seq_order;  // sequences, longest first
   int32_t* seq_start;  // first work item of each sorted sequence
+  uint8_t* ivmask;     // per q tile: bit t set iff interval t is non-empty for some row
   uint8_t* cls;
   int64_t total;
   int32_t batch, nfunc, nt, max_seqlen;
@@ -98,6 +100,7 @@ struct AttnParams {
   __nv_bfloat16* out1;  // bwd: dk
   __nv_bfloat16* out2;  // bwd: dv
   const uint8_t* cls;
+  const uint8_t* ivmask;
   const int32_t* list;
   int32_t* header;
   int64_t total;
@@ -125,15 +128,17 @@ struct TgtParams {
 
 // ---------------------------------------------------------------- func decode
 // Clamped intervals of one row; an empty interval becomes [0, 0) so that it
-// can never widen a bound or pass a membership test.
+// can never widen a bound or pass a membership test. Intervals whose bit is
+// clear in `active` (empty for every row of the tile, as the plan found) are
+// not read at all.
 template <int NINT>
 __device__ __forceinline__ void load_row_intervals(const int32_t* __restrict__ func, int64_t total,
                                                    int64_t row, int L, bool valid, int (&lo)[NINT],
-                                                   int (&hi)[NINT]) {
+                                                   int (&hi)[NINT], uint32_t active = 0xffu) {
 #pragma unroll
   for (int t = 0; t < NINT; ++t) {
     int a = 0, e = 0;
-    if (valid) {
+    if (valid && ((active >> t) & 1u)) {
       a = (t == 0) ? 0 : __ldg(func + static_cast<int64_t>(2 * t - 1) * total + row);
       e = __ldg(func + static_cast<int64_t>(2 * t) * total + row);
       a = min(max(a, 0), L);

@@ -39,6 +39,8 @@ __global__ void __launch_bounds__(128) plan_classify_kernel(const PlanParams p) 
   __shared__ uint32_t any_bits[4][kMaxTiles / 32];
   __shared__ uint32_t all_bits[4][kMaxTiles / 32];
   __shared__ int n_visit;
+  __shared__ uint32_t active_iv;
+  if (tid == 0) active_iv = 0;
   for (int x = tid; x < 4 * (kMaxTiles / 32); x += 128) {
     (&any_bits[0][0])[x] = 0;
     (&all_bits[0][0])[x] = 0;
@@ -50,6 +52,11 @@ __global__ void __launch_bounds__(128) plan_classify_kernel(const PlanParams p) 
   const bool valid = i < L;
   int lo[NINT], hi[NINT];
   load_row_intervals<NINT>(p.func, p.total, static_cast<int64_t>(o0) + i, L, valid, lo, hi);
+  uint32_t nonempty = 0;
+#pragma unroll
+  for (int t = 0; t < NINT; ++t) nonempty |= (hi[t] > lo[t] ? 1u : 0u) << t;
+  nonempty = __reduce_or_sync(0xffffffffu, nonempty);
+  if (lane == 0 && nonempty) atomicOr(&active_iv, nonempty);
 
   int count = 0;
   for (int j = 0; j < ntiles; ++j) {
@@ -85,7 +92,10 @@ __global__ void __launch_bounds__(128) plan_classify_kernel(const PlanParams p) 
   }
   if (mine) atomicAdd(&n_visit, mine);
   __syncthreads();
-  if (tid == 0) p.qvis[static_cast<size_t>(b) * p.nt + qt] = n_visit;
+  if (tid == 0) {
+    p.qvis[static_cast<size_t>(b) * p.nt + qt] = n_visit;
+    p.ivmask[static_cast<size_t>(b) * p.nt + qt] = static_cast<uint8_t>(active_iv);
+  }
 }
 
 // Exclusive scan of cnt[0..n) in place (one block of 1024 threads).
