@@ -36,10 +36,10 @@ UNIT = "TFLOP/s"
 DEFAULT_CONFIG = "sla_b32_s1024"
 L2_FLUSH_BYTES = 512 << 20
 
-# DRAM bytes per launch of the backward kernel from an ncu capture, with the
-# hash of the kernel sources they were taken on (the value is reported only
-# while the sources are unchanged). Filled from profiles/.
-NCU_TRAFFIC = {"bwd": None, "sources_sha": None}
+# DRAM bytes (read + write) per launch of the backward kernel on the default
+# workload, from one ncu capture of that kernel, with the hash of the kernel
+# sources it was taken on; reported only while the sources are unchanged.
+NCU_TRAFFIC = {"bwd": 134827520 + 64033024, "sources_sha": "1a6cef63749c3b0d"}
 
 
 def kernel_sources_sha() -> str:
@@ -318,14 +318,19 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default=DEFAULT_CONFIG)
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the workload's batch size (small profiling cases only)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
+    import dataclasses
     from jagged_hstu_attention_gb300 import workloads as wl
     cfg = wl.CONFIGS[args.config]
+    if args.batch is not None:
+        cfg = dataclasses.replace(cfg, batch=args.batch, name=f"{cfg.name}@b{args.batch}")
     if args.impl == "reference":
         run_reference(args, cfg)
         return

@@ -288,9 +288,8 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
     // ------------------------------------------------------------ MMA issuer
     if (elect_one_sync()) {
       // Half-tile pipeline: step u covers the 64-column half (u & 1) of tile
-      // u >> 1. S/dP of step u go into TMEM half (u & 1) while the epilogue
-      // works on step u - 1 in the other half; the accumulating MMAs of step
-      // u - 1 follow as soon as its packed P/dS are in place.
+      // u >> 1. While the epilogue works on one half, the tensor core runs
+      // the accumulating MMAs of the other half and S/dP two steps ahead.
       constexpr uint32_t idesc_s = idesc_bf16(128, 64, false, false);
       constexpr uint32_t idesc_acc = idesc_bf16(128, DP, false, true);
       // Descriptors are built once; each MMA only advances a start address.
@@ -314,56 +313,62 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
         if (!mbar_wait(smem_u32(&s.bar_res_full), res_uses & 1, abort_flag)) break;
         tc_fence_after();
         const int nsteps = 2 * nt;
-        for (int u = 0; u <= nsteps; ++u) {
-          if (u < nsteps) {
-            const int g = gs + (u >> 1), hh = u & 1, st = g & 1;
-            if (hh == 0) {
-              if (!mbar_wait(smem_u32(&s.bar_full[st]), (g >> 1) & 1, abort_flag)) { ok = false; break; }
-              tc_fence_after();
-            }
-            // S (or S^T) = res0 . str0_h^T ; dP (or dP^T) = res1 . str1_h^T, N = 64
-            const uint32_t hoff = st * kTile + hh * 64 * 128;
-            const uint64_t b0 = sdesc_advance(ds0, hoff), b1 = sdesc_advance(ds1, hoff);
-#pragma unroll
-            for (int kk = 0; kk < DP / 16; ++kk) {
-              const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-              umma_ss(tS + hh * 64, sdesc_advance(dr0, off), sdesc_advance(b0, off), idesc_s, kk > 0);
-            }
-#pragma unroll
-            for (int kk = 0; kk < DP / 16; ++kk) {
-              const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-              umma_ss(tdP + hh * 64, sdesc_advance(dr1, off), sdesc_advance(b1, off), idesc_s, kk > 0);
-            }
-            umma_commit(smem_u32(&s.bar_s_full[hh]));
-            if (u == nsteps - 1) umma_commit(smem_u32(&s.bar_res_empty));  // residents free
-          }
-          if (u >= 1) {
-            const int pu = u - 1, pit = pu >> 1, ph = pu & 1, g = gs + pit, pst = g & 1;
-            if (pu == 0 && res_uses > 0 &&
-                !mbar_wait(smem_u32(&s.bar_acc_empty), (res_uses - 1) & 1, abort_flag)) {
-              ok = false;  // the previous item's accumulators have not been read out
-              break;
-            }
-            if (!mbar_wait(smem_u32(&s.bar_p_full[ph]), g & 1, abort_flag)) { ok = false; break; }
+        // S/dP of step u (64-column half u & 1 of tile u >> 1, N = 64 MMAs)
+        // into TMEM half u & 1: S (or S^T) = res0 . str0_h^T,
+        // dP (or dP^T) = res1 . str1_h^T.
+        auto issue_sdp = [&](int u) -> bool {
+          const int g = gs + (u >> 1), hh = u & 1, st = g & 1;
+          if (hh == 0) {
+            if (!mbar_wait(smem_u32(&s.bar_full[st]), (g >> 1) & 1, abort_flag)) return false;
             tc_fence_after();
-            const uint32_t boff0 = pst * kTile + ph * 64 * 128;
-            const uint64_t m0 = sdesc_advance(ds0_mn, boff0), m1 = sdesc_advance(ds1_mn, boff0);
-            const uint32_t first = (pit > 0 || ph > 0) ? 1u : 0u;
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {  // K = the 64 rows of this half
-              const uint32_t acol = ph * 64 + ks * 8;
-              const uint32_t acc = ks > 0 ? 1u : first;
-              if (dkdv) {
-                // dV += P^T dO (dO = str1, MN-major); dK += dS^T Q (Q = str0, MN-major)
-                umma_ts(t_acc0, tS + acol, sdesc_advance(m1, ks * 16 * 128), idesc_acc, acc);
-                umma_ts(t_acc1, tdP + acol, sdesc_advance(m0, ks * 16 * 128), idesc_acc, acc);
-              } else {
-                // dQ += dS K (K = str0, MN-major)
-                umma_ts(t_acc0, tS + acol, sdesc_advance(m0, ks * 16 * 128), idesc_acc, acc);
-              }
-            }
-            if (ph == 1) umma_commit(smem_u32(&s.bar_empty[pst]));
           }
+          const uint32_t hoff = st * kTile + hh * 64 * 128;
+          const uint64_t b0 = sdesc_advance(ds0, hoff), b1 = sdesc_advance(ds1, hoff);
+#pragma unroll
+          for (int kk = 0; kk < DP / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+            umma_ss(tS + hh * 64, sdesc_advance(dr0, off), sdesc_advance(b0, off), idesc_s, kk > 0);
+          }
+#pragma unroll
+          for (int kk = 0; kk < DP / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+            umma_ss(tdP + hh * 64, sdesc_advance(dr1, off), sdesc_advance(b1, off), idesc_s, kk > 0);
+          }
+          umma_commit(smem_u32(&s.bar_s_full[hh]));
+          if (u == nsteps - 1) umma_commit(smem_u32(&s.bar_res_empty));  // residents free
+          return true;
+        };
+        // S/dP run two steps ahead of the accumulating MMAs: S/dP of step
+        // u + 2 reuse the TMEM half of step u, whose packed P/dS the
+        // accumulating MMAs of step u (issued just before, in order) read.
+        ok = issue_sdp(0) && issue_sdp(1);
+        for (int u = 0; ok && u < nsteps; ++u) {
+          const int pit = u >> 1, ph = u & 1, g = gs + pit, pst = g & 1;
+          if (u == 0 && res_uses > 0 &&
+              !mbar_wait(smem_u32(&s.bar_acc_empty), (res_uses - 1) & 1, abort_flag)) {
+            ok = false;  // the previous item's accumulators have not been read out
+            break;
+          }
+          if (!mbar_wait(smem_u32(&s.bar_p_full[ph]), g & 1, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t boff0 = pst * kTile + ph * 64 * 128;
+          const uint64_t m0 = sdesc_advance(ds0_mn, boff0), m1 = sdesc_advance(ds1_mn, boff0);
+          const uint32_t first = (pit > 0 || ph > 0) ? 1u : 0u;
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {  // K = the 64 rows of this half
+            const uint32_t acol = ph * 64 + ks * 8;
+            const uint32_t acc = ks > 0 ? 1u : first;
+            if (dkdv) {
+              // dV += P^T dO (dO = str1, MN-major); dK += dS^T Q (Q = str0, MN-major)
+              umma_ts(t_acc0, tS + acol, sdesc_advance(m1, ks * 16 * 128), idesc_acc, acc);
+              umma_ts(t_acc1, tdP + acol, sdesc_advance(m0, ks * 16 * 128), idesc_acc, acc);
+            } else {
+              // dQ += dS K (K = str0, MN-major)
+              umma_ts(t_acc0, tS + acol, sdesc_advance(m0, ks * 16 * 128), idesc_acc, acc);
+            }
+          }
+          if (ph == 1) umma_commit(smem_u32(&s.bar_empty[pst]));
+          if (u + 2 < nsteps && !issue_sdp(u + 2)) ok = false;
         }
         if (!ok) break;
         umma_commit(smem_u32(&s.bar_acc_full));

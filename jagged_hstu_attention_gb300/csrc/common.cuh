@@ -192,17 +192,17 @@ __device__ __forceinline__ float silu_pu(float s, float half_alpha) {
 __device__ __forceinline__ void silu_pu_gu(float s, float dp, float half_alpha, float& p, float& g) {
   const float h = half_alpha * s;
   const float t = tanh_approx(h);
-  p = fmaf(s, t, s);
-  const float a = 1.0f + t;
-  const float f = fmaf(-h, t, h + 1.0f);
-  g = (dp * a) * f;
+  p = fmaf(s, t, s);                      // s (1 + t)
+  const float u = fmaf(dp, t, dp);        // dP (1 + t)
+  const float f = fmaf(-h, t, h + 1.0f);  // 1 + h - h t
+  g = u * f;
 }
 __device__ __forceinline__ float silu_gu(float s, float dp, float half_alpha) {
   const float h = half_alpha * s;
   const float t = tanh_approx(h);
-  const float a = 1.0f + t;
+  const float u = fmaf(dp, t, dp);
   const float f = fmaf(-h, t, h + 1.0f);
-  return (dp * a) * f;
+  return u * f;
 }
 
 }  // namespace hstu
