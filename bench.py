@@ -170,7 +170,7 @@ class Leg:
         ev[3].record()
 
 
-LAUNCHES_PER_STEP = 4  # plan classify + plan sort + forward + backward
+LAUNCHES_PER_STEP = 3  # plan (classify + work lists) + forward + backward
 
 
 def time_legs(legs, steps, warmup, flush):

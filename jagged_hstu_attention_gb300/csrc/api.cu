@@ -44,16 +44,17 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // (tokens, H, D) bf16 viewed as a 3-D tensor {D, H, tokens}; box = 64
-// columns x 1 head x 128 rows with 128-byte swizzle. For D = 32 the box is
+// columns x 1 head x box_rows rows with 128-byte swizzle. For D = 32 the box is
 // wider than the tensor and TMA fills the missing columns with zeros.
-bool make_map(CUtensorMap* m, const void* ptr, int64_t tokens, int heads, int dim) {
+bool make_map(CUtensorMap* m, const void* ptr, int64_t tokens, int heads, int dim,
+              int box_rows = kBlock) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(dim), static_cast<cuuint64_t>(heads),
                         static_cast<cuuint64_t>(tokens)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(dim) * 2,
                            static_cast<cuuint64_t>(heads) * dim * 2};
-  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(kBlock)};
+  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(box_rows)};
   cuuint32_t es[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -83,8 +84,6 @@ hstu::PlanParams plan_params(const int32_t* seq_offsets, const int32_t* func,
   p.func = func;
   p.row_counts = row_counts;
   p.header = reinterpret_cast<int32_t*>(base + l.header);
-  p.qvis = reinterpret_cast<int32_t*>(base + l.qvis);
-  p.kvvis = reinterpret_cast<int32_t*>(base + l.kvvis);
   p.fwd_list = reinterpret_cast<int32_t*>(base + l.fwd_list);
   p.bwd_list = reinterpret_cast<int32_t*>(base + l.bwd_list);
   p.seq_order = reinterpret_cast<int32_t*>(base + l.seq_order);
@@ -204,7 +203,11 @@ hstu_status_t hstu_attn_bwd(const void* dout, const void* q, const void* k, cons
   if (!make_map(&p.tm_q, q, shape->total, shape->num_heads, shape->head_dim) ||
       !make_map(&p.tm_k, k, shape->total, shape->num_heads, shape->head_dim) ||
       !make_map(&p.tm_v, v, shape->total, shape->num_heads, shape->head_dim) ||
-      !make_map(&p.tm_do, dout, shape->total, shape->num_heads, shape->head_dim))
+      !make_map(&p.tm_do, dout, shape->total, shape->num_heads, shape->head_dim) ||
+      !make_map(&p.tm_q64, q, shape->total, shape->num_heads, shape->head_dim, kBlock / 2) ||
+      !make_map(&p.tm_k64, k, shape->total, shape->num_heads, shape->head_dim, kBlock / 2) ||
+      !make_map(&p.tm_v64, v, shape->total, shape->num_heads, shape->head_dim, kBlock / 2) ||
+      !make_map(&p.tm_do64, dout, shape->total, shape->num_heads, shape->head_dim, kBlock / 2))
     return HSTU_ERR_CUDA;
   p.seq_offsets = seq_offsets;
   p.func = func;

@@ -22,7 +22,9 @@
 // workspace and no reduce-add traffic.
 //
 // Warps: 0-7 epilogue, 8 producer (tile lists into two item slots, TMA
-// loads), 9 TMEM owner and MMA issuer. The next item's lists and resident
+// loads; streamed tiles travel as 64-row halves through a 4-slot ring, each
+// slot freed right after its half's accumulating MMAs), 9 TMEM owner and MMA
+// issuer. The next item's lists and resident
 // tiles are fetched while the current item finishes; its first accumulating
 // MMA waits until the epilogue has read out the previous item's accumulators.
 //
@@ -57,14 +59,18 @@ struct BwdItem {
 template <int DP>
 struct BwdSmem {
   static constexpr int kChunks = DP / 64;
-  static constexpr int kTile = kChunks * kBlock * 128;
+  static constexpr int kTile = kChunks * kBlock * 128;           // 128 rows
+  static constexpr int kHalfTile = kChunks * (kBlock / 2) * 128;  // 64 rows
+  static constexpr int kSlots = 4;                               // streamed half tiles
   // dK/dV role: res0 = K, res1 = V, str0 = Q, str1 = dO.
   // dQ role:    res0 = Q, res1 = dO, str0 = K, str1 = V.
+  // Streamed tiles travel as 64-row halves through a ring of kSlots, each
+  // slot freed as soon as the accumulating MMAs of its half have completed.
   alignas(1024) uint8_t res0[kTile];
   alignas(1024) uint8_t res1[kTile];
-  alignas(1024) uint8_t str0[2][kTile];
-  alignas(1024) uint8_t str1[2][kTile];
-  alignas(8) uint64_t bar_res_full, bar_res_empty, bar_full[2], bar_empty[2], bar_s_full[2],
+  alignas(1024) uint8_t str0[kSlots][kHalfTile];
+  alignas(1024) uint8_t str1[kSlots][kHalfTile];
+  alignas(8) uint64_t bar_res_full, bar_res_empty, bar_full[kSlots], bar_empty[kSlots], bar_s_full[2],
       bar_p_full[2], bar_acc_full, bar_acc_empty, bar_func[2], bar_item_full[2], bar_item_empty[2],
       bar_drain;
   uint32_t tmem_base;
@@ -148,7 +154,8 @@ template <int DP, int NINT>
 __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant__ AttnParams p) {
   using Smem = BwdSmem<DP>;
   constexpr int kTile = Smem::kTile;
-  constexpr int kChunkBytes = kBlock * 128;
+  constexpr int kChunkBytes = kBlock * 128;       // one 64-column chunk of a 128-row tile
+  constexpr int kHalfChunk = (kBlock / 2) * 128;  // one 64-column chunk of a 64-row half
   extern __shared__ uint8_t smem_raw[];
   Smem& s = smem_as_b<Smem>(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -161,9 +168,11 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
     s.abort_flag = 0;
     mbar_init(smem_u32(&s.bar_res_full), 1);
     mbar_init(smem_u32(&s.bar_res_empty), 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < Smem::kSlots; ++i) {
       mbar_init(smem_u32(&s.bar_full[i]), 1);
       mbar_init(smem_u32(&s.bar_empty[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&s.bar_s_full[i]), 1);
       mbar_init(smem_u32(&s.bar_p_full[i]), 128);
       mbar_init(smem_u32(&s.bar_func[i]), 256);
@@ -193,7 +202,7 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
 
   if (warp == 8) {
     // ------------------------------------------------------------ producer
-    int str_last[2] = {-1, -1};
+    int str_last[Smem::kSlots] = {-1, -1, -1, -1};
     int res_uses = 0;  // items with at least one tile (one resident load each)
     int gs = 0;        // streamed tiles over all items
     bool ok = true;
@@ -243,8 +252,8 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
         if (n > 0) {
           const CUtensorMap* m_res0 = dkdv ? &p.tm_k : &p.tm_q;
           const CUtensorMap* m_res1 = dkdv ? &p.tm_v : &p.tm_do;
-          const CUtensorMap* m_str0 = dkdv ? &p.tm_q : &p.tm_k;
-          const CUtensorMap* m_str1 = dkdv ? &p.tm_do : &p.tm_v;
+          const CUtensorMap* m_str0 = dkdv ? &p.tm_q64 : &p.tm_k64;
+          const CUtensorMap* m_str1 = dkdv ? &p.tm_do64 : &p.tm_v64;
           if (res_uses > 0 && !mbar_wait(smem_u32(&s.bar_res_empty), (res_uses - 1) & 1, abort_flag))
             ok = false;
           if (ok) {
@@ -257,18 +266,18 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
             }
             ++res_uses;
           }
-          for (int t = 0; ok && t < n; ++t) {
-            const int g = gs + t, st = g & 1, use = g >> 1;
+          for (int t = 0; ok && t < 2 * n; ++t) {  // 64-row halves
+            const int gh = 2 * gs + t, st = gh % Smem::kSlots, use = gh / Smem::kSlots;
             if (use > 0 && !mbar_wait(smem_u32(&s.bar_empty[st]), (use - 1) & 1, abort_flag)) {
               ok = false;
               break;
             }
-            const int srow0 = o0 + (it_slot.idx[t] & 0xff) * kBlock;
+            const int srow0 = o0 + (it_slot.idx[t >> 1] & 0xff) * kBlock + (t & 1) * (kBlock / 2);
             const uint32_t bar = smem_u32(&s.bar_full[st]);
-            mbar_expect_tx(bar, 2 * kTile);
+            mbar_expect_tx(bar, 2 * Smem::kHalfTile);
             for (int c = 0; c < Smem::kChunks; ++c) {
-              tma_load_3d(smem_u32(s.str0[st] + c * kChunkBytes), m_str0, bar, c * 64, h, srow0);
-              tma_load_3d(smem_u32(s.str1[st] + c * kChunkBytes), m_str1, bar, c * 64, h, srow0);
+              tma_load_3d(smem_u32(s.str0[st] + c * kHalfChunk), m_str0, bar, c * 64, h, srow0);
+              tma_load_3d(smem_u32(s.str1[st] + c * kHalfChunk), m_str1, bar, c * 64, h, srow0);
             }
             str_last[st] = use;
           }
@@ -280,7 +289,7 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
     // Never leave with a copy in flight.
     if (lane == 0) {
       if (res_uses > 0) mbar_wait_drain(smem_u32(&s.bar_res_full), (res_uses - 1) & 1);
-      for (int st = 0; st < 2; ++st)
+      for (int st = 0; st < Smem::kSlots; ++st)
         if (str_last[st] >= 0) mbar_wait_drain(smem_u32(&s.bar_full[st]), str_last[st] & 1);
     }
     __syncwarp();
@@ -297,8 +306,8 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
       const uint64_t dr1 = sdesc_sw128(smem_u32(s.res1), 16, 1024);
       const uint64_t ds0 = sdesc_sw128(smem_u32(s.str0[0]), 16, 1024);
       const uint64_t ds1 = sdesc_sw128(smem_u32(s.str1[0]), 16, 1024);
-      const uint64_t ds0_mn = sdesc_sw128(smem_u32(s.str0[0]), kChunkBytes, 1024);
-      const uint64_t ds1_mn = sdesc_sw128(smem_u32(s.str1[0]), kChunkBytes, 1024);
+      const uint64_t ds0_mn = sdesc_sw128(smem_u32(s.str0[0]), kHalfChunk, 1024);
+      const uint64_t ds1_mn = sdesc_sw128(smem_u32(s.str1[0]), kHalfChunk, 1024);
       int gs = 0;        // streamed tiles over all items
       int res_uses = 0;  // items with at least one tile
       bool ok = true;
@@ -317,22 +326,22 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
         // into TMEM half u & 1: S (or S^T) = res0 . str0_h^T,
         // dP (or dP^T) = res1 . str1_h^T.
         auto issue_sdp = [&](int u) -> bool {
-          const int g = gs + (u >> 1), hh = u & 1, st = g & 1;
-          if (hh == 0) {
-            if (!mbar_wait(smem_u32(&s.bar_full[st]), (g >> 1) & 1, abort_flag)) return false;
-            tc_fence_after();
-          }
-          const uint32_t hoff = st * kTile + hh * 64 * 128;
+          const int gh = 2 * gs + u, hh = u & 1, st = gh % Smem::kSlots;
+          if (!mbar_wait(smem_u32(&s.bar_full[st]), (gh / Smem::kSlots) & 1, abort_flag)) return false;
+          tc_fence_after();
+          const uint32_t hoff = st * Smem::kHalfTile;
           const uint64_t b0 = sdesc_advance(ds0, hoff), b1 = sdesc_advance(ds1, hoff);
 #pragma unroll
           for (int kk = 0; kk < DP / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-            umma_ss(tS + hh * 64, sdesc_advance(dr0, off), sdesc_advance(b0, off), idesc_s, kk > 0);
+            const uint32_t aoff = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+            const uint32_t boff = (kk >> 2) * kHalfChunk + (kk & 3) * 32;
+            umma_ss(tS + hh * 64, sdesc_advance(dr0, aoff), sdesc_advance(b0, boff), idesc_s, kk > 0);
           }
 #pragma unroll
           for (int kk = 0; kk < DP / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-            umma_ss(tdP + hh * 64, sdesc_advance(dr1, off), sdesc_advance(b1, off), idesc_s, kk > 0);
+            const uint32_t aoff = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+            const uint32_t boff = (kk >> 2) * kHalfChunk + (kk & 3) * 32;
+            umma_ss(tdP + hh * 64, sdesc_advance(dr1, aoff), sdesc_advance(b1, boff), idesc_s, kk > 0);
           }
           umma_commit(smem_u32(&s.bar_s_full[hh]));
           if (u == nsteps - 1) umma_commit(smem_u32(&s.bar_res_empty));  // residents free
@@ -343,7 +352,7 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
         // accumulating MMAs of step u (issued just before, in order) read.
         ok = issue_sdp(0) && issue_sdp(1);
         for (int u = 0; ok && u < nsteps; ++u) {
-          const int pit = u >> 1, ph = u & 1, g = gs + pit, pst = g & 1;
+          const int pit = u >> 1, ph = u & 1, g = gs + pit, pst = (2 * gs + u) % Smem::kSlots;
           if (u == 0 && res_uses > 0 &&
               !mbar_wait(smem_u32(&s.bar_acc_empty), (res_uses - 1) & 1, abort_flag)) {
             ok = false;  // the previous item's accumulators have not been read out
@@ -351,7 +360,7 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
           }
           if (!mbar_wait(smem_u32(&s.bar_p_full[ph]), g & 1, abort_flag)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t boff0 = pst * kTile + ph * 64 * 128;
+          const uint32_t boff0 = pst * Smem::kHalfTile;
           const uint64_t m0 = sdesc_advance(ds0_mn, boff0), m1 = sdesc_advance(ds1_mn, boff0);
           const uint32_t first = (pit > 0 || ph > 0) ? 1u : 0u;
 #pragma unroll
@@ -367,7 +376,7 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
               umma_ts(t_acc0, tS + acol, sdesc_advance(m0, ks * 16 * 128), idesc_acc, acc);
             }
           }
-          if (ph == 1) umma_commit(smem_u32(&s.bar_empty[pst]));
+          umma_commit(smem_u32(&s.bar_empty[pst]));  // this half's slot is free
           if (u + 2 < nsteps && !issue_sdp(u + 2)) ok = false;
         }
         if (!ok) break;

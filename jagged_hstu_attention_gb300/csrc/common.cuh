@@ -22,6 +22,7 @@ constexpr int kMaxIntervals = 3;   // nfunc <= 5
 constexpr int kHdrErr = 0;     // error bits (kErrInput | kErrTimeout)
 constexpr int kHdrNFwd = 1;    // entries of the forward work list
 constexpr int kHdrNBwd = 2;    // entries of the backward work list
+constexpr int kHdrTicket = 3;  // plan blocks finished (the last one builds the lists)
 constexpr int kHdrWords = 64;  // 256 bytes
 constexpr int kErrInput = 1;
 constexpr int kErrTimeout = 2;
@@ -35,21 +36,19 @@ constexpr int kRoleDkdv = 1 << 30;
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Layout of the HSTU_WS_FULL workspace. header, qvis and kvvis are contiguous
-// so that one memset clears them at the start of a plan.
+// Layout of the HSTU_WS_FULL workspace. Only the header is cleared at the
+// start of a plan; every other region is fully written before it is read.
 struct FullLayout {
   int nt = 0;  // tiles per sequence at max_seqlen
-  size_t header = 0, qvis = 0, kvvis = 0, zero_bytes = 0, fwd_list = 0, bwd_list = 0, seq_order = 0,
-         seq_start = 0, ivmask = 0, cls = 0, total = 0;
+  size_t header = 0, zero_bytes = 0, fwd_list = 0, bwd_list = 0, seq_order = 0, seq_start = 0,
+         ivmask = 0, cls = 0, total = 0;
 };
 inline FullLayout full_layout(int batch, int max_seqlen) {
   FullLayout l;
   l.nt = (max_seqlen + kBlock - 1) / kBlock;
   const size_t items = static_cast<size_t>(batch) * l.nt;
   l.header = 0;
-  l.qvis = kHdrWords * 4;
-  l.kvvis = l.qvis + align_up(items * 4, 256);
-  l.zero_bytes = l.kvvis + align_up(items * 4, 256);
+  l.zero_bytes = kHdrWords * 4;
   l.fwd_list = l.zero_bytes;
   l.bwd_list = l.fwd_list + align_up(items * 4, 256);
   l.seq_order = l.bwd_list + align_up(2 * items * 4, 256);
@@ -80,8 +79,6 @@ struct PlanParams {
   const int32_t* func;
   int32_t* row_counts;  // nullable
   int32_t* header;
-  int32_t* qvis;
-  int32_t* kvvis;
   int32_t* fwd_list;
   int32_t* bwd_list;
   int32_t* seq_order;  // sequences, longest first
@@ -93,7 +90,8 @@ struct PlanParams {
 };
 
 struct AttnParams {
-  CUtensorMap tm_q, tm_k, tm_v, tm_do;
+  CUtensorMap tm_q, tm_k, tm_v, tm_do;          // 128-row boxes
+  CUtensorMap tm_q64, tm_k64, tm_v64, tm_do64;  // 64-row boxes (backward streams)
   const int32_t* seq_offsets;
   const int32_t* func;
   __nv_bfloat16* out0;  // fwd: o; bwd: dq

@@ -1,7 +1,7 @@
 // Plan: device-side validation of seq_offsets, the func prologue that
 // classifies every (q-tile, kv-tile) pair of a sequence, the per-row visible
 // counts, and the longest-first work lists of the forward and backward
-// kernels. Nothing here needs a host synchronisation.
+// kernels, all in one launch. Nothing here needs a host synchronisation.
 //
 // The pages' kernels reduce per-tile min/max bounds of every interval
 // (including the empty padded ones) and then test every interval in every KV
@@ -18,8 +18,11 @@
 
 namespace hstu {
 
+// Classifies the kv tiles seen by one (sequence b, q tile qt) block and
+// writes that tile's row counts, class row and active-interval mask. Blocks
+// past a sequence's last q tile (or of an invalid sequence) do nothing.
 template <int NINT>
-__global__ void __launch_bounds__(128) plan_classify_kernel(const PlanParams p) {
+__device__ void classify_tile(const PlanParams& p) {
   const int b = blockIdx.x, qt = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int o0 = p.seq_offsets[b];
@@ -38,14 +41,12 @@ __global__ void __launch_bounds__(128) plan_classify_kernel(const PlanParams p) 
 
   __shared__ uint32_t any_bits[4][kMaxTiles / 32];
   __shared__ uint32_t all_bits[4][kMaxTiles / 32];
-  __shared__ int n_visit;
   __shared__ uint32_t active_iv;
   if (tid == 0) active_iv = 0;
   for (int x = tid; x < 4 * (kMaxTiles / 32); x += 128) {
     (&any_bits[0][0])[x] = 0;
     (&all_bits[0][0])[x] = 0;
   }
-  if (tid == 0) n_visit = 0;
   __syncthreads();
 
   const int i = qt * kBlock + tid;
@@ -75,7 +76,6 @@ __global__ void __launch_bounds__(128) plan_classify_kernel(const PlanParams p) 
   __syncthreads();
 
   const size_t row_base = (static_cast<size_t>(b) * p.nt + qt) * p.nt;
-  int mine = 0;
   for (int j = tid; j < ntiles; j += 128) {
     const uint32_t bit = 1u << (j & 31);
     const int word = j >> 5;
@@ -83,19 +83,9 @@ __global__ void __launch_bounds__(128) plan_classify_kernel(const PlanParams p) 
                        any_bits[3][word]) & bit) != 0;
     const bool all = ((all_bits[0][word] & all_bits[1][word] & all_bits[2][word] &
                        all_bits[3][word]) & bit) != 0;
-    const uint8_t cls = all ? kFull : (any ? kPartial : kSkip);
-    p.cls[row_base + j] = cls;
-    if (cls != kSkip) {
-      ++mine;
-      atomicAdd(p.kvvis + static_cast<size_t>(b) * p.nt + j, 1);
-    }
+    p.cls[row_base + j] = all ? kFull : (any ? kPartial : kSkip);
   }
-  if (mine) atomicAdd(&n_visit, mine);
-  __syncthreads();
-  if (tid == 0) {
-    p.qvis[static_cast<size_t>(b) * p.nt + qt] = n_visit;
-    p.ivmask[static_cast<size_t>(b) * p.nt + qt] = static_cast<uint8_t>(active_iv);
-  }
+  if (tid == 0) p.ivmask[static_cast<size_t>(b) * p.nt + qt] = static_cast<uint8_t>(active_iv);
 }
 
 // Exclusive scan of cnt[0..n) in place (one block of 1024 threads).
@@ -145,7 +135,7 @@ __device__ void block_exclusive_scan(int* cnt, int n) {
 // of equal length may come out in any order: every output element is
 // computed by exactly one CTA with a fixed internal order, so the order only
 // changes scheduling, never results.
-__global__ void __launch_bounds__(1024) plan_sort_kernel(const PlanParams p) {
+__device__ void build_work_lists(const PlanParams& p) {
   __shared__ int hist[kMaxTiles + 1];
   __shared__ int n_items;
   const int tid = threadIdx.x;
@@ -187,17 +177,32 @@ __global__ void __launch_bounds__(1024) plan_sort_kernel(const PlanParams p) {
   }
 }
 
+// One launch: every block classifies one (sequence, q tile); the last block
+// to finish (ticket counter in the header) builds the work lists.
+template <int NINT>
+__global__ void __launch_bounds__(128) plan_kernel(const PlanParams p) {
+  classify_tile<NINT>(p);
+  __shared__ int is_last;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const int done = atomicAdd(p.header + kHdrTicket, 1);
+    is_last = done == static_cast<int>(gridDim.x * gridDim.y) - 1;
+  }
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  build_work_lists(p);
+}
+
 cudaError_t launch_plan(const PlanParams& p, size_t zero_bytes, cudaStream_t stream) {
   cudaError_t e = cudaMemsetAsync(p.header, 0, zero_bytes, stream);
   if (e != cudaSuccess) return e;
   const dim3 grid(p.batch, p.nt);
   const int nint = (p.nfunc + 1) / 2;
-  if (nint == 1) plan_classify_kernel<1><<<grid, 128, 0, stream>>>(p);
-  else if (nint == 2) plan_classify_kernel<2><<<grid, 128, 0, stream>>>(p);
-  else plan_classify_kernel<3><<<grid, 128, 0, stream>>>(p);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  plan_sort_kernel<<<1, 1024, 0, stream>>>(p);
+  if (nint == 1) plan_kernel<1><<<grid, 128, 0, stream>>>(p);
+  else if (nint == 2) plan_kernel<2><<<grid, 128, 0, stream>>>(p);
+  else plan_kernel<3><<<grid, 128, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
