@@ -286,6 +286,89 @@ def dist_env():
     return ws, rank, local
 
 
+def run_targets(args, cfg, device, world, rank):
+    """Targets-only mode: one candidate row per sequence (its last row,
+    causal: it sees the whole sequence) against full-length K/V, fwd + bwd.
+    HBM-bound: reports achieved bytes/s against the measured copy bandwidth."""
+    import torch
+    import torch.distributed as dist
+    from jagged_hstu_attention_gb300 import binding as hb
+    from jagged_hstu_attention_gb300 import workloads as wl
+    seed = args.seed + rank
+    lens = wl.lengths(cfg, seed)
+    off = wl.offsets_from_lengths(lens)
+    T, B, H, D = int(off[-1]), len(lens), cfg.heads, cfg.dim
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    k = wl.randn_bf16((T, H, D), gen, device)
+    v = wl.randn_bf16((T, H, D), gen, device)
+    q_c = wl.randn_bf16((B, H, D), gen, device)
+    do_c = wl.randn_bf16((B, H, D), gen, device)
+    d_off = torch.tensor(off, dtype=torch.int32, device=device)
+    fc = torch.tensor(wl.build_func_candidates(lens, 1), dtype=torch.int32, device=device)
+    N = int(lens.max())
+    alpha = 1.0 / math.sqrt(D)
+    shape = hb.make_shape(B, T, H, D, 1, N, alpha)
+    ws = hb.alloc_workspace(shape, hb.WS_TARGETS, device)
+    o_c, dq_c, dk, dv = torch.empty_like(q_c), torch.empty_like(q_c), torch.empty_like(k), torch.empty_like(v)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+
+    def step(ev):
+        ev[0].record()
+        hb.fwd_targets_only(q_c, k, v, d_off, fc, N, alpha, ws=ws, out=o_c)
+        ev[1].record()
+        hb.bwd_targets_only(do_c, q_c, k, v, d_off, fc, N, alpha, ws=ws, outs=(dq_c, dk, dv))
+        ev[2].record()
+
+    for _ in range(args.warmup):
+        step([torch.cuda.Event(enable_timing=True) for _ in range(3)])
+    torch.cuda.synchronize()
+    assert hb.device_status(ws) == hb.HSTU_OK
+    sampler = ClockSampler(torch.cuda.current_device())
+    if world > 1:
+        dist.barrier()
+    sampler.start()
+    recs = []
+    for _ in range(args.steps):
+        flush.zero_()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        step(ev)
+        recs.append(ev)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in recs)
+    bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in recs)
+    ms = fwd_ms + bwd_ms
+    ms_t = torch.tensor([ms], device=device)
+    if world > 1:
+        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
+        ms = float(ms_t.item())
+    if rank != 0:
+        return
+    row = H * D * 2
+    bytes_fwd = 2 * T * row + 2 * B * row   # read K, V, q_c; write o_c
+    bytes_bwd = 4 * T * row + 3 * B * row   # read K, V, q_c, dO_c; write dK, dV, dq_c
+    useful = float(T) * H * 14 * D          # every key is visible to its candidate
+    peaks = load_peaks()
+    gbs = (bytes_fwd + bytes_bwd) / (ms * 1e-3) / 1e9
+    line = {
+        "metric": "HSTU targets-only fwd+bwd ms and achieved HBM GB/s (% of measured copy bandwidth)",
+        "mode": "targets_only", "value": gbs * world, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": cfg.name + ":targets_only", "batch": B, "total_tokens": T, "heads": H,
+                   "head_dim": D, "candidates_per_seq": 1, "l2": "flushed between steps"},
+        "breakdown_ms": {"fwd": fwd_ms, "bwd": bwd_ms},
+        "useful_tflops": useful / (ms * 1e-3) / 1e12,
+        "gpu_launches": 4 * args.steps,
+        "roofline": {"kernel": "tgt_partial_kernel (fwd + bwd)", "bound": "hbm", "achieved": gbs,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
+                     "traffic": None, "peak_source": peaks["source"] + " copy bandwidth"},
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def run_reference(args, cfg):
     """The oracle as it stands on the host cores (bounded sample per step)."""
     world, rank, _ = dist_env()
@@ -322,6 +405,8 @@ def main():
                     help="override the workload's batch size (small profiling cases only)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--mode", default="full", choices=["full", "targets"],
+                    help="full: plan + fwd + bwd over every row; targets: targets-only fwd + bwd")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -346,6 +431,11 @@ def main():
     build_ext.build()
     from jagged_hstu_attention_gb300 import binding as hb
     hb.load()
+    if args.mode == "targets":
+        run_targets(args, cfg, device, world, rank)
+        if world > 1:
+            dist.destroy_process_group()
+        return
 
     # Each rank runs its own batch (seed + rank): independent sequences, no
     # data-path collective; weak scaling.
