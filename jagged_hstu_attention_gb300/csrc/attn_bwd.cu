@@ -4,10 +4,10 @@
 //
 // dK/dV role -- item (sequence b, kv tile kt, head h). K and V of the tile
 // stay in SMEM; the Q and dO tiles of every q tile that visits kt stream
-// through a 2-stage ring. Per q tile (TMEM lanes = kv rows):
+// through a ring of 64-row halves. Per half (TMEM lanes = kv rows):
 //     S^T  = K Q^T,  dP^T = V dO^T                      (SMEM x SMEM)
 //     P^T  = silu(alpha S^T)/N,  dS^T = dP^T * silu'(alpha S^T) * alpha/N
-//            (masked on partial tiles, packed bf16 in place over S^T, dP^T;
+//            (masked on partial tiles, both packed bf16 in place over S^T;
 //            the common factor alpha/(2N) is applied once at the stores)
 //     dV  += P^T dO,  dK += dS^T Q                       (TMEM x SMEM)
 // dK and dV accumulate in TMEM across the whole item and are stored once:
@@ -29,22 +29,26 @@
 // MMA waits until the epilogue has read out the previous item's accumulators.
 //
 // TMEM (512 columns, the same for both roles): acc0 [0,128) (dV or dQ),
-// acc1 [128,256) (dK), S [256,384), dP [384,512).
+// acc1 [128,256) (dK), three S slots at 256, 320 and 384, one dP slot at
+// 448 (64 columns each).
 //
-// Half-tile pipeline: every 128-wide tile is handled as two 64-column halves.
-// S/dP of a half are N=64 MMAs into their own TMEM half. The epilogue warps
-// form two groups of four (TMEM lanes 32(w%4)..), and group h owns half h of
-// every tile, so both halves are converted at the same time while the tensor
-// core runs the accumulating MMAs of a finished half and S/dP of the next.
-// Each warp packs its bf16 results over the first 32 of its half's 64
-// columns, which it has read itself; the accumulating MMA's four K-steps of
-// half h read columns [64h, 64h+32).
+// Half-step pipeline: every 128-wide tile is handled as two 64-column halves
+// ("half-steps", counted globally as v). S(v) and dP(v) are N=64 MMAs; S(v)
+// goes to S slot v % 3, dP(v) to the single dP slot. The epilogue warps form
+// two groups of four (TMEM lanes 32(w%4)..); group h takes the half-steps with
+// v % 2 == h. A group first reads all of dP(v) and releases the dP slot, so
+// that dP(v+1) can be computed while it converts; it then packs P^T and dS^T
+// (or dS alone) as bf16 over the S columns it has read. Since S slots are
+// reused only every third half-step, S/dP of v + 3 are issued right after the
+// accumulating MMAs of v, and a group's conversion of v overlaps the tensor
+// work of two later half-steps instead of one.
 //
-// Partial-tile masks of the dK/dV role are built by transposition: each warp
-// holds 32 q rows of the visiting q tile, computes each row's visible-column
-// bits over its 64 kv columns from the row's intervals, and one ballot per kv
-// column turns them into that column's 32-row word. The cost does not depend
-// on the number of intervals, so empty padded intervals stay free.
+// Partial-tile masks of the dK/dV role are built by transposition inside
+// each warp: lane l takes the two q rows of its half's chunks, computes which
+// of the warp's 32 kv rows they see from the rows' intervals, and one ballot
+// per kv row turns the bits into that row's 32-q-row words. No warp needs
+// another's result, and the cost does not depend on the number of intervals,
+// so empty padded intervals stay free.
 #include "common.cuh"
 #include "internal.h"
 
@@ -61,7 +65,7 @@ struct BwdSmem {
   static constexpr int kChunks = DP / 64;
   static constexpr int kTile = kChunks * kBlock * 128;           // 128 rows
   static constexpr int kHalfTile = kChunks * (kBlock / 2) * 128;  // 64 rows
-  static constexpr int kSlots = 4;                               // streamed half tiles
+  static constexpr int kSlots = 5;                               // streamed half tiles
   // dK/dV role: res0 = K, res1 = V, str0 = Q, str1 = dO.
   // dQ role:    res0 = Q, res1 = dO, str0 = K, str1 = V.
   // Streamed tiles travel as 64-row halves through a ring of kSlots, each
@@ -70,16 +74,17 @@ struct BwdSmem {
   alignas(1024) uint8_t res1[kTile];
   alignas(1024) uint8_t str0[kSlots][kHalfTile];
   alignas(1024) uint8_t str1[kSlots][kHalfTile];
-  alignas(8) uint64_t bar_res_full, bar_res_empty, bar_full[kSlots], bar_empty[kSlots], bar_s_full[2],
-      bar_p_full[2], bar_acc_full, bar_acc_empty, bar_func[2], bar_item_full[2], bar_item_empty[2],
-      bar_drain;
+  static constexpr int kSSlots = 3;  // S slots in TMEM
+  alignas(8) uint64_t bar_res_full, bar_res_empty, bar_full[kSlots], bar_empty[kSlots],
+      bar_s_full[kSSlots], bar_p_full[kSSlots], bar_dp_free, bar_acc_full, bar_acc_empty,
+      bar_item_full[2], bar_item_empty[2], bar_drain;
   uint32_t tmem_base;
   int abort_flag;
-  // dK/dV role: per partial q tile, colmask[c][j] bit e = q row 32c+e sees
-  // kv column j of the tile (double buffered).
-  uint32_t colmask[2][4][kBlock];
   BwdItem item[2];
 };
+
+// 227 KB of dynamic shared memory per CTA, with 1 KB of alignment slack.
+static_assert(sizeof(BwdSmem<128>) + 1024 <= 232448, "backward shared memory over the per-CTA limit");
 
 template <typename S>
 __device__ __forceinline__ S& smem_as_b(uint8_t* raw) {
@@ -91,56 +96,52 @@ __device__ __forceinline__ bool warp_wait_b(uint32_t bar, uint32_t parity, volat
   return __all_sync(0xffffffffu, ok);
 }
 
-// Stores 32 fp32 accumulator columns of one row, times `scale`, as bf16.
-__device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const uint32_t (&a)[32], float scale) {
-  uint32_t pk[16];
-#pragma unroll
-  for (int e = 0; e < 16; ++e)
-    pk[e] = pack_bf16x2(scale * __uint_as_float(a[2 * e]), scale * __uint_as_float(a[2 * e + 1]));
-  uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (int e = 0; e < 4; ++e) d4[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
-}
-
 // Writes this warp's half of TMEM columns [taddr, taddr + DP) of its lane (or
-// zeros), times `scale`, into a bf16 row of `dim` elements.
+// zeros), times `scale`, into a bf16 row of `dim` elements. Both 32-column
+// chunks are read before the first store.
 template <int DP>
 __device__ __forceinline__ void store_acc_half(uint32_t taddr, int half, bool have, bool valid,
-                                               __nv_bfloat16* dst, int dim, float scale) {
+                                               __nv_bfloat16* dst, int dim, float scale, bool wide) {
+  constexpr int kNc = DP / 64;
+  uint32_t a[kNc][32];
+  if (have) {
 #pragma unroll
-  for (int c = 0; c < DP / 64; ++c) {
+    for (int c = 0; c < kNc; ++c) tmem_ld32(taddr + half * (DP / 2) + c * 32, a[c]);
+#pragma unroll
+    for (int c = 0; c < kNc; ++c) tmem_ld_wait(a[c]);
+  } else {
+#pragma unroll
+    for (int c = 0; c < kNc; ++c)
+#pragma unroll
+      for (int e = 0; e < 32; ++e) a[c][e] = 0u;
+  }
+#pragma unroll
+  for (int c = 0; c < kNc; ++c) {
     const int col = half * (DP / 2) + c * 32;
-    uint32_t a[32];
-    if (have) {
-      tmem_ld32(taddr + col, a);
-      tmem_ld_wait(a);
-    } else {
-#pragma unroll
-      for (int e = 0; e < 32; ++e) a[e] = 0u;
-    }
-    if (valid && col < dim) store_row32(dst + col, a, scale);
+    if (valid && col < dim) store_row32(dst + col, a[c], scale, wide);
   }
 }
 
-// 32 columns of S and dP -> packed bf16 P' = s (1 + t) (when WANT_P) and
-// G' = dP (1 + t)(1 + h - h t), h = alpha s / 2, t = tanh(h): the backward
-// quantities up to the factor alpha / (2N) applied to dV, dK and dQ at their
-// store. MASKED zeroes the columns whose bit is clear.
-template <bool MASKED, bool WANT_P>
-__device__ __forceinline__ void epilogue32(const uint32_t (&sv)[32], const uint32_t (&dv)[32],
-                                           uint32_t mask, float half_alpha, uint32_t (&pp)[16],
-                                           uint32_t (&pd)[16]) {
+// 16 columns [C0, C0 + 16) of 32 loaded S and dP columns -> packed bf16
+// P' = s (1 + t) (when WANT_P) and G' = dP (1 + t)(1 + h - h t), h = alpha s / 2,
+// t = tanh(h): the backward quantities up to the factor alpha / (2N) applied
+// to dV, dK and dQ at their store. MASKED zeroes the columns whose bit (of
+// the 32-column word) is clear.
+template <int C0, bool MASKED, bool WANT_P>
+__device__ __forceinline__ void epilogue16(const uint32_t (&sv)[32], const uint32_t (&dv)[32],
+                                           uint32_t mask, float half_alpha, uint32_t (&pp)[8],
+                                           uint32_t (&pd)[8]) {
 #pragma unroll
-  for (int e = 0; e < 32; e += 2) {
+  for (int e = 0; e < 16; e += 2) {
     float g[2], pv[2];
 #pragma unroll
     for (int x = 0; x < 2; ++x) {
-      const float sc = __uint_as_float(sv[e + x]);
-      const float dp = __uint_as_float(dv[e + x]);
+      const float sc = __uint_as_float(sv[C0 + e + x]);
+      const float dp = __uint_as_float(dv[C0 + e + x]);
       if (WANT_P) silu_pu_gu(sc, dp, half_alpha, pv[x], g[x]);
       else g[x] = silu_gu(sc, dp, half_alpha);
       if (MASKED) {
-        const bool on = (mask >> (e + x)) & 1u;
+        const bool on = (mask >> (C0 + e + x)) & 1u;
         if (WANT_P) pv[x] = on ? pv[x] : 0.0f;
         g[x] = on ? g[x] : 0.0f;
       }
@@ -148,6 +149,23 @@ __device__ __forceinline__ void epilogue32(const uint32_t (&sv)[32], const uint3
     if (WANT_P) pp[e / 2] = pack_bf16x2(pv[0], pv[1]);
     pd[e / 2] = pack_bf16x2(g[0], g[1]);
   }
+}
+
+// Converts one 32-column chunk (the q rows of K-steps 2c and 2c + 1 of a
+// half) and packs it over S columns this warp has already read. dK/dV role:
+// K-step ks of the accumulating MMAs reads P^T from slot columns
+// [16ks, 16ks + 8) and dS^T from [16ks + 8, 16ks + 16); dQ role: dS from
+// [8ks, 8ks + 8).
+template <bool MASKED, bool DKDV>
+__device__ __forceinline__ void convert_chunk(const uint32_t (&sv)[32], const uint32_t (&dv)[32],
+                                              uint32_t mask, float half_alpha, uint32_t xs, int c) {
+  uint32_t pp[8], pd[8];
+  epilogue16<0, MASKED, DKDV>(sv, dv, mask, half_alpha, pp, pd);
+  if (DKDV) tmem_st8x2(xs + 32 * c, pp, pd);
+  else tmem_st8(xs + 16 * c, pd);
+  epilogue16<16, MASKED, DKDV>(sv, dv, mask, half_alpha, pp, pd);
+  if (DKDV) tmem_st8x2(xs + 32 * c + 16, pp, pd);
+  else tmem_st8(xs + 16 * c + 8, pd);
 }
 
 template <int DP, int NINT>
@@ -172,10 +190,12 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
       mbar_init(smem_u32(&s.bar_full[i]), 1);
       mbar_init(smem_u32(&s.bar_empty[i]), 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < Smem::kSSlots; ++i) {
       mbar_init(smem_u32(&s.bar_s_full[i]), 1);
       mbar_init(smem_u32(&s.bar_p_full[i]), 128);
-      mbar_init(smem_u32(&s.bar_func[i]), 256);
+    }
+    mbar_init(smem_u32(&s.bar_dp_free), 128);
+    for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&s.bar_item_full[i]), 1);
       mbar_init(smem_u32(&s.bar_item_empty[i]), 1 + 256);  // MMA issuer + epilogue threads
     }
@@ -194,8 +214,8 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
   const uint32_t tbase = s.tmem_base;
   const uint32_t t_acc0 = tbase;        // dV (dK/dV role) or dQ (dQ role)
   const uint32_t t_acc1 = tbase + 128;  // dK (dK/dV role)
-  const uint32_t tS = tbase + 256;
-  const uint32_t tdP = tbase + 384;
+  const uint32_t tS = tbase + 256;      // S slot k at tS + 64 k
+  const uint32_t tdP = tbase + 448;
   volatile int* abort_flag = &s.abort_flag;
   const int stride = gridDim.x;
   const size_t nt_all = static_cast<size_t>(p.nt);
@@ -266,6 +286,17 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
             }
             ++res_uses;
           }
+          // Streamed halves are first requested into L2 kPrefetch halves ahead of
+          // their load, which covers most of the HBM latency of the load.
+          constexpr int kPrefetch = 4;
+          auto prefetch_half = [&](int t) {
+            const int prow0 = o0 + (it_slot.idx[t >> 1] & 0xff) * kBlock + (t & 1) * (kBlock / 2);
+            for (int c = 0; c < Smem::kChunks; ++c) {
+              tma_prefetch_l2_3d(m_str0, c * 64, h, prow0);
+              tma_prefetch_l2_3d(m_str1, c * 64, h, prow0);
+            }
+          };
+          for (int t = 0; t < kPrefetch && t < 2 * n; ++t) prefetch_half(t);
           for (int t = 0; ok && t < 2 * n; ++t) {  // 64-row halves
             const int gh = 2 * gs + t, st = gh % Smem::kSlots, use = gh / Smem::kSlots;
             if (use > 0 && !mbar_wait(smem_u32(&s.bar_empty[st]), (use - 1) & 1, abort_flag)) {
@@ -280,6 +311,7 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
               tma_load_3d(smem_u32(s.str1[st] + c * kHalfChunk), m_str1, bar, c * 64, h, srow0);
             }
             str_last[st] = use;
+            if (t + kPrefetch < 2 * n) prefetch_half(t + kPrefetch);
           }
           gs += n;
         }
@@ -296,9 +328,8 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (elect_one_sync()) {
-      // Half-tile pipeline: step u covers the 64-column half (u & 1) of tile
-      // u >> 1. While the epilogue works on one half, the tensor core runs
-      // the accumulating MMAs of the other half and S/dP two steps ahead.
+      // Half-step pipeline: step v covers the 64-column half (v & 1) of tile
+      // v >> 1. S/dP run three steps ahead of the accumulating MMAs.
       constexpr uint32_t idesc_s = idesc_bf16(128, 64, false, false);
       constexpr uint32_t idesc_acc = idesc_bf16(128, DP, false, true);
       // Descriptors are built once; each MMA only advances a start address.
@@ -322,12 +353,13 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
         if (!mbar_wait(smem_u32(&s.bar_res_full), res_uses & 1, abort_flag)) break;
         tc_fence_after();
         const int nsteps = 2 * nt;
-        // S/dP of step u (64-column half u & 1 of tile u >> 1, N = 64 MMAs)
-        // into TMEM half u & 1: S (or S^T) = res0 . str0_h^T,
-        // dP (or dP^T) = res1 . str1_h^T.
-        auto issue_sdp = [&](int u) -> bool {
-          const int gh = 2 * gs + u, hh = u & 1, st = gh % Smem::kSlots;
-          if (!mbar_wait(smem_u32(&s.bar_full[st]), (gh / Smem::kSlots) & 1, abort_flag)) return false;
+        const int gv0 = 2 * gs;  // global index of this item's first half-step
+        // S/dP of step v (N = 64 MMAs): S (or S^T) = res0 . str0_h^T into S
+        // slot gv % 3, dP (or dP^T) = res1 . str1_h^T into the dP slot once
+        // the epilogue has read dP of step gv - 1 out of it.
+        auto issue_sdp = [&](int v) -> bool {
+          const int gv = gv0 + v, st = gv % Smem::kSlots, k = gv % Smem::kSSlots;
+          if (!mbar_wait(smem_u32(&s.bar_full[st]), (gv / Smem::kSlots) & 1, abort_flag)) return false;
           tc_fence_after();
           const uint32_t hoff = st * Smem::kHalfTile;
           const uint64_t b0 = sdesc_advance(ds0, hoff), b1 = sdesc_advance(ds1, hoff);
@@ -335,49 +367,53 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
           for (int kk = 0; kk < DP / 16; ++kk) {
             const uint32_t aoff = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
             const uint32_t boff = (kk >> 2) * kHalfChunk + (kk & 3) * 32;
-            umma_ss(tS + hh * 64, sdesc_advance(dr0, aoff), sdesc_advance(b0, boff), idesc_s, kk > 0);
+            umma_ss(tS + 64 * k, sdesc_advance(dr0, aoff), sdesc_advance(b0, boff), idesc_s, kk > 0);
           }
+          if (gv > 0 && !mbar_wait(smem_u32(&s.bar_dp_free), (gv - 1) & 1, abort_flag)) return false;
+          tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < DP / 16; ++kk) {
             const uint32_t aoff = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
             const uint32_t boff = (kk >> 2) * kHalfChunk + (kk & 3) * 32;
-            umma_ss(tdP + hh * 64, sdesc_advance(dr1, aoff), sdesc_advance(b1, boff), idesc_s, kk > 0);
+            umma_ss(tdP, sdesc_advance(dr1, aoff), sdesc_advance(b1, boff), idesc_s, kk > 0);
           }
-          umma_commit(smem_u32(&s.bar_s_full[hh]));
-          if (u == nsteps - 1) umma_commit(smem_u32(&s.bar_res_empty));  // residents free
+          umma_commit(smem_u32(&s.bar_s_full[k]));
+          if (v == nsteps - 1) umma_commit(smem_u32(&s.bar_res_empty));  // residents free
           return true;
         };
-        // S/dP run two steps ahead of the accumulating MMAs: S/dP of step
-        // u + 2 reuse the TMEM half of step u, whose packed P/dS the
-        // accumulating MMAs of step u (issued just before, in order) read.
-        ok = issue_sdp(0) && issue_sdp(1);
-        for (int u = 0; ok && u < nsteps; ++u) {
-          const int pit = u >> 1, ph = u & 1, g = gs + pit, pst = (2 * gs + u) % Smem::kSlots;
-          if (u == 0 && res_uses > 0 &&
+        // S of step v + 3 reuses the S slot of step v, whose packed P/dS the
+        // accumulating MMAs of step v (issued just before, in order) read.
+        for (int v = 0; ok && v < 3 && v < nsteps; ++v) ok = issue_sdp(v);
+        for (int v = 0; ok && v < nsteps; ++v) {
+          const int gv = gv0 + v, pst = gv % Smem::kSlots, k = gv % Smem::kSSlots;
+          if (v == 0 && res_uses > 0 &&
               !mbar_wait(smem_u32(&s.bar_acc_empty), (res_uses - 1) & 1, abort_flag)) {
             ok = false;  // the previous item's accumulators have not been read out
             break;
           }
-          if (!mbar_wait(smem_u32(&s.bar_p_full[ph]), g & 1, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(smem_u32(&s.bar_p_full[k]), (gv / Smem::kSSlots) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
           const uint32_t boff0 = pst * Smem::kHalfTile;
           const uint64_t m0 = sdesc_advance(ds0_mn, boff0), m1 = sdesc_advance(ds1_mn, boff0);
-          const uint32_t first = (pit > 0 || ph > 0) ? 1u : 0u;
+          const uint32_t first = v > 0 ? 1u : 0u;
+          const uint32_t xs = tS + 64 * k;
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {  // K = the 64 rows of this half
-            const uint32_t acol = ph * 64 + ks * 8;
             const uint32_t acc = ks > 0 ? 1u : first;
             if (dkdv) {
               // dV += P^T dO (dO = str1, MN-major); dK += dS^T Q (Q = str0, MN-major)
-              umma_ts(t_acc0, tS + acol, sdesc_advance(m1, ks * 16 * 128), idesc_acc, acc);
-              umma_ts(t_acc1, tdP + acol, sdesc_advance(m0, ks * 16 * 128), idesc_acc, acc);
+              umma_ts(t_acc0, xs + 16 * ks, sdesc_advance(m1, ks * 16 * 128), idesc_acc, acc);
+              umma_ts(t_acc1, xs + 16 * ks + 8, sdesc_advance(m0, ks * 16 * 128), idesc_acc, acc);
             } else {
               // dQ += dS K (K = str0, MN-major)
-              umma_ts(t_acc0, tS + acol, sdesc_advance(m0, ks * 16 * 128), idesc_acc, acc);
+              umma_ts(t_acc0, xs + 8 * ks, sdesc_advance(m0, ks * 16 * 128), idesc_acc, acc);
             }
           }
           umma_commit(smem_u32(&s.bar_empty[pst]));  // this half's slot is free
-          if (u + 2 < nsteps && !issue_sdp(u + 2)) ok = false;
+          if (v + 3 < nsteps && !issue_sdp(v + 3)) ok = false;
         }
         if (!ok) break;
         umma_commit(smem_u32(&s.bar_acc_full));
@@ -396,10 +432,10 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     const float half_alpha = 0.5f * p.alpha;
     const float out_scale = 0.5f * p.alpha * p.inv_n;  // hc = alpha / (2N)
-    const int hc = half * 64;  // first S column of this warp's half
-    const int hh = half;       // this warp group owns TMEM half `half` of every tile
-    int g0 = 0;                // tiles over all items
-    int fu = 0;                // partial dK/dV tiles over all items: selects the mask buffer
+    // 32-byte stores need every output row to start on a 32-byte boundary.
+    const bool wide = wide_rows_ok(p.out0, p.out1, p.out2, p.dim);
+    const int hh = half;  // this warp group converts half `half` of every tile
+    int g0 = 0;           // tiles over all items
     int acc_uses = 0;
     bool ok = true;
     int i = 0;
@@ -416,73 +452,73 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
       if (!dkdv)
         load_row_intervals<NINT>(p.func, p.total, static_cast<int64_t>(o0) + own_loc, L, valid, lo, hi,
                                  iv_b[tile]);
-      int buf = 0;
       for (int it = 0; it < nt; ++it) {
         const int other = item.idx[it] & 0xff;
         const bool partial = (item.idx[it] & 0x100) != 0;
+        uint32_t qmask0 = 0, qmask1 = 0;
         if (dkdv && partial) {
-          buf = fu & 1;
-          // This warp's 32 q rows of the visiting q tile; their visible bits
-          // over kv columns [hc, hc + 64) of tile `tile`, transposed by ballot.
+          // Lane l takes q rows 64h + l and 64h + 32 + l of the visiting q
+          // tile and finds which of this warp's 32 kv rows each of them sees;
+          // one ballot per kv row turns the bits around, so that lane j holds
+          // the q-row masks of kv row 32 quarter + j for both chunks of half h.
           int flo[NINT], fhi[NINT];
-          const int qi = other * kBlock + r;
-          load_row_intervals<NINT>(p.func, p.total, static_cast<int64_t>(o0) + qi, L, qi < L, flo, fhi,
+          const int qa = other * kBlock + 64 * hh + lane;
+          const int kv0 = tile * kBlock + 32 * quarter;
+          load_row_intervals<NINT>(p.func, p.total, static_cast<int64_t>(o0) + qa, L, qa < L, flo, fhi,
                                    iv_b[other]);
-          const uint32_t w0 = row_mask_word<NINT>(flo, fhi, tile * kBlock + hc);
-          const uint32_t w1 = row_mask_word<NINT>(flo, fhi, tile * kBlock + hc + 32);
-          uint32_t mine0 = 0, mine1 = 0;
+          const uint32_t w0 = row_mask_word<NINT>(flo, fhi, kv0);
+          load_row_intervals<NINT>(p.func, p.total, static_cast<int64_t>(o0) + qa + 32, L, qa + 32 < L, flo,
+                                   fhi, iv_b[other]);
+          const uint32_t w1 = row_mask_word<NINT>(flo, fhi, kv0);
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const uint32_t b0 = __ballot_sync(0xffffffffu, (w0 >> j) & 1u);
             const uint32_t b1 = __ballot_sync(0xffffffffu, (w1 >> j) & 1u);
             if (lane == j) {
-              mine0 = b0;
-              mine1 = b1;
+              qmask0 = b0;
+              qmask1 = b1;
             }
           }
-          s.colmask[buf][quarter][hc + lane] = mine0;
-          s.colmask[buf][quarter][hc + 32 + lane] = mine1;
-          // Bounded hand-off between the 256 epilogue threads (an mbarrier, not
-          // bar.sync, so that an aborting warp cannot strand the others).
-          mbar_arrive(smem_u32(&s.bar_func[buf]));
-          if (!warp_wait_b(smem_u32(&s.bar_func[buf]), (fu >> 1) & 1, abort_flag)) { ok = false; break; }
-          ++fu;
         }
-        const int g = g0 + it;
-        if (!warp_wait_b(smem_u32(&s.bar_s_full[hh]), g & 1, abort_flag)) { ok = false; break; }
+        const int gv = 2 * (g0 + it) + hh;  // global half-step
+        const int k = gv % Smem::kSSlots;
+        const uint32_t xs = tS + 64 * k + lane_addr;
+        if (!warp_wait_b(smem_u32(&s.bar_s_full[k]), (gv / Smem::kSSlots) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
-#pragma unroll 1
+        // All of dP first, so that the dP slot is released for the next step.
+        uint32_t dv0[32], dv1[32], sv[32];
+        tmem_ld32(tdP + lane_addr, dv0);
+        tmem_ld32(tdP + lane_addr + 32, dv1);
+        tmem_ld32(xs, sv);
+        tmem_ld_wait(dv0);
+        tmem_ld_wait(dv1);
+        tmem_ld_wait(sv);
+        tc_fence_before();
+        mbar_arrive(smem_u32(&s.bar_dp_free));
+#pragma unroll
         for (int c = 0; c < 2; ++c) {
           const int chunk = 2 * hh + c;  // 32-column chunk of S / dP (of the 128)
-          uint32_t sv[32], dv[32];
-          tmem_ld32(tS + lane_addr + chunk * 32, sv);
-          tmem_ld32(tdP + lane_addr + chunk * 32, dv);
-          tmem_ld_wait(sv);
-          tmem_ld_wait(dv);
-          uint32_t pp[16], pd[16];
-          if (partial) {  // item-uniform: full tiles run no mask arithmetic
-            const uint32_t mask =
-                dkdv ? s.colmask[buf][chunk][r] : row_mask_word<NINT>(lo, hi, other * kBlock + chunk * 32);
-            if (dkdv) epilogue32<true, true>(sv, dv, mask, half_alpha, pp, pd);
-            else epilogue32<true, false>(sv, dv, mask, half_alpha, pp, pd);
-          } else {
-            if (dkdv) epilogue32<false, true>(sv, dv, 0u, half_alpha, pp, pd);
-            else epilogue32<false, false>(sv, dv, 0u, half_alpha, pp, pd);
+          if (c == 1) {
+            tmem_ld32(xs + 32, sv);
+            tmem_ld_wait(sv);
           }
-          // Packed over columns [64h + 16c, 64h + 16c + 16), which this warp
-          // has already read: K-step ks of the half's accumulating MMA reads
-          // columns [64h + 8ks, 64h + 8ks + 8).
-          const uint32_t dst = lane_addr + hh * 64 + c * 16;
-          if (dkdv) {
-            tmem_st16(tS + dst, pp);
-            tmem_st16(tdP + dst, pd);
+          const uint32_t(&dv)[32] = c == 0 ? dv0 : dv1;
+          if (partial) {  // item-uniform: full tiles run no mask arithmetic
+            const uint32_t mask = dkdv ? (c == 0 ? qmask0 : qmask1)
+                                       : row_mask_word<NINT>(lo, hi, other * kBlock + chunk * 32);
+            if (dkdv) convert_chunk<true, true>(sv, dv, mask, half_alpha, xs, c);
+            else convert_chunk<true, false>(sv, dv, mask, half_alpha, xs, c);
           } else {
-            tmem_st16(tS + dst, pd);
+            if (dkdv) convert_chunk<false, true>(sv, dv, 0u, half_alpha, xs, c);
+            else convert_chunk<false, false>(sv, dv, 0u, half_alpha, xs, c);
           }
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(smem_u32(&s.bar_p_full[hh]));
+        mbar_arrive(smem_u32(&s.bar_p_full[k]));
       }
       if (!ok) break;
       if (nt > 0) {
@@ -493,12 +529,12 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
       const int64_t row = static_cast<int64_t>(o0 + own_loc) * p.heads + h;
       if (dkdv) {
         store_acc_half<DP>(t_acc0 + lane_addr, half, nt > 0, valid, p.out2 + row * p.dim, p.dim,
-                           out_scale);  // dV
+                           out_scale, wide);  // dV
         store_acc_half<DP>(t_acc1 + lane_addr, half, nt > 0, valid, p.out1 + row * p.dim, p.dim,
-                           out_scale);  // dK
+                           out_scale, wide);  // dK
       } else {
         store_acc_half<DP>(t_acc0 + lane_addr, half, nt > 0, valid, p.out0 + row * p.dim, p.dim,
-                           out_scale);  // dQ
+                           out_scale, wide);  // dQ
       }
       if (nt > 0) {
         tc_fence_before();

@@ -331,6 +331,7 @@ __global__ void __launch_bounds__(320, 1) hstu_fwd_kernel(const __grid_constant_
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     const float half_alpha = 0.5f * p.alpha;
     const float out_scale = 0.5f * p.alpha * p.inv_n;  // hc = alpha / (2N)
+    const bool wide = wide_rows_ok(p.out0, p.out0, p.out0, p.dim);
     const int r = quarter * 32 + lane;                 // q row within the tile == TMEM lane
     int g = 0, o_uses = 0;
     bool ok = true;
@@ -365,30 +366,25 @@ __global__ void __launch_bounds__(320, 1) hstu_fwd_kernel(const __grid_constant_
       }
       if (*abort_flag) break;
       constexpr int kHalfCols = DP / 2;
+      constexpr int kNc = kHalfCols / 32;
       __nv_bfloat16* dst =
           p.out0 + (static_cast<int64_t>(o0 + qt * kBlock + r) * p.heads + h) * p.dim;
+      uint32_t v32[kNc][32];
+      if (nt > 0) {
 #pragma unroll
-      for (int cc = 0; cc < kHalfCols / 32; ++cc) {
+        for (int cc = 0; cc < kNc; ++cc) tmem_ld32(tO + lane_addr + grp * kHalfCols + cc * 32, v32[cc]);
+#pragma unroll
+        for (int cc = 0; cc < kNc; ++cc) tmem_ld_wait(v32[cc]);
+      } else {
+#pragma unroll
+        for (int cc = 0; cc < kNc; ++cc)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v32[cc][e] = 0u;
+      }
+#pragma unroll
+      for (int cc = 0; cc < kNc; ++cc) {
         const int col = grp * kHalfCols + cc * 32;
-        uint32_t v32[32];
-        if (nt > 0) {
-          tmem_ld32(tO + lane_addr + col, v32);
-          tmem_ld_wait(v32);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) v32[e] = 0u;
-        }
-        if (valid && col < p.dim) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e)
-            pk[e] = pack_bf16x2(out_scale * __uint_as_float(v32[2 * e]),
-                                out_scale * __uint_as_float(v32[2 * e + 1]));
-          uint4* d4 = reinterpret_cast<uint4*>(dst + col);
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            d4[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
-        }
+        if (valid && col < p.dim) store_row32(dst + col, v32[cc], out_scale, wide);
       }
       if (nt > 0) {
         tc_fence_before();

@@ -203,4 +203,36 @@ __device__ __forceinline__ float silu_gu(float s, float dp, float half_alpha) {
   return u * f;
 }
 
+// Stores 32 fp32 accumulator columns of one row, times `scale`, as bf16:
+// 64 bytes as two 32-byte stores when `wide` (a 32-byte aligned row), else
+// as four 16-byte stores. Each thread writes its own row, so every store
+// instruction of a warp touches 32 rows; wider stores halve their number.
+__device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const uint32_t (&a)[32], float scale,
+                                            bool wide) {
+  uint32_t pk[16];
+#pragma unroll
+  for (int e = 0; e < 16; ++e)
+    pk[e] = pack_bf16x2(scale * __uint_as_float(a[2 * e]), scale * __uint_as_float(a[2 * e + 1]));
+  if (wide) {
+#pragma unroll
+    for (int e = 0; e < 2; ++e)
+      asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst + 16 * e),
+                   "r"(pk[8 * e]), "r"(pk[8 * e + 1]), "r"(pk[8 * e + 2]), "r"(pk[8 * e + 3]),
+                   "r"(pk[8 * e + 4]), "r"(pk[8 * e + 5]), "r"(pk[8 * e + 6]), "r"(pk[8 * e + 7])
+                   : "memory");
+  } else {
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) d4[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+  }
+}
+
+// True when 32-byte stores of output rows of `dim` bf16 elements from these
+// bases stay aligned.
+__device__ __forceinline__ bool wide_rows_ok(const void* a, const void* b, const void* c, int dim) {
+  return ((reinterpret_cast<uintptr_t>(a) | reinterpret_cast<uintptr_t>(b) | reinterpret_cast<uintptr_t>(c)) &
+          31u) == 0 &&
+         (dim % 16) == 0;
+}
+
 }  // namespace hstu
