@@ -1,6 +1,8 @@
-// Backward kernel, persistent: one CTA per SM walks one longest-first work
-// list whose entries carry a role bit, so both roles run side by side and a
-// CTA keeps its pipelines running across items of either role.
+// Backward kernel, persistent: one CTA per SM takes work items, in the order
+// of one longest-first list whose entries carry a role bit, from a
+// device-wide counter; so both roles run side by side, CTAs that finish
+// early take the remaining items, and a CTA keeps its pipelines running
+// across items of either role.
 //
 // dK/dV role -- item (sequence b, kv tile kt, head h). K and V of the tile
 // stay in SMEM; the Q and dO tiles of every q tile that visits kt stream
@@ -179,8 +181,12 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int32_t* hdr = p.header;
   if (hdr[kHdrErr] != 0) return;
+  const bool uniform = hdr[kHdrUniform] != 0;
   const int n_work = hdr[kHdrNBwd] * p.heads;
-  if (static_cast<int>(blockIdx.x) >= n_work) return;
+  if (static_cast<int>(blockIdx.x) >= n_work) {
+    if (threadIdx.x == 0 && !uniform) finish_work(p.header, kHdrBwdNext, kHdrBwdDone);
+    return;
+  }
 
   if (threadIdx.x == 0) {
     s.abort_flag = 0;
@@ -217,7 +223,6 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
   const uint32_t tS = tbase + 256;      // S slot k at tS + 64 k
   const uint32_t tdP = tbase + 448;
   volatile int* abort_flag = &s.abort_flag;
-  const int stride = gridDim.x;
   const size_t nt_all = static_cast<size_t>(p.nt);
 
   if (warp == 8) {
@@ -227,10 +232,25 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
     int gs = 0;        // streamed tiles over all items
     bool ok = true;
     int i = 0;
-    for (int w = blockIdx.x; ok && w < n_work; w += stride, ++i) {
+    for (; ok; ++i) {
       const int slot = i & 1;
       if (i >= 2 && !warp_wait_b(smem_u32(&s.bar_item_empty[slot]), ((i >> 1) - 1) & 1, abort_flag)) {
         ok = false;
+        break;
+      }
+      // Work is handed out in list order (longest first): by a fixed stride
+      // of the grid when all sequences are equally long, else dynamically,
+      // so that CTAs finishing early take the remaining items.
+      int w = static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
+      if (!uniform) {
+        if (lane == 0) w = fetch_work(p.header, kHdrBwdNext);
+        w = __shfl_sync(0xffffffffu, w, 0);
+      }
+      if (w >= n_work) {  // no more work: an item with nt = -1 tells the other roles
+        if (lane == 0) s.item[slot].nt = -1;
+        __threadfence_block();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&s.bar_item_full[slot]));
         break;
       }
       const int code = p.list[w / p.heads];
@@ -343,10 +363,11 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
       int res_uses = 0;  // items with at least one tile
       bool ok = true;
       int i = 0;
-      for (int w = blockIdx.x; ok && w < n_work; w += stride, ++i) {
+      for (; ok; ++i) {
         const int slot = i & 1;
         if (!mbar_wait(smem_u32(&s.bar_item_full[slot]), (i >> 1) & 1, abort_flag)) break;
         const int nt = s.item[slot].nt;
+        if (nt < 0) break;  // no more work
         const bool dkdv = s.item[slot].dkdv != 0;
         mbar_arrive(smem_u32(&s.bar_item_empty[slot]));
         if (nt == 0) continue;
@@ -439,10 +460,11 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
     int acc_uses = 0;
     bool ok = true;
     int i = 0;
-    for (int w = blockIdx.x; ok && w < n_work; w += stride, ++i) {
+    for (; ok; ++i) {
       const int slot = i & 1;
       if (!warp_wait_b(smem_u32(&s.bar_item_full[slot]), (i >> 1) & 1, abort_flag)) break;
       const BwdItem& item = s.item[slot];
+      if (item.nt < 0) break;  // no more work
       const bool dkdv = item.dkdv != 0;
       const int nt = item.nt, tile = item.tile, h = item.h, o0 = item.o0, L = item.L;
       const int own_loc = tile * kBlock + r;
@@ -553,6 +575,7 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
     tmem_dealloc(tbase, 512);
   }
   if (threadIdx.x == 0 && s.abort_flag) atomicOr(p.header + kHdrErr, kErrTimeout);
+  if (threadIdx.x == 0 && !uniform) finish_work(p.header, kHdrBwdNext, kHdrBwdDone);
 }
 
 template <int DP, int NINT>

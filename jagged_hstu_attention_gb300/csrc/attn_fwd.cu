@@ -1,6 +1,6 @@
-// Forward kernel, persistent: one CTA per SM walks the work list (sequence
-// b, q tile qt, head h; longest sequences first) with a stride of the grid
-// size, and keeps every pipeline running across work items.
+// Forward kernel, persistent: one CTA per SM takes work items (sequence b,
+// q tile qt, head h; longest sequences first) from a device-wide counter in
+// list order, and keeps every pipeline running across work items.
 //
 //   warp 8      producer. All 32 lanes build the next item's list of visited
 //               kv tiles (from the plan's tile classes) into one of two item
@@ -120,8 +120,12 @@ __global__ void __launch_bounds__(320, 1) hstu_fwd_kernel(const __grid_constant_
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int32_t* hdr = p.header;
   if (hdr[kHdrErr] != 0) return;
+  const bool uniform = hdr[kHdrUniform] != 0;
   const int n_work = hdr[kHdrNFwd] * p.heads;
-  if (static_cast<int>(blockIdx.x) >= n_work) return;
+  if (static_cast<int>(blockIdx.x) >= n_work) {
+    if (threadIdx.x == 0 && !uniform) finish_work(p.header, kHdrFwdNext, kHdrFwdDone);
+    return;
+  }
 
   if (threadIdx.x == 0) {
     s.abort_flag = 0;
@@ -156,7 +160,6 @@ __global__ void __launch_bounds__(320, 1) hstu_fwd_kernel(const __grid_constant_
   const uint32_t tbase = s.tmem_base;
   const uint32_t tO = tbase + 384;  // O accumulator columns [384, 384 + DP)
   volatile int* abort_flag = &s.abort_flag;
-  const int stride = gridDim.x;
 
   if (warp == 8) {
     // ------------------------------------------------------------ producer
@@ -166,10 +169,25 @@ __global__ void __launch_bounds__(320, 1) hstu_fwd_kernel(const __grid_constant_
     int g = 0;       // tiles issued over all items
     bool ok = true;
     int i = 0;
-    for (int w = blockIdx.x; ok && w < n_work; w += stride, ++i) {
+    for (; ok; ++i) {
       const int slot = i & 1;
       if (i >= 2 && !warp_wait(smem_u32(&s.bar_item_empty[slot]), ((i >> 1) - 1) & 1, abort_flag)) {
         ok = false;
+        break;
+      }
+      // Work is handed out in list order (longest first): by a fixed stride
+      // of the grid when all sequences are equally long, else dynamically,
+      // so that CTAs finishing early take the remaining items.
+      int w = static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
+      if (!uniform) {
+        if (lane == 0) w = fetch_work(p.header, kHdrFwdNext);
+        w = __shfl_sync(0xffffffffu, w, 0);
+      }
+      if (w >= n_work) {  // no more work: an item with nt = -1 tells the other roles
+        if (lane == 0) s.item[slot].nt = -1;
+        __threadfence_block();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&s.bar_item_full[slot]));
         break;
       }
       const int code = p.list[w / p.heads];
@@ -267,10 +285,11 @@ __global__ void __launch_bounds__(320, 1) hstu_fwd_kernel(const __grid_constant_
       int q_uses = 0;  // items with at least one tile
       bool ok = true;
       int i = 0;
-      for (int w = blockIdx.x; ok && w < n_work; w += stride, ++i) {
+      for (; ok; ++i) {
         const int slot = i & 1;
         if (!mbar_wait(smem_u32(&s.bar_item_full[slot]), (i >> 1) & 1, abort_flag)) break;
         const int nt = s.item[slot].nt;
+        if (nt < 0) break;  // no more work
         mbar_arrive(smem_u32(&s.bar_item_empty[slot]));
         if (nt == 0) continue;
         if (!mbar_wait(smem_u32(&s.bar_q_full), q_uses & 1, abort_flag)) break;
@@ -336,10 +355,11 @@ __global__ void __launch_bounds__(320, 1) hstu_fwd_kernel(const __grid_constant_
     int g = 0, o_uses = 0;
     bool ok = true;
     int i = 0;
-    for (int w = blockIdx.x; ok && w < n_work; w += stride, ++i) {
+    for (; ok; ++i) {
       const int slot = i & 1;
       if (!warp_wait(smem_u32(&s.bar_item_full[slot]), (i >> 1) & 1, abort_flag)) break;
       const FwdItem& item = s.item[slot];
+      if (item.nt < 0) break;  // no more work
       const int nt = item.nt, qt = item.qt, h = item.h, o0 = item.o0, L = item.L;
       const int i_loc = qt * kBlock + r;
       const bool valid = i_loc < L;
@@ -403,6 +423,7 @@ __global__ void __launch_bounds__(320, 1) hstu_fwd_kernel(const __grid_constant_
     tmem_dealloc(tbase, 512);
   }
   if (threadIdx.x == 0 && s.abort_flag) atomicOr(p.header + kHdrErr, kErrTimeout);
+  if (threadIdx.x == 0 && !uniform) finish_work(p.header, kHdrFwdNext, kHdrFwdDone);
 }
 
 // Number of SMs of the current device (looked up per call; cheap).

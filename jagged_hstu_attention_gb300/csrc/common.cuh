@@ -23,6 +23,18 @@ constexpr int kHdrErr = 0;     // error bits (kErrInput | kErrTimeout)
 constexpr int kHdrNFwd = 1;    // entries of the forward work list
 constexpr int kHdrNBwd = 2;    // entries of the backward work list
 constexpr int kHdrTicket = 3;  // plan blocks finished (the last one builds the lists)
+// Dynamic work distribution of the persistent attention kernels: the next
+// work index to hand out and the CTAs that have finished. The last CTA of a
+// launch puts both back to zero, so that a reused plan starts clean.
+constexpr int kHdrFwdNext = 4;
+constexpr int kHdrFwdDone = 5;
+constexpr int kHdrBwdNext = 6;
+constexpr int kHdrBwdDone = 7;
+// 1 when every sequence has the same tile count. Then striding the list by
+// the grid size already hands every CTA the same mix of items, and the
+// persistent kernels use that fixed assignment; otherwise they take items
+// from the counters above, which balances ragged batches.
+constexpr int kHdrUniform = 8;
 constexpr int kHdrWords = 64;  // 256 bytes
 constexpr int kErrInput = 1;
 constexpr int kErrTimeout = 2;
@@ -57,6 +69,20 @@ inline FullLayout full_layout(int batch, int max_seqlen) {
   l.cls = l.ivmask + align_up(items, 256);
   l.total = l.cls + align_up(items * l.nt, 256);
   return l;
+}
+
+// Hands out the next work index of a persistent kernel (one thread).
+__device__ __forceinline__ int fetch_work(int32_t* header, int next_word) {
+  return atomicAdd(header + next_word, 1);
+}
+// Called once per CTA after all its roles have finished; the last CTA of the
+// launch resets the counters for the next launch on the same plan.
+__device__ __forceinline__ void finish_work(int32_t* header, int next_word, int done_word) {
+  __threadfence();
+  if (atomicAdd(header + done_word, 1) == static_cast<int>(gridDim.x) - 1) {
+    atomicExch(header + next_word, 0);
+    atomicExch(header + done_word, 0);
+  }
 }
 
 // Targets-only: keys per CTA chunk and the workspace of fp32 partials.

@@ -174,6 +174,8 @@ __device__ void build_work_lists(const PlanParams& p) {
   if (tid == 0) {
     p.header[kHdrNFwd] = n_items;
     p.header[kHdrNBwd] = 2 * n_items;
+    // seq_order is sorted by tile count: equal ends mean equal counts.
+    p.header[kHdrUniform] = tiles_of(p.seq_order[0]) == tiles_of(p.seq_order[p.batch - 1]) ? 1 : 0;
   }
 }
 
