@@ -198,36 +198,58 @@ def time_legs(legs, steps, warmup, flush):
 
 
 def e2e_leg(leg, steps, warmup):
-    """Same step through the C ABI from pinned HOST buffers: copies of the
-    step's inputs in, of its outputs out, inside the timed region."""
+    """Same step through the C ABI from pinned HOST buffers: every step copies
+    its inputs in and its outputs out, inside the timed region. The steps are
+    pipelined over three streams (inputs of step i + 1 go in while step i
+    computes and the outputs of step i - 1 come out), with two device buffer
+    sets, the way a training loop feeds a device from host memory."""
     import torch
     hb = leg.hb
     pin = lambda t: t.cpu().pin_memory()
     h_in = [pin(t) for t in (leg.q, leg.k, leg.v, leg.do, leg.d_off, leg.d_func)]
-    h_out = [torch.empty(leg.q.shape, dtype=leg.q.dtype).pin_memory() for _ in range(4)]
-    d_in = [torch.empty_like(t, device="cuda") for t in h_in]
-    d_out = [torch.empty_like(leg.q) for _ in range(4)]
+    h_out = [[torch.empty(leg.q.shape, dtype=leg.q.dtype).pin_memory() for _ in range(4)] for _ in range(2)]
+    d_in = [[torch.empty_like(t, device="cuda") for t in h_in] for _ in range(2)]
+    d_out = [[torch.empty_like(leg.q) for _ in range(4)] for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in h_in)
-    d2h = sum(t.numel() * t.element_size() for t in h_out)
+    d2h = sum(t.numel() * t.element_size() for t in h_out[0])
+    s_in, s_comp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_comp = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
 
-    def one():
-        for d, h in zip(d_in, h_in):
-            d.copy_(h, non_blocking=True)
-        q, k, v, do, off, func = d_in
-        hb.plan(off, func, leg.shape, leg.ws)
-        hb.fwd(q, k, v, off, func, leg.N, leg.alpha, ws=leg.ws, reuse_plan=True, out=d_out[0])
-        hb.bwd(do, q, k, v, off, func, leg.N, leg.alpha, ws=leg.ws, reuse_plan=True, outs=tuple(d_out[1:]))
-        for h, d in zip(h_out, d_out):
-            h.copy_(d, non_blocking=True)
+    def one(i):
+        b = i % 2
+        s_in.wait_event(ev_comp[b])  # step i - 2 has finished reading buffer set b
+        with torch.cuda.stream(s_in):
+            for d, h in zip(d_in[b], h_in):
+                d.copy_(h, non_blocking=True)
+        ev_in[b].record(s_in)
+        s_comp.wait_event(ev_in[b])
+        s_comp.wait_event(ev_out[b])  # outputs of step i - 2 have left buffer set b
+        q, k, v, do, off, func = d_in[b]
+        hb.plan(off, func, leg.shape, leg.ws, stream=s_comp)
+        hb.fwd(q, k, v, off, func, leg.N, leg.alpha, ws=leg.ws, reuse_plan=True, out=d_out[b][0],
+               stream=s_comp)
+        hb.bwd(do, q, k, v, off, func, leg.N, leg.alpha, ws=leg.ws, reuse_plan=True,
+               outs=tuple(d_out[b][1:]), stream=s_comp)
+        ev_comp[b].record(s_comp)
+        s_out.wait_event(ev_comp[b])
+        with torch.cuda.stream(s_out):
+            for h, d in zip(h_out[b], d_out[b]):
+                h.copy_(d, non_blocking=True)
+        ev_out[b].record(s_out)
 
-    for _ in range(warmup):
-        one()
+    for i in range(warmup):
+        one(i)
     torch.cuda.synchronize()
+    main = torch.cuda.current_stream()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(steps):
-        one()
-    e1.record()
+    e0.record(main)
+    s_in.wait_event(e0)
+    for i in range(warmup, warmup + steps):
+        one(i)
+    main.wait_stream(s_out)
+    e1.record(main)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
     return ms, h2d, d2h
