@@ -61,9 +61,21 @@ __device__ void classify_tile(const PlanParams& p) {
 
   int count = 0;
   for (int j = 0; j < ntiles; ++j) {
-    int c = 0;
+    // Most tiles lie wholly inside one interval or outside all of them (an
+    // empty interval is [0,0) and never meets a tile); only the others need
+    // the row's column bits.
+    const int s0 = j * kBlock;
+    bool none = true, cover = false;
 #pragma unroll
-    for (int w = 0; w < 4; ++w) c += __popc(row_mask_word<NINT>(lo, hi, j * kBlock + 32 * w));
+    for (int t = 0; t < NINT; ++t) {
+      none = none && (hi[t] <= s0 || lo[t] >= s0 + kBlock);
+      cover = cover || (lo[t] <= s0 && hi[t] >= s0 + kBlock);
+    }
+    int c = cover ? kBlock : 0;
+    if (!cover && !none) {
+#pragma unroll
+      for (int w = 0; w < 4; ++w) c += __popc(row_mask_word<NINT>(lo, hi, s0 + 32 * w));
+    }
     count += c;
     const unsigned any = __ballot_sync(0xffffffffu, c > 0);
     const unsigned all = __ballot_sync(0xffffffffu, c == kBlock);
