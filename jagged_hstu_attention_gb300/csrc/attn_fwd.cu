@@ -109,8 +109,12 @@ __device__ __forceinline__ void fwd_tile_epilogue(uint32_t sb, int col0, const i
   }
 }
 
+// 16 warps: 0-11 three epilogue groups, 12 producer, 13 MMA issuer, 14-15
+// idle; 128 registers a thread fill the register file.
+constexpr int kFwdThreads = 512;
+
 template <int DP, int NINT>
-__global__ void __launch_bounds__(320, 1) hstu_fwd_kernel(const __grid_constant__ AttnParams p) {
+__global__ void __launch_bounds__(kFwdThreads, 1) hstu_fwd_kernel(const __grid_constant__ AttnParams p) {
   using Smem = FwdSmem<DP>;
   constexpr int NS = Smem::kStages;
   constexpr int kTile = Smem::kTile;
@@ -142,15 +146,15 @@ __global__ void __launch_bounds__(320, 1) hstu_fwd_kernel(const __grid_constant_
       mbar_init(smem_u32(&s.bar_p_full[i]), 128);
     }
     mbar_init(smem_u32(&s.bar_o_full), 1);
-    mbar_init(smem_u32(&s.bar_o_empty), 256);
+    mbar_init(smem_u32(&s.bar_o_empty), 256);  // epilogue groups 0 and 1 read O out
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&s.bar_item_full[i]), 1);
-      mbar_init(smem_u32(&s.bar_item_empty[i]), 1 + 256);  // MMA issuer + epilogue threads
+      mbar_init(smem_u32(&s.bar_item_empty[i]), 1 + 384);  // MMA issuer + epilogue threads
     }
     mbar_init(smem_u32(&s.bar_drain), 1);
     fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == 13) {
     tmem_alloc(smem_u32(&s.tmem_base), 512);
     tmem_relinquish();
   }
@@ -161,7 +165,7 @@ __global__ void __launch_bounds__(320, 1) hstu_fwd_kernel(const __grid_constant_
   const uint32_t tO = tbase + 384;  // O accumulator columns [384, 384 + DP)
   volatile int* abort_flag = &s.abort_flag;
 
-  if (warp == 8) {
+  if (warp == 12) {
     // ------------------------------------------------------------ producer
     int k_last[NS], v_last[NS];
     for (int i = 0; i < NS; ++i) k_last[i] = v_last[i] = -1;
@@ -272,7 +276,7 @@ __global__ void __launch_bounds__(320, 1) hstu_fwd_kernel(const __grid_constant_
       }
     }
     __syncwarp();
-  } else if (warp == 9) {
+  } else if (warp == 13) {
     // ------------------------------------------------------------ MMA issuer
     if (elect_one_sync()) {
       constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
@@ -344,9 +348,9 @@ __global__ void __launch_bounds__(320, 1) hstu_fwd_kernel(const __grid_constant_
       mbar_wait_drain(smem_u32(&s.bar_drain), 0);
     }
     __syncwarp();
-  } else {
+  } else if (warp < 12) {
     // ------------------------------------------------------------ epilogue
-    const int quarter = warp & 3, grp = warp >> 2;
+    const int quarter = warp & 3, grp = warp >> 2;  // three groups of four warps
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     const float half_alpha = 0.5f * p.alpha;
     const float out_scale = 0.5f * p.alpha * p.inv_n;  // hc = alpha / (2N)
@@ -366,8 +370,8 @@ __global__ void __launch_bounds__(320, 1) hstu_fwd_kernel(const __grid_constant_
       int lo[NINT], hi[NINT];
       const uint32_t active = p.ivmask[static_cast<size_t>(item.b) * p.nt + qt];
       load_row_intervals<NINT>(p.func, p.total, static_cast<int64_t>(o0) + i_loc, L, valid, lo, hi, active);
-      // Ping-pong: this group takes the tiles with g % 2 == grp.
-      for (int t = (g & 1) == grp ? 0 : 1; t < nt; t += 2) {
+      // This group takes the tiles with g % 3 == grp, always S buffer grp.
+      for (int t = ((grp - g) % 3 + 3) % 3; t < nt; t += 3) {
         const int gg = g + t, sbuf = gg % 3;
         if (!warp_wait(smem_u32(&s.bar_s_full[sbuf]), (gg / 3) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
@@ -380,6 +384,11 @@ __global__ void __launch_bounds__(320, 1) hstu_fwd_kernel(const __grid_constant_
         mbar_arrive(smem_u32(&s.bar_p_full[sbuf]));
       }
       if (!ok) break;
+      if (grp == 2) {  // groups 0 and 1 read O out; this one goes on to the next item
+        mbar_arrive(smem_u32(&s.bar_item_empty[slot]));
+        g += nt;
+        continue;
+      }
       if (nt > 0) {
         if (!warp_wait(smem_u32(&s.bar_o_full), o_uses & 1, abort_flag)) break;
         tc_fence_after();
@@ -418,7 +427,7 @@ __global__ void __launch_bounds__(320, 1) hstu_fwd_kernel(const __grid_constant_
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == 13) {
     tc_fence_after();
     tmem_dealloc(tbase, 512);
   }
@@ -450,7 +459,7 @@ static cudaError_t launch_fwd_t(const AttnParams& p, int grid_items, cudaStream_
   cudaError_t e = sm_count(&sms);
   if (e != cudaSuccess) return e;
   const long long ctas = work < sms ? work : sms;  // persistent: one CTA per SM
-  hstu_fwd_kernel<DP, NINT><<<static_cast<unsigned>(ctas), 320, smem, stream>>>(p);
+  hstu_fwd_kernel<DP, NINT><<<static_cast<unsigned>(ctas), kFwdThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
