@@ -2,14 +2,14 @@
 // q tile qt, head h; longest sequences first) from a device-wide counter in
 // list order, and keeps every pipeline running across work items.
 //
-//   warp 8      producer. All 32 lanes build the next item's list of visited
+//   warp 12     producer. All 32 lanes build the next item's list of visited
 //               kv tiles (from the plan's tile classes) into one of two item
 //               slots; lane 0 then loads the item's Q tile and the K and V
 //               tiles of every visited kv tile by TMA into two rings of
 //               kStages (3 at D=128, 4 at D<=64). K frees after QK^T, V after
 //               PV, so the next item's Q and K arrive while the current item
 //               finishes.
-//   warp 9      TMEM owner and MMA issuer (one elected lane):
+//   warp 13     TMEM owner and MMA issuer (one elected lane):
 //                 S[g % 3] = Q K^T             (tcgen05, SMEM x SMEM)
 //                 O       += P[g % 3] V        (tcgen05, TMEM x SMEM)
 //               with g the tile index counted over all items of the CTA. S
@@ -17,16 +17,20 @@
 //               buffer while the epilogue groups work on the other two. The
 //               first PV of an item waits until the epilogue has read out the
 //               previous item's O.
-//   warps 0-7   epilogue, two groups of four warps that ping-pong over the
-//               tiles: group gr (warps 4gr..4gr+3, TMEM lanes 32(w%4)..) takes
-//               the tiles with g % 2 == gr. Per tile: P' = S (1 + tanh(alpha
-//               S / 2)) (that is silu(alpha S) / N up to the factor
-//               alpha / (2N), applied once to O at the store), with the row's
-//               interval mask on partial tiles only (full tiles run no mask
-//               arithmetic), packed to bf16 in place over the first 64
-//               columns of the buffer. At the end of an item each group
-//               stores half of O's columns (bf16, rows past L_b untouched;
-//               rows that see no column get zeros).
+//   warps 0-11  epilogue, three groups of four warps: group gr (warps
+//               4gr..4gr+3, TMEM lanes 32(w%4)..) takes the tiles with
+//               g % 3 == gr, so always S buffer gr. Per tile: P' = S (1 +
+//               tanh(alpha S / 2)) (that is silu(alpha S) / N up to the
+//               factor alpha / (2N), applied once to O at the store), with
+//               the row's interval mask on partial tiles only (full tiles run
+//               no mask arithmetic), packed to bf16 in place over the first 64
+//               columns of the buffer. At the end of an item groups 0 and 1
+//               each store half of O's columns (bf16, rows past L_b
+//               untouched; rows that see no column get zeros) while group 2
+//               goes on to the next item.
+//   warps 14-15 idle: 16 warps at 128 registers fill the register file, and
+//               a third epilogue group hides more TMEM and MUFU latency than
+//               two groups at 168 registers.
 //
 // TMEM (512 columns): S0 [0,128), S1 [128,256), S2 [256,384), O [384, 384+DP).
 // Packed P of buffer b occupies columns [128b, 128b+64).
