@@ -211,3 +211,53 @@ def test_device_side_offset_error_sets_status_and_writes_nothing():
     o2 = hb.fwd(gb.q, gb.k, gb.v, gb.d_off, gb.d_func, 100, gb.alpha, ws=ws)
     assert hb.device_status(ws) == hb.HSTU_OK
     assert torch.isfinite(o2.float()).all()
+
+
+def _launch(gb, ws, shape, reuse):
+    o = hb.fwd(gb.q, gb.k, gb.v, gb.d_off, gb.d_func, gb.max_seqlen, gb.alpha, ws=ws, reuse_plan=reuse)
+    dq, dk, dv = hb.bwd(gb.do, gb.q, gb.k, gb.v, gb.d_off, gb.d_func, gb.max_seqlen, gb.alpha, ws=ws,
+                        reuse_plan=True)
+    torch.cuda.synchronize()
+    assert hb.device_status(ws) == hb.HSTU_OK
+    return {"o": o, "dq": dq, "dk": dk, "dv": dv}
+
+
+def test_reused_plan_hands_out_all_work_every_launch():
+    # A ragged batch takes its work from device counters; they must be back
+    # at zero after every launch, or a later launch on the same plan would
+    # find no work left.
+    gb = GpuBatch.from_config(wl.CONFIGS["onerank_b64"], 3)
+    shape = hb.make_shape(len(gb.lens), gb.total, gb.q.shape[1], gb.q.shape[2], gb.nfunc, gb.max_seqlen,
+                          gb.alpha)
+    ws = hb.alloc_workspace(shape, hb.WS_FULL)
+    first = _launch(gb, ws, shape, reuse=False)
+    for _ in range(3):
+        again = _launch(gb, ws, shape, reuse=True)
+        for n in ("o", "dq", "dk", "dv"):
+            assert torch.equal(first[n], again[n]), n
+    sub = sample_seqs(gb.lens, 3, seed=0)
+    ref = gb.oracle(sub)
+    rows = torch.as_tensor(ref["rows"], device="cuda", dtype=torch.long)
+    check_o(np64(first["o"].index_select(0, rows)), ref["o"])
+    check_grad(np64(first["dq"].index_select(0, rows)), ref["dq"], "dq")
+
+
+def test_workspace_switches_between_equal_length_and_ragged_batches():
+    # An equal-length batch is split by a fixed stride, a ragged one through
+    # the counters; one workspace serves both in turn.
+    uni = GpuBatch.from_config(wl.CONFIGS["sla_b32_s1024"], 0)
+    rag = GpuBatch.from_config(wl.CONFIGS["tiny"], 5)
+    big = hb.make_shape(len(uni.lens), uni.total, uni.q.shape[1], uni.q.shape[2], uni.nfunc, uni.max_seqlen,
+                        uni.alpha)
+    ws = hb.alloc_workspace(big, hb.WS_FULL)
+    for gb in (rag, uni, rag):
+        shape = hb.make_shape(len(gb.lens), gb.total, gb.q.shape[1], gb.q.shape[2], gb.nfunc, gb.max_seqlen,
+                              gb.alpha)
+        assert ws.numel() >= hb.workspace_size(shape, hb.WS_FULL)
+        out = _launch(gb, ws, shape, reuse=False)
+        out2 = _launch(gb, ws, shape, reuse=True)
+        for n in ("o", "dq", "dk", "dv"):
+            assert torch.equal(out[n], out2[n]), n
+    ref = rag.oracle()
+    check_o(np64(out["o"]), ref["o"])
+    check_grad(np64(out["dk"]), ref["dk"], "dk")
