@@ -227,6 +227,16 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
 
   if (warp == 8) {
     // ------------------------------------------------------------ producer
+    if (lane == 0) {  // descriptors into the TMA unit's cache before the first copy
+      tma_prefetch_map(&p.tm_q);
+      tma_prefetch_map(&p.tm_k);
+      tma_prefetch_map(&p.tm_v);
+      tma_prefetch_map(&p.tm_do);
+      tma_prefetch_map(&p.tm_q64);
+      tma_prefetch_map(&p.tm_k64);
+      tma_prefetch_map(&p.tm_v64);
+      tma_prefetch_map(&p.tm_do64);
+    }
     int str_last[Smem::kSlots] = {-1, -1, -1, -1};
     int res_uses = 0;  // items with at least one tile (one resident load each)
     int gs = 0;        // streamed tiles over all items
@@ -306,17 +316,6 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
             }
             ++res_uses;
           }
-          // Streamed halves are first requested into L2 kPrefetch halves ahead of
-          // their load, which covers most of the HBM latency of the load.
-          constexpr int kPrefetch = 4;
-          auto prefetch_half = [&](int t) {
-            const int prow0 = o0 + (it_slot.idx[t >> 1] & 0xff) * kBlock + (t & 1) * (kBlock / 2);
-            for (int c = 0; c < Smem::kChunks; ++c) {
-              tma_prefetch_l2_3d(m_str0, c * 64, h, prow0);
-              tma_prefetch_l2_3d(m_str1, c * 64, h, prow0);
-            }
-          };
-          for (int t = 0; t < kPrefetch && t < 2 * n; ++t) prefetch_half(t);
           for (int t = 0; ok && t < 2 * n; ++t) {  // 64-row halves
             const int gh = 2 * gs + t, st = gh % Smem::kSlots, use = gh / Smem::kSlots;
             if (use > 0 && !mbar_wait(smem_u32(&s.bar_empty[st]), (use - 1) & 1, abort_flag)) {
@@ -331,7 +330,6 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
               tma_load_3d(smem_u32(s.str1[st] + c * kHalfChunk), m_str1, bar, c * 64, h, srow0);
             }
             str_last[st] = use;
-            if (t + kPrefetch < 2 * n) prefetch_half(t + kPrefetch);
           }
           gs += n;
         }

@@ -171,6 +171,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1) hstu_fwd_kernel(const __grid_c
 
   if (warp == 12) {
     // ------------------------------------------------------------ producer
+    if (lane == 0) {  // descriptors into the TMA unit's cache before the first copy
+      tma_prefetch_map(&p.tm_q);
+      tma_prefetch_map(&p.tm_k);
+      tma_prefetch_map(&p.tm_v);
+    }
     int k_last[NS], v_last[NS];
     for (int i = 0; i < NS; ++i) k_last[i] = v_last[i] = -1;
     int q_uses = 0;  // items with at least one tile (one Q load each)

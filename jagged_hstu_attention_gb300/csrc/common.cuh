@@ -200,32 +200,6 @@ __device__ __forceinline__ float tanh_approx(float x) {
   return y;
 }
 
-// 2^x on the MUFU unit (PTX ex2.approx, flush-to-zero).
-__device__ __forceinline__ float ex2_approx(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-// The same P' = s (1 + tanh(alpha s / 2)) = 2 s sigma(alpha s) as silu_pu, with
-// one ex2 instead of one tanh on the MUFU unit (ex2 issues at twice tanh's
-// rate) and the reciprocal on the FMA pipe:
-//   d = (1 + 2^(-alpha s log2 e)) / 2,  P' = s / d,
-//   1/d by two Newton-Raphson steps r <- r (2 - d r) from the bit-pattern
-//   seed r0 = float(K - bits(d)). K = 0x7ef311c0 minimises the seed's largest
-//   relative error over a binade (5.1%), so two steps leave below 1e-5, far
-//   under the bf16 rounding of P'. The exponent is clamped at 64 so that d
-//   stays finite; s / d is then below 2^-60 |s| where the clamp acts.
-// `neg_alpha_log2e` is -alpha * log2(e).
-__device__ __forceinline__ float silu_pu_ex2(float s, float neg_alpha_log2e) {
-  const float x = fminf(s * neg_alpha_log2e, 64.0f);
-  const float d = fmaf(ex2_approx(x), 0.5f, 0.5f);
-  float r = __int_as_float(0x7ef311c0 - __float_as_int(d));
-  r = r * fmaf(-d, r, 2.0f);
-  r = r * fmaf(-d, r, 2.0f);
-  return s * r;
-}
-
 // Epilogue arithmetic on one S element s, with t = tanh(alpha s / 2) so that
 // sigmoid(alpha s) = (1 + t) / 2 (one MUFU op per element). The common factor
 // hc = alpha / (2N) is left out of every element and applied once to the fp32

@@ -91,19 +91,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
       : "memory");
 }
-// Brings the box at {x, y, z} of a 3-D tensor map into L2 without a
-// destination in shared memory (same alignment rule on x as tma_load_3d).
-__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int x, int y, int z) {
-  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(x), "r"(y), "r"(z)
-               : "memory");
-}
-// Makes generic-proxy shared-memory writes visible to the async proxy (UMMA).
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 // ---------------------------------------------------------------- TMEM
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
@@ -153,10 +140,6 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
       : "memory");
 }
 // Two 32-column loads, one wait: 64 columns in flight per thread.
-__device__ __forceinline__ void tmem_ld_wait2(uint32_t (&a)[32], uint32_t (&b)[32]) {
-  tmem_ld_wait(a);
-  tmem_ld_wait(b);
-}
 // 32 lanes x 16 consecutive 32-bit columns, thread t writes lane (lane + t).
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
   asm volatile(
