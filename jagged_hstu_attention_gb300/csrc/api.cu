@@ -43,20 +43,23 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// (tokens, H, D) bf16 viewed as a 3-D tensor {D, H, tokens}; box = 64
-// columns x 1 head x box_rows rows with 128-byte swizzle. For D = 32 the box is
-// wider than the tensor and TMA fills the missing columns with zeros.
+// (tokens, H, D) bf16 viewed as a 4-D tensor {64 columns, tokens, H, D / 64
+// chunks} with the chunk stride (128 B) below the row stride. One box of
+// 64 columns x box_rows rows x 1 head x all chunks, with 128-byte swizzle,
+// lands in shared memory as [chunk][row][128 B]: the K-major layout of the
+// kernels' UMMA descriptors, in one TMA instruction per tile. For D = 32 the
+// box is wider than the tensor and TMA fills the missing columns with zeros.
 bool make_map(CUtensorMap* m, const void* ptr, int64_t tokens, int heads, int dim,
               int box_rows = kBlock) {
   auto fn = encode_fn();
   if (!fn) return false;
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(dim), static_cast<cuuint64_t>(heads),
-                        static_cast<cuuint64_t>(tokens)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(dim) * 2,
-                           static_cast<cuuint64_t>(heads) * dim * 2};
-  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(box_rows)};
-  cuuint32_t es[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
+  const cuuint64_t chunks = dim > 64 ? static_cast<cuuint64_t>(dim / 64) : 1;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(dim < 64 ? dim : 64), static_cast<cuuint64_t>(tokens),
+                        static_cast<cuuint64_t>(heads), chunks};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(heads) * dim * 2, static_cast<cuuint64_t>(dim) * 2, 128};
+  cuuint32_t box[4] = {64, static_cast<cuuint32_t>(box_rows), 1, static_cast<cuuint32_t>(chunks)};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

@@ -310,10 +310,8 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
             const uint32_t br = smem_u32(&s.bar_res_full);
             mbar_expect_tx(br, 2 * kTile);
             const int row0 = o0 + tile * kBlock;
-            for (int c = 0; c < Smem::kChunks; ++c) {
-              tma_load_3d(smem_u32(s.res0 + c * kChunkBytes), m_res0, br, c * 64, h, row0);
-              tma_load_3d(smem_u32(s.res1 + c * kChunkBytes), m_res1, br, c * 64, h, row0);
-            }
+            tma_load_4d(smem_u32(s.res0), m_res0, br, 0, row0, h, 0);
+            tma_load_4d(smem_u32(s.res1), m_res1, br, 0, row0, h, 0);
             ++res_uses;
           }
           for (int t = 0; ok && t < 2 * n; ++t) {  // 64-row halves
@@ -325,10 +323,8 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
             const int srow0 = o0 + (it_slot.idx[t >> 1] & 0xff) * kBlock + (t & 1) * (kBlock / 2);
             const uint32_t bar = smem_u32(&s.bar_full[st]);
             mbar_expect_tx(bar, 2 * Smem::kHalfTile);
-            for (int c = 0; c < Smem::kChunks; ++c) {
-              tma_load_3d(smem_u32(s.str0[st] + c * kHalfChunk), m_str0, bar, c * 64, h, srow0);
-              tma_load_3d(smem_u32(s.str1[st] + c * kHalfChunk), m_str1, bar, c * 64, h, srow0);
-            }
+            tma_load_4d(smem_u32(s.str0[st]), m_str0, bar, 0, srow0, h, 0);
+            tma_load_4d(smem_u32(s.str1[st]), m_str1, bar, 0, srow0, h, 0);
             str_last[st] = use;
           }
           gs += n;

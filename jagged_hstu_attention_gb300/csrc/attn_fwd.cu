@@ -237,9 +237,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) hstu_fwd_kernel(const __grid_c
           if (q_uses > 0 && !mbar_wait(smem_u32(&s.bar_q_empty), (q_uses - 1) & 1, abort_flag)) ok = false;
           if (ok) {
             mbar_expect_tx(smem_u32(&s.bar_q_full), kTile);
-            for (int c = 0; c < Smem::kChunks; ++c)
-              tma_load_3d(smem_u32(s.q + c * kChunkBytes), &p.tm_q, smem_u32(&s.bar_q_full), c * 64, h,
-                          o0 + qt * kBlock);
+            tma_load_4d(smem_u32(s.q), &p.tm_q, smem_u32(&s.bar_q_full), 0, o0 + qt * kBlock, h, 0);
             ++q_uses;
           }
           // K runs one tile ahead of V within the item.
@@ -253,8 +251,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) hstu_fwd_kernel(const __grid_c
               const uint32_t bar = smem_u32(&s.bar_k_full[st]);
               mbar_expect_tx(bar, kTile);
               const int row = o0 + (it_slot.tile[t] & 0xff) * kBlock;
-              for (int c = 0; c < Smem::kChunks; ++c)
-                tma_load_3d(smem_u32(s.k[st] + c * kChunkBytes), &p.tm_k, bar, c * 64, h, row);
+              tma_load_4d(smem_u32(s.k[st]), &p.tm_k, bar, 0, row, h, 0);
               k_last[st] = use;
             }
             if (t >= 1) {
@@ -266,8 +263,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) hstu_fwd_kernel(const __grid_c
               const uint32_t bar = smem_u32(&s.bar_v_full[st]);
               mbar_expect_tx(bar, kTile);
               const int row = o0 + (it_slot.tile[t - 1] & 0xff) * kBlock;
-              for (int c = 0; c < Smem::kChunks; ++c)
-                tma_load_3d(smem_u32(s.v[st] + c * kChunkBytes), &p.tm_v, bar, c * 64, h, row);
+              tma_load_4d(smem_u32(s.v[st]), &p.tm_v, bar, 0, row, h, 0);
               v_last[st] = use;
             }
           }
