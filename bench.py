@@ -43,9 +43,13 @@ NCU_TRAFFIC = {"bwd": 135056384 + 68607232, "sources_sha": "d2232c0f380d65b2"}
 
 
 def kernel_sources_sha() -> str:
+    """Hash of the sources that make up the device code (host-only .cpp files
+    are left out); recorded ncu traffic is only reported while it matches."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "jagged_hstu_attention_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
+        if name.endswith(".cpp"):
+            continue
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())
@@ -122,14 +126,14 @@ class ClockSampler:
 class Leg:
     """One jagged batch resident on the GPU with preallocated outputs."""
 
-    def __init__(self, cfg, seed, nfunc, device, shared=None):
+    def __init__(self, cfg, seed, nfunc, device, shared=None, lens=None, max_seqlen=None):
         import torch
         from jagged_hstu_attention_gb300 import binding as hb
         from jagged_hstu_attention_gb300 import workloads as wl
         self.hb = hb
         if shared is None:
             gen_dev = "cuda" if cfg.name.startswith("dlrm") else "cpu"
-            b = wl.make_batch(cfg, seed, device=gen_dev, nfunc=nfunc)
+            b = wl.make_batch(cfg, seed, device=gen_dev, nfunc=nfunc, lens=lens)
             self.lens, self.offsets, self.func = b.lens, b.offsets, b.func
             self.q, self.k, self.v, self.do = (t.to(device) for t in (b.q, b.k, b.v, b.do))
         else:  # same activations, another func width
@@ -138,7 +142,7 @@ class Leg:
             self.q, self.k, self.v, self.do = shared.q, shared.k, shared.v, shared.do
         self.cfg, self.nfunc = cfg, nfunc
         self.T = int(self.offsets[-1])
-        self.N = int(self.lens.max())
+        self.N = int(self.lens.max()) if max_seqlen is None else int(max_seqlen)
         self.alpha = 1.0 / math.sqrt(cfg.dim)
         self.d_off = torch.tensor(self.offsets, dtype=torch.int32, device=device)
         self.d_func = torch.tensor(self.func, dtype=torch.int32, device=device)
@@ -300,6 +304,40 @@ def cpu_cores():
     return os.cpu_count()
 
 
+# ---------------------------------------------------------------- ranks
+def rank_sequences(cfg, seed, world, rank):
+    """This rank's share of the job's batch: (indices into the job's batch,
+    their lengths, the batch-wide max_seqlen).
+
+    The job's batch is ``cfg.batch * world`` sequences drawn from ``seed``;
+    hstu_attn_shard_sequences splits it by whole sequences (cost L_b^2), so the
+    work per rank stays fixed as the number of ranks grows (weak scaling). N is
+    the batch-wide maximum on every rank: the op's 1/N scale must not depend
+    on the split."""
+    import dataclasses
+    from jagged_hstu_attention_gb300 import binding as hb
+    from jagged_hstu_attention_gb300 import workloads as wl
+    lens = wl.lengths(dataclasses.replace(cfg, batch=cfg.batch * world), seed)
+    if world == 1:
+        return np.arange(len(lens)), lens, int(lens.max())
+    owner, _ = hb.shard_sequences(lens * lens, world)
+    idx = np.nonzero(owner.numpy() == rank)[0]
+    return idx, lens[idx], int(lens.max())
+
+
+def reduce_over_ranks(ms, work, device, world):
+    """(max over ranks of the step time, sum over ranks of the work)."""
+    if world == 1:
+        return ms, work
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    w = torch.tensor([work], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(w, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(w.item())
+
+
 # ---------------------------------------------------------------- main
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
@@ -317,7 +355,7 @@ def run_targets(args, cfg, device, world, rank):
     from jagged_hstu_attention_gb300 import binding as hb
     from jagged_hstu_attention_gb300 import workloads as wl
     seed = args.seed + rank
-    lens = wl.lengths(cfg, seed)
+    _, lens, N = rank_sequences(cfg, args.seed, world, rank)
     off = wl.offsets_from_lengths(lens)
     T, B, H, D = int(off[-1]), len(lens), cfg.heads, cfg.dim
     gen = torch.Generator(device=device)
@@ -328,7 +366,6 @@ def run_targets(args, cfg, device, world, rank):
     do_c = wl.randn_bf16((B, H, D), gen, device)
     d_off = torch.tensor(off, dtype=torch.int32, device=device)
     fc = torch.tensor(wl.build_func_candidates(lens, 1), dtype=torch.int32, device=device)
-    N = int(lens.max())
     alpha = 1.0 / math.sqrt(D)
     shape = hb.make_shape(B, T, H, D, 1, N, alpha)
     ws = hb.alloc_workspace(shape, hb.WS_TARGETS, device)
@@ -360,28 +397,27 @@ def run_targets(args, cfg, device, world, rank):
     clocks = sampler.stop()
     fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in recs)
     bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in recs)
-    ms = fwd_ms + bwd_ms
-    ms_t = torch.tensor([ms], device=device)
-    if world > 1:
-        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
-        ms = float(ms_t.item())
-    if rank != 0:
-        return
+    ms_local = fwd_ms + bwd_ms
     row = H * D * 2
     bytes_fwd = 2 * T * row + 2 * B * row   # read K, V, q_c; write o_c
     bytes_bwd = 4 * T * row + 3 * B * row   # read K, V, q_c, dO_c; write dK, dV, dq_c
+    ms, job_bytes = reduce_over_ranks(ms_local, float(bytes_fwd + bytes_bwd), device, world)
+    if rank != 0:
+        return
     useful = float(T) * H * 14 * D          # every key is visible to its candidate
     peaks = load_peaks()
-    gbs = (bytes_fwd + bytes_bwd) / (ms * 1e-3) / 1e9
+    gbs = (bytes_fwd + bytes_bwd) / (ms_local * 1e-3) / 1e9
     line = {
         "metric": "HSTU targets-only fwd+bwd ms and achieved HBM GB/s (% of measured copy bandwidth)",
-        "mode": "targets_only", "value": gbs * world, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "mode": "targets_only", "value": job_bytes / (ms * 1e-3) / 1e9, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": cfg.name + ":targets_only", "batch": B, "total_tokens": T, "heads": H,
-                   "head_dim": D, "candidates_per_seq": 1, "l2": "flushed between steps"},
+        "config": {"workload": cfg.name + ":targets_only", "batch": B, "global_batch": cfg.batch * world,
+                   "total_tokens": T, "heads": H, "head_dim": D, "candidates_per_seq": 1,
+                   "parallelism": f"dp{world}" if world > 1 else "single", "l2": "flushed between steps"},
         "breakdown_ms": {"fwd": fwd_ms, "bwd": bwd_ms},
-        "useful_tflops": useful / (ms * 1e-3) / 1e12,
+        "useful_tflops": useful / (ms_local * 1e-3) / 1e12,
         "gpu_launches": 4 * args.steps,
         "roofline": {"kernel": "tgt_partial_kernel (fwd + bwd)", "bound": "hbm", "achieved": gbs,
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
@@ -459,10 +495,12 @@ def main():
             dist.destroy_process_group()
         return
 
-    # Each rank runs its own batch (seed + rank): independent sequences, no
-    # data-path collective; weak scaling.
+    # Each rank runs its share of a batch of cfg.batch * world sequences (whole
+    # sequences, split longest-first); no data-path collective; weak scaling.
+    # Activations are drawn from seed + rank.
     seed = args.seed + rank
-    leg_main = Leg(cfg, seed, cfg.nfunc, device)
+    _, lens, n_max = rank_sequences(cfg, args.seed, world, rank)
+    leg_main = Leg(cfg, seed, cfg.nfunc, device, lens=lens, max_seqlen=n_max)
     legs = [leg_main]
     if cfg.mask == "sla" and cfg.nfunc == 5:
         legs.append(Leg(cfg, seed, 3, device, shared=leg_main))
@@ -483,16 +521,14 @@ def main():
 
     r = res[0]
     ms_step = statistics.mean(r["step"])
-    ms_tensor = torch.tensor([ms_step], device=device)
-    if world > 1:
-        dist.all_reduce(ms_tensor, op=dist.ReduceOp.MAX)
-    ms_max = float(ms_tensor.item())
     f_fwd, f_bwd = leg_main.flops()
     useful = f_fwd + f_bwd
-    value = useful * world / (ms_max * 1e-3) / 1e12
+    ms_max, job_useful = reduce_over_ranks(ms_step, useful, device, world)
+    value = job_useful / (ms_max * 1e-3) / 1e12
 
     e2e_ms, h2d, d2h = e2e_leg(leg_main, max(3, args.steps // 2), 2)
-    e2e_val = useful * world / (e2e_ms * 1e-3) / 1e12
+    e2e_max, _ = reduce_over_ranks(e2e_ms, useful, device, world)
+    e2e_val = job_useful / (e2e_max * 1e-3) / 1e12
 
     if rank != 0:
         if world > 1:
@@ -508,10 +544,10 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": cfg.name, "batch": cfg.batch, "seq_len": cfg.len_hi if cfg.len_lo == cfg.len_hi
+        "config": {"workload": cfg.name, "batch": len(lens), "global_batch": cfg.batch * world, "seq_len": cfg.len_hi if cfg.len_lo == cfg.len_hi
                    else f"U[{cfg.len_lo},{cfg.len_hi}]", "heads": cfg.heads, "head_dim": cfg.dim,
                    "nfunc": cfg.nfunc, "mask": cfg.mask, "total_tokens": leg_main.T,
-                   "parallelism": f"replicas{world}" if world > 1 else "single", "l2": "flushed between steps"},
+                   "parallelism": f"dp{world}" if world > 1 else "single", "l2": "flushed between steps"},
         "pct_of_bf16_peak": 100.0 * value / world / peaks["bf16_tflops"],
         "breakdown_ms": {k: statistics.mean(r[k]) for k in ("plan", "fwd", "bwd")},
         "useful_gflop_per_step": useful / 1e9,
@@ -521,7 +557,7 @@ def main():
                      "frac": achieved / peaks["bf16_tflops"], "traffic": traffic,
                      "peak_source": peaks["source"] + " burst bf16"},
         "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_ms},
+                "ms_per_step": e2e_max},
         "clocks": clocks,
         "wall_s_timed_region": wall,
     }

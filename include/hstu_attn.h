@@ -180,6 +180,25 @@ HSTU_API hstu_status_t hstu_attn_get_device_status(const void* ws, void* stream)
 /* Static description of a status code. */
 HSTU_API const char* hstu_status_string(hstu_status_t status);
 
+/* Splits a batch over `world` data-parallel ranks, by whole sequences. Every
+ * (sequence, head) unit of the op is independent in the forward and the
+ * backward pass, so the ranks need no exchange; each runs the op on its own
+ * sequences with the same max_seqlen N (N is the 1/N scale, so it must be the
+ * one of the whole batch for results to match an unsplit run). The pages give
+ * no partitioning; this is the greedy longest-processing-time rule: sequences
+ * in descending cost (equal costs: lower index first) each go to the rank with
+ * the smallest load so far (equal loads: lower rank).
+ *   cost:      HOST int64 (batch), >= 0, the caller's work estimate of each
+ *              sequence (its visible pairs, or L_b^2 for causal masks).
+ *   owner:     HOST int32 (batch), written: the rank of each sequence.
+ *   rank_load: HOST int64 (world), nullable, written: each rank's total cost.
+ * Deterministic, so every rank computes the same split from the same costs.
+ * Host-only: touches no GPU. Returns HSTU_ERR_INVALID_ARG (writing nothing)
+ * for batch < 0, world < 1, a null cost or owner with batch > 0, a negative
+ * cost, or costs whose sum overflows int64. */
+HSTU_API hstu_status_t hstu_attn_shard_sequences(const int64_t* cost, int32_t batch, int32_t world,
+                                                 int32_t* owner, int64_t* rank_load);
+
 #ifdef __cplusplus
 }
 #endif

@@ -30,6 +30,7 @@ EXPORTED = (
     "hstu_attn_nfunc_supported", "hstu_attn_workspace_size", "hstu_attn_plan", "hstu_attn_fwd",
     "hstu_attn_bwd", "hstu_attn_fwd_targets_only", "hstu_attn_bwd_targets_only",
     "hstu_attn_get_device_status", "hstu_status_string", "hstu_attn_fwd_noalloc",
+    "hstu_attn_shard_sequences",
 )
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
@@ -78,6 +79,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "hstu_attn_get_device_status": (ctypes.c_int, [vp, vp]),
         "hstu_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "hstu_attn_fwd_noalloc": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, sp, vp, vp]),
+        "hstu_attn_shard_sequences": (ctypes.c_int, [vp, i32, i32, vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -250,3 +252,18 @@ def fwd_noalloc(q, k, v, seq_offsets, func, max_seqlen: int, alpha: Optional[flo
                                         ctypes.byref(shape), _ptr(row_counts), _stream(stream)),
            "hstu_attn_fwd_noalloc")
     return o
+
+
+def shard_sequences(cost, world: int) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Splits a batch over ``world`` data-parallel ranks by whole sequences
+    (hstu_attn_shard_sequences, host-only). ``cost`` is one non-negative work
+    estimate per sequence. Returns (owner, rank_load): the rank of each
+    sequence (int32) and each rank's total cost (int64), as CPU tensors."""
+    c = torch.as_tensor(cost, dtype=torch.int64).contiguous()
+    if c.dim() != 1 or c.is_cuda:
+        raise ValueError("cost must be a 1-D host array")
+    owner = torch.empty(c.numel(), dtype=torch.int32)
+    load_ = torch.empty(max(world, 0), dtype=torch.int64)
+    _check(load().hstu_attn_shard_sequences(_ptr(c), c.numel(), world, _ptr(owner), _ptr(load_)),
+           "hstu_attn_shard_sequences")
+    return owner, load_

@@ -182,8 +182,10 @@ class Batch:
 
 
 def make_batch(cfg: Config, seed: int = 0, device="cpu", nfunc: Optional[int] = None,
-               with_grad_out: bool = True) -> Batch:
-    lens = lengths(cfg, seed)
+               with_grad_out: bool = True, lens: Optional[np.ndarray] = None) -> Batch:
+    """A jagged batch of the workload; ``lens`` (optional) replaces the drawn
+    lengths, e.g. with one rank's share of a larger batch."""
+    lens = lengths(cfg, seed) if lens is None else np.asarray(lens, dtype=np.int64)
     off = offsets_from_lengths(lens)
     func = build_func(cfg, lens, nfunc)
     T = int(off[-1])
