@@ -115,8 +115,7 @@ bool tensor_ok(const void* p) { return p && aligned(p, 16); }
 hstu_status_t run_plan(const int32_t* seq_offsets, const int32_t* func, const hstu_attn_shape_t* s,
                        int32_t* row_counts, void* ws, cudaStream_t stream) {
   const hstu::FullLayout l = hstu::full_layout(s->batch, s->max_seqlen);
-  return from_cuda(hstu::launch_plan(plan_params(seq_offsets, func, s, row_counts, ws, l),
-                                     l.zero_bytes, stream));
+  return from_cuda(hstu::launch_plan(plan_params(seq_offsets, func, s, row_counts, ws, l), stream));
 }
 
 }  // namespace

@@ -22,7 +22,6 @@ constexpr int kMaxIntervals = 3;   // nfunc <= 5
 constexpr int kHdrErr = 0;     // error bits (kErrInput | kErrTimeout)
 constexpr int kHdrNFwd = 1;    // entries of the forward work list
 constexpr int kHdrNBwd = 2;    // entries of the backward work list
-constexpr int kHdrTicket = 3;  // plan blocks finished (the last one builds the lists)
 // Dynamic work distribution of the persistent attention kernels: the next
 // work index to hand out and the CTAs that have finished. The last CTA of a
 // launch puts both back to zero, so that a reused plan starts clean.
@@ -48,11 +47,11 @@ constexpr int kRoleDkdv = 1 << 30;
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Layout of the HSTU_WS_FULL workspace. Only the header is cleared at the
-// start of a plan; every other region is fully written before it is read.
+// Layout of the HSTU_WS_FULL workspace. The plan writes every header word
+// the kernels read; every other region is fully written before it is read.
 struct FullLayout {
   int nt = 0;  // tiles per sequence at max_seqlen
-  size_t header = 0, zero_bytes = 0, fwd_list = 0, bwd_list = 0, seq_order = 0, seq_start = 0,
+  size_t header = 0, header_bytes = 0, fwd_list = 0, bwd_list = 0, seq_order = 0, seq_start = 0,
          ivmask = 0, cls = 0, total = 0;
 };
 inline FullLayout full_layout(int batch, int max_seqlen) {
@@ -60,8 +59,8 @@ inline FullLayout full_layout(int batch, int max_seqlen) {
   l.nt = (max_seqlen + kBlock - 1) / kBlock;
   const size_t items = static_cast<size_t>(batch) * l.nt;
   l.header = 0;
-  l.zero_bytes = kHdrWords * 4;
-  l.fwd_list = l.zero_bytes;
+  l.header_bytes = kHdrWords * 4;
+  l.fwd_list = l.header_bytes;
   l.bwd_list = l.fwd_list + align_up(items * 4, 256);
   l.seq_order = l.bwd_list + align_up(2 * items * 4, 256);
   l.seq_start = l.seq_order + align_up(static_cast<size_t>(batch) * 4, 256);

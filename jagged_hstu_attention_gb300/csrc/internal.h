@@ -7,7 +7,7 @@
 
 namespace hstu {
 
-cudaError_t launch_plan(const PlanParams& p, size_t zero_bytes, cudaStream_t stream);
+cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream);
 // grid_items: upper bound on the number of work items (CTAs = items * heads).
 cudaError_t launch_fwd(const AttnParams& p, int nint, int grid_items, cudaStream_t stream);
 cudaError_t launch_bwd(const AttnParams& p, int nint, int grid_items, cudaStream_t stream);

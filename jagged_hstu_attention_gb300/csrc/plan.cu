@@ -2,6 +2,9 @@
 // classifies every (q-tile, kv-tile) pair of a sequence, the per-row visible
 // counts, and the longest-first work lists of the forward and backward
 // kernels, all in one launch. Nothing here needs a host synchronisation.
+// The work lists depend on seq_offsets alone, so block 0 validates the
+// offsets and builds them while the other blocks classify tiles; block 0 also
+// writes every header word the kernels read, so no memset precedes the plan.
 //
 // The pages' kernels reduce per-tile min/max bounds of every interval
 // (including the empty padded ones) and then test every interval in every KV
@@ -20,22 +23,15 @@ namespace hstu {
 
 // Classifies the kv tiles seen by one (sequence b, q tile qt) block and
 // writes that tile's row counts, class row and active-interval mask. Blocks
-// past a sequence's last q tile (or of an invalid sequence) do nothing.
+// past a sequence's last q tile (or of an invalid sequence, which block 0
+// reports) do nothing.
 template <int NINT>
-__device__ void classify_tile(const PlanParams& p) {
-  const int b = blockIdx.x, qt = blockIdx.y;
+__device__ void classify_tile(const PlanParams& p, int b, int qt) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int o0 = p.seq_offsets[b];
   const int o1 = p.seq_offsets[b + 1];
   const int L = o1 - o0;
-  if (b == 0 && qt == 0 && tid == 0) {
-    if (p.seq_offsets[0] != 0 || static_cast<int64_t>(p.seq_offsets[p.batch]) != p.total)
-      atomicOr(p.header + kHdrErr, kErrInput);
-  }
-  if (L < 0 || L > p.max_seqlen || o0 < 0 || static_cast<int64_t>(o1) > p.total) {
-    if (qt == 0 && tid == 0) atomicOr(p.header + kHdrErr, kErrInput);
-    return;
-  }
+  if (L < 0 || L > p.max_seqlen || o0 < 0 || static_cast<int64_t>(o1) > p.total) return;
   const int ntiles = (L + kBlock - 1) / kBlock;
   if (qt >= ntiles) return;
 
@@ -147,11 +143,41 @@ __device__ void block_exclusive_scan(int* cnt, int n) {
 // of equal length may come out in any order: every output element is
 // computed by exactly one CTA with a fixed internal order, so the order only
 // changes scheduling, never results.
+//
+// Before that it checks seq_offsets (first 0, last = total, every length in
+// [0, max_seqlen]) and writes the header: the error word (kErrInput, with
+// empty lists, if the check fails), the list lengths, the uniform flag and
+// the zeroed work counters.
 __device__ void build_work_lists(const PlanParams& p) {
   __shared__ int hist[kMaxTiles + 1];
   __shared__ int n_items;
+  __shared__ int bad;
   const int tid = threadIdx.x;
-  if (p.header[kHdrErr] != 0) return;
+  if (tid == 0)
+    bad = (p.seq_offsets[0] != 0 || static_cast<int64_t>(p.seq_offsets[p.batch]) != p.total) ? 1 : 0;
+  __syncthreads();
+  for (int b = tid; b < p.batch; b += blockDim.x) {
+    const int o0 = p.seq_offsets[b], o1 = p.seq_offsets[b + 1];
+    const int64_t L = static_cast<int64_t>(o1) - o0;
+    if (o0 < 0 || static_cast<int64_t>(o1) > p.total || L < 0 || L > p.max_seqlen)
+      bad = 1;  // every writer stores the same value
+  }
+  __syncthreads();
+  if (tid == 0) {
+    p.header[kHdrFwdNext] = 0;
+    p.header[kHdrFwdDone] = 0;
+    p.header[kHdrBwdNext] = 0;
+    p.header[kHdrBwdDone] = 0;
+  }
+  if (bad) {
+    if (tid == 0) {
+      p.header[kHdrErr] = kErrInput;
+      p.header[kHdrNFwd] = 0;
+      p.header[kHdrNBwd] = 0;
+      p.header[kHdrUniform] = 0;
+    }
+    return;
+  }
   const int nt = p.nt;
   auto tiles_of = [&](int b) {
     int L = p.seq_offsets[b + 1] - p.seq_offsets[b];
@@ -184,6 +210,7 @@ __device__ void build_work_lists(const PlanParams& p) {
   if (tid == 0) n_items = p.seq_start[p.batch - 1] + tiles_of(p.seq_order[p.batch - 1]);
   __syncthreads();
   if (tid == 0) {
+    p.header[kHdrErr] = 0;
     p.header[kHdrNFwd] = n_items;
     p.header[kHdrNBwd] = 2 * n_items;
     // seq_order is sorted by tile count: equal ends mean equal counts.
@@ -191,28 +218,22 @@ __device__ void build_work_lists(const PlanParams& p) {
   }
 }
 
-// One launch: every block classifies one (sequence, q tile); the last block
-// to finish (ticket counter in the header) builds the work lists.
+// One launch of 1 + batch * nt blocks: block 0 checks the offsets and builds
+// the work lists; block 1 + b * nt + qt classifies (sequence b, q tile qt).
 template <int NINT>
 __global__ void __launch_bounds__(128) plan_kernel(const PlanParams p) {
-  classify_tile<NINT>(p);
-  __shared__ int is_last;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    const int done = atomicAdd(p.header + kHdrTicket, 1);
-    is_last = done == static_cast<int>(gridDim.x * gridDim.y) - 1;
+  if (blockIdx.x == 0) {
+    build_work_lists(p);
+    return;
   }
-  __syncthreads();
-  if (!is_last) return;
-  __threadfence();
-  build_work_lists(p);
+  const int idx = static_cast<int>(blockIdx.x) - 1;
+  classify_tile<NINT>(p, idx / p.nt, idx % p.nt);
 }
 
-cudaError_t launch_plan(const PlanParams& p, size_t zero_bytes, cudaStream_t stream) {
-  cudaError_t e = cudaMemsetAsync(p.header, 0, zero_bytes, stream);
-  if (e != cudaSuccess) return e;
-  const dim3 grid(p.batch, p.nt);
+cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream) {
+  const long long blocks = 1 + static_cast<long long>(p.batch) * p.nt;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  const unsigned grid = static_cast<unsigned>(blocks);
   const int nint = (p.nfunc + 1) / 2;
   if (nint == 1) plan_kernel<1><<<grid, 128, 0, stream>>>(p);
   else if (nint == 2) plan_kernel<2><<<grid, 128, 0, stream>>>(p);
