@@ -73,7 +73,7 @@ typedef struct {
   int64_t total;      /* T = seq_offsets[B], rows of k and v (and of q, o) */
   int32_t num_heads;  /* H >= 1 */
   int32_t head_dim;   /* D = D_qk = D_v, one of 32, 64, 128 */
-  int32_t nfunc;      /* rows of func: 1, 3 or 5 */
+  int32_t nfunc;      /* rows of func: odd, 1 to 9 */
   int32_t max_seqlen; /* N: >= every L_b, <= 32768; also the 1/N scale */
   float alpha;        /* scale on q.k, usually 1/sqrt(head_dim) */
 } hstu_attn_shape_t;
@@ -89,7 +89,7 @@ typedef struct {
  * shape; skip rebuilding it. The caller guarantees that none changed. */
 #define HSTU_FLAG_REUSE_PLAN 1
 
-/* 1 if this build has kernels for that nfunc (1, 3, 5), else 0. The pages'
+/* 1 if this build has kernels for that nfunc (1, 3, 5, 7, 9), else 0. The pages'
  * wheel bakes NFUNC in at compile time (TorchEasyRec PR #670 review thread on
  * exposing it at runtime); here it is a runtime argument dispatched to
  * compiled variants, and this query exposes which ones exist. */

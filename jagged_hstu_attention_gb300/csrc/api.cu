@@ -123,7 +123,7 @@ hstu_status_t run_plan(const int32_t* seq_offsets, const int32_t* func, const hs
 extern "C" {
 
 int hstu_attn_nfunc_supported(int32_t nfunc) {
-  return (nfunc == 1 || nfunc == 3 || nfunc == 5) ? 1 : 0;
+  return (nfunc >= 1 && nfunc <= 2 * hstu::kMaxIntervals - 1 && nfunc % 2 == 1) ? 1 : 0;
 }
 
 size_t hstu_attn_workspace_size(const hstu_attn_shape_t* shape, int32_t mode) {

@@ -593,15 +593,20 @@ static cudaError_t launch_bwd_t(const AttnParams& p, int grid_items, cudaStream_
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd(const AttnParams& p, int nint, int grid_items, cudaStream_t stream) {
-  if (p.dim > 64) {
-    if (nint == 1) return launch_bwd_t<128, 1>(p, grid_items, stream);
-    if (nint == 2) return launch_bwd_t<128, 2>(p, grid_items, stream);
-    return launch_bwd_t<128, 3>(p, grid_items, stream);
+template <int DP>
+static cudaError_t launch_bwd_dp(const AttnParams& p, int nint, int grid_items, cudaStream_t stream) {
+  switch (nint) {
+    case 1: return launch_bwd_t<DP, 1>(p, grid_items, stream);
+    case 2: return launch_bwd_t<DP, 2>(p, grid_items, stream);
+    case 3: return launch_bwd_t<DP, 3>(p, grid_items, stream);
+    case 4: return launch_bwd_t<DP, 4>(p, grid_items, stream);
+    default: return launch_bwd_t<DP, 5>(p, grid_items, stream);
   }
-  if (nint == 1) return launch_bwd_t<64, 1>(p, grid_items, stream);
-  if (nint == 2) return launch_bwd_t<64, 2>(p, grid_items, stream);
-  return launch_bwd_t<64, 3>(p, grid_items, stream);
+}
+
+cudaError_t launch_bwd(const AttnParams& p, int nint, int grid_items, cudaStream_t stream) {
+  return p.dim > 64 ? launch_bwd_dp<128>(p, nint, grid_items, stream)
+                    : launch_bwd_dp<64>(p, nint, grid_items, stream);
 }
 
 }  // namespace hstu

@@ -468,15 +468,20 @@ static cudaError_t launch_fwd_t(const AttnParams& p, int grid_items, cudaStream_
   return cudaGetLastError();
 }
 
-cudaError_t launch_fwd(const AttnParams& p, int nint, int grid_items, cudaStream_t stream) {
-  if (p.dim > 64) {
-    if (nint == 1) return launch_fwd_t<128, 1>(p, grid_items, stream);
-    if (nint == 2) return launch_fwd_t<128, 2>(p, grid_items, stream);
-    return launch_fwd_t<128, 3>(p, grid_items, stream);
+template <int DP>
+static cudaError_t launch_fwd_dp(const AttnParams& p, int nint, int grid_items, cudaStream_t stream) {
+  switch (nint) {
+    case 1: return launch_fwd_t<DP, 1>(p, grid_items, stream);
+    case 2: return launch_fwd_t<DP, 2>(p, grid_items, stream);
+    case 3: return launch_fwd_t<DP, 3>(p, grid_items, stream);
+    case 4: return launch_fwd_t<DP, 4>(p, grid_items, stream);
+    default: return launch_fwd_t<DP, 5>(p, grid_items, stream);
   }
-  if (nint == 1) return launch_fwd_t<64, 1>(p, grid_items, stream);
-  if (nint == 2) return launch_fwd_t<64, 2>(p, grid_items, stream);
-  return launch_fwd_t<64, 3>(p, grid_items, stream);
+}
+
+cudaError_t launch_fwd(const AttnParams& p, int nint, int grid_items, cudaStream_t stream) {
+  return p.dim > 64 ? launch_fwd_dp<128>(p, nint, grid_items, stream)
+                    : launch_fwd_dp<64>(p, nint, grid_items, stream);
 }
 
 }  // namespace hstu

@@ -16,7 +16,7 @@ namespace hstu {
 constexpr int kBlock = 128;        // q-tile rows = kv-tile rows
 constexpr int kMaxSeqlen = 32768;  // => at most 256 tiles per sequence
 constexpr int kMaxTiles = kMaxSeqlen / kBlock;
-constexpr int kMaxIntervals = 3;   // nfunc <= 5
+constexpr int kMaxIntervals = 5;   // nfunc <= 9
 
 // Workspace header (int32 words).
 constexpr int kHdrErr = 0;     // error bits (kErrInput | kErrTimeout)

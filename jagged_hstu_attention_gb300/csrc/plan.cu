@@ -235,9 +235,13 @@ cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream) {
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   const unsigned grid = static_cast<unsigned>(blocks);
   const int nint = (p.nfunc + 1) / 2;
-  if (nint == 1) plan_kernel<1><<<grid, 128, 0, stream>>>(p);
-  else if (nint == 2) plan_kernel<2><<<grid, 128, 0, stream>>>(p);
-  else plan_kernel<3><<<grid, 128, 0, stream>>>(p);
+  switch (nint) {
+    case 1: plan_kernel<1><<<grid, 128, 0, stream>>>(p); break;
+    case 2: plan_kernel<2><<<grid, 128, 0, stream>>>(p); break;
+    case 3: plan_kernel<3><<<grid, 128, 0, stream>>>(p); break;
+    case 4: plan_kernel<4><<<grid, 128, 0, stream>>>(p); break;
+    default: plan_kernel<5><<<grid, 128, 0, stream>>>(p); break;
+  }
   return cudaGetLastError();
 }
 

@@ -173,9 +173,13 @@ template <int D, bool BWD>
 static cudaError_t launch_tgt_t(const TgtParams& p, cudaStream_t stream) {
   const dim3 grid(static_cast<unsigned>(p.batch) * p.nc, p.heads);
   const int nint = (p.nfunc + 1) / 2;
-  if (nint == 1) tgt_partial_kernel<D, 1, BWD><<<grid, kTgtThreads, 0, stream>>>(p);
-  else if (nint == 2) tgt_partial_kernel<D, 2, BWD><<<grid, kTgtThreads, 0, stream>>>(p);
-  else tgt_partial_kernel<D, 3, BWD><<<grid, kTgtThreads, 0, stream>>>(p);
+  switch (nint) {
+    case 1: tgt_partial_kernel<D, 1, BWD><<<grid, kTgtThreads, 0, stream>>>(p); break;
+    case 2: tgt_partial_kernel<D, 2, BWD><<<grid, kTgtThreads, 0, stream>>>(p); break;
+    case 3: tgt_partial_kernel<D, 3, BWD><<<grid, kTgtThreads, 0, stream>>>(p); break;
+    case 4: tgt_partial_kernel<D, 4, BWD><<<grid, kTgtThreads, 0, stream>>>(p); break;
+    default: tgt_partial_kernel<D, 5, BWD><<<grid, kTgtThreads, 0, stream>>>(p); break;
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   tgt_fold_kernel<D><<<p.batch * p.heads, 128, 0, stream>>>(p, BWD ? p.dq_c : p.o_c);

@@ -47,7 +47,9 @@ def _shape(**kw):
 
 
 def test_nfunc_supported(lib):
-    assert [hb.nfunc_supported(n) for n in range(7)] == [False, True, False, True, False, True, False]
+    assert [hb.nfunc_supported(n) for n in range(12)] == [False, True, False, True, False, True, False,
+                                                          True, False, True, False, False]
+    assert not hb.nfunc_supported(-1)
 
 
 def test_workspace_size(lib):

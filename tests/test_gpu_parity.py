@@ -44,7 +44,7 @@ def test_ragged_tails_all_masks(D, mask):
     compare(gb.run(), gb.oracle())
 
 
-@pytest.mark.parametrize("nfunc", [1, 3, 5])
+@pytest.mark.parametrize("nfunc", [1, 3, 5, 7, 9])
 def test_random_intervals(nfunc):
     """Arbitrary (also negative, out-of-range, reversed) func values."""
     lens = np.array([200, 77, 384, 5])
@@ -67,11 +67,12 @@ def test_all_intervals_empty_gives_zeros():
     assert not out["counts"].any()
 
 
-def test_sla_padding_is_bitwise_inert():
+@pytest.mark.parametrize("nfunc_padded", [5, 9])
+def test_sla_padding_is_bitwise_inert(nfunc_padded):
     cfg = wl.CONFIGS["sla_b32_s1024"]
-    g5 = GpuBatch.from_config(cfg, 0, nfunc=5)
-    g3 = GpuBatch(g5.lens, g5.func[:3], g5.q, g5.k, g5.v, g5.do)
-    a, b = g5.run(), g3.run()
+    gp = GpuBatch.from_config(cfg, 0, nfunc=nfunc_padded)
+    g3 = GpuBatch(gp.lens, gp.func[:3], gp.q, gp.k, gp.v, gp.do)
+    a, b = gp.run(), g3.run()
     for n in ("o", "dq", "dk", "dv", "counts"):
         assert torch.equal(a[n], b[n]), n
 
@@ -144,7 +145,7 @@ def test_targets_only_equals_full_candidate_row():
     check_grad(np64(dv), rdv, "dv")
 
 
-@pytest.mark.parametrize("nfunc", [3, 5])
+@pytest.mark.parametrize("nfunc", [3, 5, 7, 9])
 def test_targets_only_interval_masks(nfunc):
     lens = np.array([700, 33, 260])
     T = int(lens.sum())

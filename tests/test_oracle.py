@@ -85,7 +85,7 @@ def _textbook_causal(q, k, v, off, N, alpha):
     return out
 
 
-@pytest.mark.parametrize("nfunc", [1, 3, 5])
+@pytest.mark.parametrize("nfunc", [1, 3, 5, 7, 9])
 def test_causal_special_case_matches_textbook(nfunc):
     lens, off, q, k, v, do = _small_batch(3, [37, 5, 64, 20], H=2, D=16)
     cfg = wl.Config("c", 4, 0, 0, 2, 16, "causal", nfunc)
