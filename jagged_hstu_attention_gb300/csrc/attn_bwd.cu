@@ -24,11 +24,11 @@
 // workspace and no reduce-add traffic.
 //
 // Warps: 0-7 epilogue, 8 producer (tile lists into two item slots, TMA
-// loads; streamed tiles travel as 64-row halves through a 4-slot ring, each
+// loads; streamed tiles travel as 64-row halves through a 5-slot ring, each
 // slot freed right after its half's accumulating MMAs), 9 TMEM owner and MMA
-// issuer. The next item's lists and resident
-// tiles are fetched while the current item finishes; its first accumulating
-// MMA waits until the epilogue has read out the previous item's accumulators.
+// issuer. The next item's lists and resident tiles are fetched while the
+// current item finishes; its first accumulating MMA waits until the epilogue
+// has read out the previous item's accumulators.
 //
 // TMEM (512 columns, the same for both roles): acc0 [0,128) (dV or dQ),
 // acc1 [128,256) (dK), three S slots at 256, 320 and 384, one dP slot at
