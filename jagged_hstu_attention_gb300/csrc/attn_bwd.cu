@@ -237,7 +237,8 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
       tma_prefetch_map(&p.tm_v64);
       tma_prefetch_map(&p.tm_do64);
     }
-    int str_last[Smem::kSlots] = {-1, -1, -1, -1};
+    int str_last[Smem::kSlots];  // last use of each ring slot, -1 if never used
+    for (int st = 0; st < Smem::kSlots; ++st) str_last[st] = -1;
     int res_uses = 0;  // items with at least one tile (one resident load each)
     int gs = 0;        // streamed tiles over all items
     bool ok = true;

@@ -188,6 +188,25 @@ def test_dlrm_targets_only_full_size():
     check_grad(np64(dv.index_select(0, ridx)), rdv, "dv")
 
 
+@pytest.mark.parametrize("lens", [[5], [130], [5, 130, 64]])
+def test_small_batches_never_reach_a_wait_limit(lens):
+    """A CTA that uses only some of its ring slots must not wait on the
+    others at exit: each launch on a tiny batch ends far inside the 2 s limit
+    of the in-kernel waits."""
+    lens = np.array(lens)
+    q, k, v, do = _gen(lens, 1, 64, seed=5)
+    gb = GpuBatch(lens, wl.build_func(wl.Config("c", len(lens), 0, 0, 1, 64, "causal", 1), lens, 1),
+                  q, k, v, do)
+    gb.run()  # warm-up: library load, first launches
+    e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    e[0].record()
+    out = gb.run()
+    e[1].record()
+    torch.cuda.synchronize()
+    assert e[0].elapsed_time(e[1]) < 200.0  # milliseconds
+    compare(out, gb.oracle())
+
+
 def test_backward_is_bitwise_repeatable():
     gb = GpuBatch.from_config(wl.CONFIGS["onerank_b64"], 1)
     a = gb.run()
