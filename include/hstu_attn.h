@@ -37,9 +37,13 @@
  *   - Host-checkable errors (null pointers, unsupported nfunc or head_dim,
  *     misalignment, workspace too small, bad sizes) return a status before
  *     anything is enqueued. Errors only visible on the device (offsets that
- *     are not monotone, a length above max_seqlen, a wrong last offset) set
- *     the workspace error word; every later kernel that reads that workspace
- *     then writes nothing. Read it with hstu_attn_get_device_status.
+ *     are not monotone, a length above max_seqlen, a wrong first or last
+ *     offset) set the workspace error word; every later kernel that reads
+ *     that workspace then writes nothing. Read it with
+ *     hstu_attn_get_device_status. (The full path checks the offsets in the
+ *     plan, before any output is written; the targets-only kernels check
+ *     them as they go, so dk/dv rows of other sequences may already be
+ *     written, but o_c and dq_c are not.)
  *   - No C++ exception crosses this boundary.
  */
 #ifndef HSTU_ATTN_H_

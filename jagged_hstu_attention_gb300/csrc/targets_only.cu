@@ -73,6 +73,9 @@ __global__ void __launch_bounds__(kTgtThreads) tgt_partial_kernel(const TgtParam
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int o0 = p.seq_offsets[b];
   const int L = p.seq_offsets[b + 1] - o0;
+  if (blockIdx.x == 0 && h == 0 && threadIdx.x == 0 &&
+      (p.seq_offsets[0] != 0 || static_cast<int64_t>(p.seq_offsets[p.batch]) != p.total))
+    atomicOr(p.header + kHdrErr, kErrInput);  // first offset not 0 or last not total
   if (L < 0 || L > p.max_seqlen || o0 < 0 || static_cast<int64_t>(o0) + L > p.total) {
     if (chunk == 0 && h == 0 && threadIdx.x == 0) atomicOr(p.header + kHdrErr, kErrInput);
     return;

@@ -207,6 +207,23 @@ def test_small_batches_never_reach_a_wait_limit(lens):
     compare(out, gb.oracle())
 
 
+def test_batch_of_empty_sequences():
+    """No rows at all: every entry point accepts it, writes nothing, and the
+    targets-only candidates (which see no key) get zeros."""
+    lens = np.array([0, 0, 0])
+    q, k, v, do = _gen(lens, 2, 64, seed=2)
+    gb = GpuBatch(lens, np.zeros((3, 0), np.int32), q, k, v, do, max_seqlen=16)
+    out = gb.run()
+    for n in ("o", "dq", "dk", "dv"):
+        assert out[n].numel() == 0, n
+    g = torch.Generator().manual_seed(4)
+    q_c = wl.randn_bf16((3, 2, 64), g).cuda()
+    do_c = wl.randn_bf16((3, 2, 64), g).cuda()
+    o_c, dq_c, dk, dv = _run_targets(gb, q_c, do_c, np.zeros((3, 3), np.int32))
+    assert not o_c.any() and not dq_c.any()
+    assert dk.numel() == 0 and dv.numel() == 0
+
+
 def test_backward_is_bitwise_repeatable():
     gb = GpuBatch.from_config(wl.CONFIGS["onerank_b64"], 1)
     a = gb.run()
@@ -215,18 +232,35 @@ def test_backward_is_bitwise_repeatable():
         assert torch.equal(a[n], b[n]), n
 
 
-def test_device_side_offset_error_sets_status_and_writes_nothing():
+@pytest.mark.parametrize("bad_offsets", [[0, 120, 150],   # L_0 = 120 > max_seqlen 100
+                                         [0, 100, 140],   # last offset is not total (150)
+                                         [0, 100, 90],    # decreasing
+                                         [10, 100, 150]])  # first offset is not 0
+def test_device_side_offset_error_sets_status_and_writes_nothing(bad_offsets):
     lens = np.array([100, 50])
     q, k, v, do = _gen(lens, 2, 64, seed=1)
     func = wl.build_func(wl.Config("c", 2, 0, 0, 2, 64, "causal", 1), lens, 1)
     gb = GpuBatch(lens, func, q, k, v, do)
-    bad = torch.tensor([0, 120, 150], dtype=torch.int32, device="cuda")  # L_0 = 120 > max_seqlen 100
+    bad = torch.tensor(bad_offsets, dtype=torch.int32, device="cuda")
     shape = hb.make_shape(2, 150, 2, 64, 1, 100, gb.alpha)
     ws = hb.alloc_workspace(shape)
     o = torch.full_like(gb.q, 7.0)
     hb.fwd(gb.q, gb.k, gb.v, bad, gb.d_func, 100, gb.alpha, ws=ws, out=o)
     assert hb.device_status(ws) == 5  # HSTU_ERR_DEVICE_INPUT
     assert torch.all(o == 7.0)
+    grads = tuple(torch.full_like(gb.q, 7.0) for _ in range(3))
+    hb.bwd(gb.do, gb.q, gb.k, gb.v, bad, gb.d_func, 100, gb.alpha, ws=ws, outs=grads)
+    assert hb.device_status(ws) == 5
+    assert all(torch.all(t == 7.0) for t in grads)
+    # targets-only reports the same offsets, and leaves o_c and dq_c alone
+    tshape = hb.make_shape(2, 150, 2, 64, 1, 100, gb.alpha)
+    tws = hb.alloc_workspace(tshape, hb.WS_TARGETS)
+    q_c = gb.q[:2].clone()
+    fc = torch.tensor([[100, 50]], dtype=torch.int32, device="cuda")
+    o_c = torch.full_like(q_c, 7.0)
+    hb.fwd_targets_only(q_c, gb.k, gb.v, bad, fc, 100, gb.alpha, ws=tws, out=o_c)
+    assert hb.device_status(tws) == 5
+    assert torch.all(o_c == 7.0)
     # the same workspace recovers with valid offsets
     o2 = hb.fwd(gb.q, gb.k, gb.v, gb.d_off, gb.d_func, 100, gb.alpha, ws=ws)
     assert hb.device_status(ws) == hb.HSTU_OK
