@@ -65,7 +65,7 @@ extern "C" {
 typedef enum {
   HSTU_OK = 0,
   HSTU_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misaligned pointer */
-  HSTU_ERR_UNSUPPORTED = 2,  /* nfunc or head_dim this build has no kernel for */
+  HSTU_ERR_UNSUPPORTED = 2,  /* nfunc or head_dim the library has no kernel for */
   HSTU_ERR_WORKSPACE = 3,    /* workspace null, too small or misaligned */
   HSTU_ERR_CUDA = 4,         /* a CUDA runtime call failed (launch, sync) */
   HSTU_ERR_DEVICE_INPUT = 5, /* device-side input check failed (offsets) */
@@ -93,7 +93,7 @@ typedef struct {
  * shape; skip rebuilding it. The caller guarantees that none changed. */
 #define HSTU_FLAG_REUSE_PLAN 1
 
-/* 1 if this build has kernels for that nfunc (1, 3, 5, 7, 9), else 0. The pages'
+/* 1 if the library has kernels for that nfunc (1, 3, 5, 7, 9), else 0. The pages'
  * wheel bakes NFUNC in at compile time (TorchEasyRec PR #670 review thread on
  * exposing it at runtime); here it is a runtime argument dispatched to
  * compiled variants, and this query exposes which ones exist. */

@@ -18,9 +18,9 @@ an interval whose end <= start is empty):
   page describes for ``build_sla_func_tensor``.
 * ``onerank`` -- TorchEasyRec PR #670 (OneRank, three intervals: prefix +
   candidate + task token). The page does not fix K (task tokens) or C
-  (candidates); this build takes C=8 groups of K+1=4 tokens at the end of each
-  sequence, and gives history rows a candidate and a task token too, so that
-  every row carries three non-empty intervals.
+  (candidates); these workloads take C=8 groups of K+1=4 tokens at the end
+  of each sequence and give history rows a candidate and a task token too, so
+  that every row carries three non-empty intervals.
 * ``causal`` -- MLCommons training PR #903 (DLRMv4 last layer): plain causal
   ``[0, i+1)`` with NFUNC=1; one candidate per sequence, its last row.
 """
