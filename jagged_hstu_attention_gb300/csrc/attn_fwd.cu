@@ -2,13 +2,16 @@
 // q tile qt, head h; longest sequences first) from a device-wide counter in
 // list order, and keeps every pipeline running across work items.
 //
-//   warp 12     producer. All 32 lanes build the next item's list of visited
-//               kv tiles (from the plan's tile classes) into one of two item
-//               slots; lane 0 then loads the item's Q tile and the K and V
-//               tiles of every visited kv tile by TMA into two rings of
-//               kStages (3 at D=128, 4 at D<=64). K frees after QK^T, V after
-//               PV, so the next item's Q and K arrive while the current item
-//               finishes.
+//   warp 12     producer of Q and K. All 32 lanes build the next item's list
+//               of visited kv tiles (from the plan's tile classes) into one of
+//               two item slots; lane 0 then loads the item's Q tile and the K
+//               tile of every visited kv tile by TMA into a ring of kStages
+//               (3 at D=128, 4 at D<=64). K frees after QK^T and Q after the
+//               item's last QK^T, so the next item's Q and K arrive while the
+//               current item finishes.
+//   warp 14     producer of V: the V tile of every visited kv tile into a
+//               ring of kStages, each stage freed after its PV. Waiting for V
+//               stages never holds back the next item's list, Q and K.
 //   warp 13     TMEM owner and MMA issuer (one elected lane):
 //                 S[g % 3] = Q K^T             (tcgen05, SMEM x SMEM)
 //                 O       += P[g % 3] V        (tcgen05, TMEM x SMEM)
@@ -28,7 +31,7 @@
 //               each store half of O's columns (bf16, rows past L_b
 //               untouched; rows that see no column get zeros) while group 2
 //               goes on to the next item.
-//   warps 14-15 idle: 16 warps at 128 registers fill the register file, and
+//   warp 15     idle: 16 warps at 128 registers fill the register file, and
 //               a third epilogue group hides more TMEM and MUFU latency than
 //               two groups at 168 registers.
 //
@@ -153,7 +156,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) hstu_fwd_kernel(const __grid_c
     mbar_init(smem_u32(&s.bar_o_empty), 256);  // epilogue groups 0 and 1 read O out
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&s.bar_item_full[i]), 1);
-      mbar_init(smem_u32(&s.bar_item_empty[i]), 1 + 384);  // MMA issuer + epilogue threads
+      mbar_init(smem_u32(&s.bar_item_empty[i]), 2 + 384);  // MMA issuer, V producer, epilogue
     }
     mbar_init(smem_u32(&s.bar_drain), 1);
     fence_mbar_init();
@@ -176,8 +179,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) hstu_fwd_kernel(const __grid_c
       tma_prefetch_map(&p.tm_k);
       tma_prefetch_map(&p.tm_v);
     }
-    int k_last[NS], v_last[NS];
-    for (int i = 0; i < NS; ++i) k_last[i] = v_last[i] = -1;
+    int k_last[NS];  // last use of each K stage, -1 if never used
+    for (int i = 0; i < NS; ++i) k_last[i] = -1;
     int q_uses = 0;  // items with at least one tile (one Q load each)
     int g = 0;       // tiles issued over all items
     bool ok = true;
@@ -240,32 +243,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1) hstu_fwd_kernel(const __grid_c
             tma_load_4d(smem_u32(s.q), &p.tm_q, smem_u32(&s.bar_q_full), 0, o0 + qt * kBlock, h, 0);
             ++q_uses;
           }
-          // K runs one tile ahead of V within the item.
-          for (int t = 0; ok && t <= n; ++t) {
-            if (t < n) {
-              const int gg = g + t, st = gg % NS, use = gg / NS;
-              if (use > 0 && !mbar_wait(smem_u32(&s.bar_k_empty[st]), (use - 1) & 1, abort_flag)) {
-                ok = false;
-                break;
-              }
-              const uint32_t bar = smem_u32(&s.bar_k_full[st]);
-              mbar_expect_tx(bar, kTile);
-              const int row = o0 + (it_slot.tile[t] & 0xff) * kBlock;
-              tma_load_4d(smem_u32(s.k[st]), &p.tm_k, bar, 0, row, h, 0);
-              k_last[st] = use;
+          for (int t = 0; ok && t < n; ++t) {
+            const int gg = g + t, st = gg % NS, use = gg / NS;
+            if (use > 0 && !mbar_wait(smem_u32(&s.bar_k_empty[st]), (use - 1) & 1, abort_flag)) {
+              ok = false;
+              break;
             }
-            if (t >= 1) {
-              const int gg = g + t - 1, st = gg % NS, use = gg / NS;
-              if (use > 0 && !mbar_wait(smem_u32(&s.bar_v_empty[st]), (use - 1) & 1, abort_flag)) {
-                ok = false;
-                break;
-              }
-              const uint32_t bar = smem_u32(&s.bar_v_full[st]);
-              mbar_expect_tx(bar, kTile);
-              const int row = o0 + (it_slot.tile[t - 1] & 0xff) * kBlock;
-              tma_load_4d(smem_u32(s.v[st]), &p.tm_v, bar, 0, row, h, 0);
-              v_last[st] = use;
-            }
+            const uint32_t bar = smem_u32(&s.bar_k_full[st]);
+            mbar_expect_tx(bar, kTile);
+            const int row = o0 + (it_slot.tile[t] & 0xff) * kBlock;
+            tma_load_4d(smem_u32(s.k[st]), &p.tm_k, bar, 0, row, h, 0);
+            k_last[st] = use;
           }
           g += n;
         }
@@ -275,10 +263,46 @@ __global__ void __launch_bounds__(kFwdThreads, 1) hstu_fwd_kernel(const __grid_c
     // Never leave with a copy in flight.
     if (lane == 0) {
       if (q_uses > 0) mbar_wait_drain(smem_u32(&s.bar_q_full), (q_uses - 1) & 1);
-      for (int st = 0; st < NS; ++st) {
+      for (int st = 0; st < NS; ++st)
         if (k_last[st] >= 0) mbar_wait_drain(smem_u32(&s.bar_k_full[st]), k_last[st] & 1);
-        if (v_last[st] >= 0) mbar_wait_drain(smem_u32(&s.bar_v_full[st]), v_last[st] & 1);
+    }
+    __syncwarp();
+  } else if (warp == 14) {
+    // ------------------------------------------------------------ V producer
+    // Follows the item slots the Q/K producer publishes and loads the V tile
+    // of every visited kv tile; it holds an item slot until its last V load
+    // of that item is issued.
+    int v_last[NS];  // last use of each V stage, -1 if never used
+    for (int i = 0; i < NS; ++i) v_last[i] = -1;
+    int g = 0;  // tiles over all items
+    bool ok = true;
+    for (int i = 0; ok; ++i) {
+      const int slot = i & 1;
+      if (!warp_wait(smem_u32(&s.bar_item_full[slot]), (i >> 1) & 1, abort_flag)) break;
+      const FwdItem& item = s.item[slot];
+      const int nt = item.nt;
+      if (nt < 0) break;  // no more work
+      if (lane == 0) {
+        for (int t = 0; t < nt; ++t) {
+          const int gg = g + t, st = gg % NS, use = gg / NS;
+          if (use > 0 && !mbar_wait(smem_u32(&s.bar_v_empty[st]), (use - 1) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint32_t bar = smem_u32(&s.bar_v_full[st]);
+          mbar_expect_tx(bar, kTile);
+          const int row = item.o0 + (item.tile[t] & 0xff) * kBlock;
+          tma_load_4d(smem_u32(s.v[st]), &p.tm_v, bar, 0, row, item.h, 0);
+          v_last[st] = use;
+        }
+        if (ok) mbar_arrive(smem_u32(&s.bar_item_empty[slot]));
       }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      g += nt;
+    }
+    if (lane == 0) {  // never leave with a copy in flight
+      for (int st = 0; st < NS; ++st)
+        if (v_last[st] >= 0) mbar_wait_drain(smem_u32(&s.bar_v_full[st]), v_last[st] & 1);
     }
     __syncwarp();
   } else if (warp == 13) {
