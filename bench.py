@@ -38,7 +38,8 @@ L2_FLUSH_BYTES = 512 << 20
 
 # DRAM bytes (read + write) per launch of the backward kernel on the default
 # workload, from one ncu capture of that kernel, with the hash of the kernel
-# sources it was taken on; reported only while the sources are unchanged.
+# sources it was taken on; reported only for that workload and while the
+# sources are unchanged.
 NCU_TRAFFIC = {"bwd": 135093248 + 67840768, "sources_sha": "55e6d7ab9a4136b2"}
 
 
@@ -545,7 +546,10 @@ def main():
     ms_bwd = statistics.mean(r["bwd"])
     achieved = f_bwd / (ms_bwd * 1e-3) / 1e12
     sha = kernel_sources_sha()
-    traffic = NCU_TRAFFIC["bwd"] if NCU_TRAFFIC["sources_sha"] == sha else None
+    # The recorded bytes are those of one launch on the default workload only
+    # (equal-length sequences, so every rank's share is that same launch).
+    same_workload = args.config == DEFAULT_CONFIG and args.batch is None
+    traffic = NCU_TRAFFIC["bwd"] if NCU_TRAFFIC["sources_sha"] == sha and same_workload else None
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
