@@ -576,13 +576,9 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
 template <int DP, int NINT>
 static cudaError_t launch_bwd_t(const AttnParams& p, int grid_items, cudaStream_t stream) {
   const int smem = static_cast<int>(sizeof(BwdSmem<DP>)) + 1024;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(hstu_bwd_kernel<DP, NINT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static std::atomic<uint64_t> configured{0};  // devices with the limit raised
+  cudaError_t e0 = ensure_smem_limit(hstu_bwd_kernel<DP, NINT>, smem, configured);
+  if (e0 != cudaSuccess) return e0;
   const long long work = 2LL * grid_items * p.heads;
   if (work <= 0) return cudaSuccess;
   int dev = 0, sms = 0;

@@ -475,13 +475,9 @@ static cudaError_t sm_count(int* sms) {
 template <int DP, int NINT>
 static cudaError_t launch_fwd_t(const AttnParams& p, int grid_items, cudaStream_t stream) {
   const int smem = static_cast<int>(sizeof(FwdSmem<DP>)) + 1024;
-  static bool configured = false;  // attribute set once per instantiation
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(hstu_fwd_kernel<DP, NINT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static std::atomic<uint64_t> configured{0};  // devices with the limit raised
+  cudaError_t e0 = ensure_smem_limit(hstu_fwd_kernel<DP, NINT>, smem, configured);
+  if (e0 != cudaSuccess) return e0;
   const long long work = static_cast<long long>(grid_items) * p.heads;
   if (work <= 0) return cudaSuccess;
   int sms = 0;

@@ -3,9 +3,27 @@
 
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "common.cuh"
 
 namespace hstu {
+
+// Raises `kernel`'s dynamic shared-memory limit to `smem` bytes on the
+// current device, once per device (the attribute belongs to the device's
+// context, so a process that drives several GPUs sets it on each).
+// `done` holds one bit per device already set up.
+template <typename Kernel>
+cudaError_t ensure_smem_limit(Kernel kernel, int smem, std::atomic<uint64_t>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev < 64 ? (uint64_t{1} << dev) : 0;
+  if (bit != 0 && (done.load(std::memory_order_acquire) & bit) != 0) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess && bit != 0) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
 
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream);
 // grid_items: upper bound on the number of work items (CTAs = items * heads).
