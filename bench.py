@@ -308,6 +308,25 @@ def oracle_sample(cfg, seed, budget_s, min_seqs=1, max_seqs=None):
     return flops, secs, done, len(lens)
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (x86) or part description (Arm), best effort."""
+    import platform
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read()
+        for key in ("model name", "Model name"):
+            for line in info.splitlines():
+                if line.startswith(key):
+                    return line.split(":", 1)[1].strip()
+        parts = sorted({line.split(":", 1)[1].strip() for line in info.splitlines()
+                        if line.startswith("CPU part")})
+        if parts:
+            return f"{platform.machine()} (CPU part {', '.join(parts)})"
+    except OSError:
+        pass
+    return platform.machine()
+
+
 def cpu_cores():
     try:
         from threadpoolctl import threadpool_info
@@ -460,7 +479,8 @@ def run_reference(args, cfg):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": cfg.name, "batch": cfg.batch, "seq_len": cfg.len_hi,
                                             "heads": cfg.heads, "head_dim": cfg.dim, "nfunc": cfg.nfunc},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "cpu": cpu_model(),
+                             "kind": "oracle",
                              "sample": f"1 of {cfg.batch} sequences (the longest) per step, all heads, "
                                        "fwd+bwd, dense fp64 numpy"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -568,6 +588,8 @@ def main():
                    "parallelism": f"dp{world}" if world > 1 else "single", "l2": "flushed between steps"},
         "pct_of_bf16_peak": 100.0 * value / world / peaks["bf16_tflops"],
         "breakdown_ms": {k: statistics.mean(r[k]) for k in ("plan", "fwd", "bwd")},
+        "step_ms_stats": {"mean": ms_step, "median": statistics.median(r["step"]), "min": min(r["step"]),
+                          "max": max(r["step"])},
         "useful_gflop_per_step": useful / 1e9,
         "gpu_launches": LAUNCHES_PER_STEP * args.steps * len(legs),
         "roofline": {"kernel": "hstu_bwd_kernel", "bound": "tensor", "achieved": achieved,
@@ -589,7 +611,8 @@ def main():
                           "padding_overhead_basis": "medians over the timed steps; legs alternate order"}
     if not args.no_cpu_baseline:
         f, s, n, nb = oracle_sample(cfg, seed, args.cpu_budget)
-        line["cpu_baseline"] = {"value": f / s / 1e12, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+        line["cpu_baseline"] = {"value": f / s / 1e12, "unit": UNIT, "cores": cpu_cores(), "cpu": cpu_model(),
+                                "kind": "oracle",
                                 "sample": f"{n} of {nb} sequences (longest first), all heads, fwd+bwd, "
                                           f"dense fp64 numpy, {s:.1f} s"}
     print(json.dumps(line), flush=True)
