@@ -184,6 +184,19 @@ HSTU_API hstu_status_t hstu_attn_get_device_status(const void* ws, void* stream)
 /* Static description of a status code. */
 HSTU_API const char* hstu_status_string(hstu_status_t status);
 
+/* Test hook for the failure path of the kernels' bounded in-kernel waits.
+ * Enqueues one small kernel that waits, with the same bounded wait the
+ * attention kernels use, on a barrier that nothing arrives at. After
+ * limit_ms milliseconds the wait gives up, and the kernel records
+ * HSTU_ERR_TIMEOUT in ws's error word, as a timed-out attention kernel does;
+ * hstu_attn_get_device_status then returns it. Nothing faults and the
+ * context stays usable. The next plan clears the error word.
+ *   ws:       DEVICE workspace of either mode, 256-byte aligned.
+ *   limit_ms: 1 to 2000.
+ * Returns HSTU_ERR_WORKSPACE for a null or misaligned ws and
+ * HSTU_ERR_INVALID_ARG for a limit out of range; nothing is enqueued then. */
+HSTU_API hstu_status_t hstu_attn_test_wait_timeout(void* ws, int32_t limit_ms, void* stream);
+
 /* Splits a batch over `world` data-parallel ranks, by whole sequences. Every
  * (sequence, head) unit of the op is independent in the forward and the
  * backward pass, so the ranks need no exchange; each runs the op on its own

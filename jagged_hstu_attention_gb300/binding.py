@@ -30,7 +30,7 @@ EXPORTED = (
     "hstu_attn_nfunc_supported", "hstu_attn_workspace_size", "hstu_attn_plan", "hstu_attn_fwd",
     "hstu_attn_bwd", "hstu_attn_fwd_targets_only", "hstu_attn_bwd_targets_only",
     "hstu_attn_get_device_status", "hstu_status_string", "hstu_attn_fwd_noalloc",
-    "hstu_attn_shard_sequences",
+    "hstu_attn_shard_sequences", "hstu_attn_test_wait_timeout",
 )
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
@@ -80,6 +80,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "hstu_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "hstu_attn_fwd_noalloc": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, sp, vp, vp]),
         "hstu_attn_shard_sequences": (ctypes.c_int, [vp, i32, i32, vp, vp]),
+        "hstu_attn_test_wait_timeout": (ctypes.c_int, [vp, i32, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -267,3 +268,11 @@ def shard_sequences(cost, world: int) -> Tuple[torch.Tensor, torch.Tensor]:
     _check(load().hstu_attn_shard_sequences(_ptr(c), c.numel(), world, _ptr(owner), _ptr(load_)),
            "hstu_attn_shard_sequences")
     return owner, load_
+
+
+def selftest_wait_timeout(ws: torch.Tensor, limit_ms: int, stream=None) -> None:
+    """Enqueues the failure-path test of the in-kernel waits
+    (hstu_attn_test_wait_timeout): a wait that nothing ends gives up after
+    ``limit_ms`` and records HSTU_ERR_TIMEOUT in ``ws``."""
+    _check(load().hstu_attn_test_wait_timeout(_ptr(ws), int(limit_ms), _stream(stream)),
+           "hstu_attn_test_wait_timeout")

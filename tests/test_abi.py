@@ -95,3 +95,11 @@ def test_status_strings(lib):
     for st in range(7):
         assert len(hb.status_string(st)) > 0
     assert "unknown" in hb.status_string(42)
+
+
+def test_wait_timeout_hook_checks_its_arguments(lib):
+    vp = ctypes.c_void_p
+    assert lib.hstu_attn_test_wait_timeout(None, 20, None) == 3          # null workspace
+    assert lib.hstu_attn_test_wait_timeout(vp((1 << 20) + 64), 20, None) == 3  # misaligned
+    assert lib.hstu_attn_test_wait_timeout(vp(1 << 20), 0, None) == 1    # limit too small
+    assert lib.hstu_attn_test_wait_timeout(vp(1 << 20), 2001, None) == 1  # limit too large

@@ -224,6 +224,30 @@ def test_batch_of_empty_sequences():
     assert dk.numel() == 0 and dv.numel() == 0
 
 
+def test_wait_timeout_reaches_the_host_and_the_context_stays_usable():
+    """A bounded in-kernel wait that nothing ends gives up after its limit and
+    reports HSTU_ERR_TIMEOUT through the workspace; the next plan clears it and
+    the same workspace runs the op correctly."""
+    lens = np.array([130, 7])
+    q, k, v, do = _gen(lens, 2, 64, seed=8)
+    func = wl.build_func(wl.Config("c", 2, 0, 0, 2, 64, "causal", 1), lens, 1)
+    gb = GpuBatch(lens, func, q, k, v, do)
+    shape = hb.make_shape(2, gb.total, 2, 64, 1, gb.max_seqlen, gb.alpha)
+    ws = hb.alloc_workspace(shape)
+    hb.plan(gb.d_off, gb.d_func, shape, ws)
+    assert hb.device_status(ws) == hb.HSTU_OK
+    e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    e[0].record()
+    hb.selftest_wait_timeout(ws, 20)
+    e[1].record()
+    assert hb.device_status(ws) == 6  # HSTU_ERR_TIMEOUT
+    assert 19.0 <= e[0].elapsed_time(e[1]) < 1000.0
+    o = hb.fwd(gb.q, gb.k, gb.v, gb.d_off, gb.d_func, gb.max_seqlen, gb.alpha, ws=ws)
+    assert hb.device_status(ws) == hb.HSTU_OK
+    ref = gb.oracle(want_bwd=False)
+    check_o(np64(o), ref["o"])
+
+
 def test_backward_is_bitwise_repeatable():
     gb = GpuBatch.from_config(wl.CONFIGS["onerank_b64"], 1)
     a = gb.run()
