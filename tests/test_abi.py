@@ -103,3 +103,20 @@ def test_wait_timeout_hook_checks_its_arguments(lib):
     assert lib.hstu_attn_test_wait_timeout(vp((1 << 20) + 64), 20, None) == 3  # misaligned
     assert lib.hstu_attn_test_wait_timeout(vp(1 << 20), 0, None) == 1    # limit too small
     assert lib.hstu_attn_test_wait_timeout(vp(1 << 20), 2001, None) == 1  # limit too large
+
+
+def test_binding_fails_loudly_without_the_library(monkeypatch):
+    monkeypatch.setattr(hb, "_lib", None)
+    with pytest.raises(RuntimeError, match="missing"):
+        hb.load(os.path.join(ROOT, "no_such_dir", "libhstu_attn.so"))
+
+
+def test_binding_has_no_cpu_path():
+    import torch
+    q = torch.zeros((4, 1, 32), dtype=torch.bfloat16)
+    off = torch.tensor([0, 4], dtype=torch.int32)
+    func = torch.full((1, 4), 4, dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA"):
+        hb.fwd(q, q, q, off, func, 4)
+    with pytest.raises(ValueError, match="CUDA"):
+        hb.bwd(q, q, q, q, off, func, 4)
