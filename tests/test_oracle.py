@@ -140,6 +140,40 @@ def test_partition_chunks_equal_causal():
                                orc.fwd_dense(q, k, v, off, fc, 1, N, alpha), rtol=0, atol=1e-15)
 
 
+def test_sla_equals_causal_when_the_prefix_spans_every_row():
+    """SLA with a global prefix K1 at least as long as the sequence sees
+    [0, i+1) on every row (the prefix clipped causally covers the window):
+    the same function as plain causal, forward and backward."""
+    lens, off, q, k, v, do = _small_batch(9, [20, 33, 5])
+    sla = wl.Config("s", 3, 0, 0, 2, 16, "sla", 5, k1=40, k2=6)
+    fs = wl.build_func(sla, lens, 5)
+    fc = wl.build_func(wl.Config("c", 3, 0, 0, 2, 16, "causal", 1), lens, 1)
+    N, alpha = 33, 0.3
+    np.testing.assert_array_equal(orc.visible_counts(off, fs, 5), orc.visible_counts(off, fc, 1))
+    np.testing.assert_allclose(orc.fwd_dense(q, k, v, off, fs, 5, N, alpha),
+                               orc.fwd_dense(q, k, v, off, fc, 1, N, alpha), rtol=0, atol=1e-15)
+    for a, b in zip(orc.bwd_dense(do, q, k, v, off, fs, 5, N, alpha),
+                    orc.bwd_dense(do, q, k, v, off, fc, 1, N, alpha)):
+        np.testing.assert_allclose(a, b, rtol=0, atol=1e-15)
+    # a shorter prefix is not causal: rows past K1 + K2 lose columns
+    short = wl.build_func(wl.Config("s", 3, 0, 0, 2, 16, "sla", 5, k1=8, k2=6), lens, 5)
+    assert orc.visible_counts(off, short, 5).sum() < orc.visible_counts(off, fc, 1).sum()
+
+
+@pytest.mark.parametrize("mask", ["tiny", "sla", "onerank", "causal"])
+@pytest.mark.parametrize("nfunc", [5, 7, 9])
+def test_func_width_matches_nfunc_and_padding_is_empty(mask, nfunc):
+    """Contract of the func builders: nfunc rows per token, and every interval
+    past the ones the mask uses is empty (max <= min) on every row."""
+    lens = np.array([40, 100] if mask == "onerank" else [40, 9])
+    cfg = wl.Config("w", 2, 0, 0, 2, 16, mask, nfunc)
+    f = wl.build_func(cfg, lens, nfunc)
+    assert f.shape == (nfunc, int(lens.sum()))
+    used = {"tiny": 3, "sla": 3, "onerank": 5, "causal": 1}[mask]
+    for t in range((used + 1) // 2, (nfunc + 1) // 2):
+        assert np.all(f[2 * t] <= f[2 * t - 1]), t
+
+
 def test_mutation_dropping_last_interval_is_caught(monkeypatch):
     """Plant the mistake the pages describe (decode loop drops the last
     interval) in the oracle: the partition pin must then fail."""
