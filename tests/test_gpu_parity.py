@@ -257,6 +257,41 @@ def test_backward_is_bitwise_repeatable():
             assert torch.equal(a[n], b[n]), n
 
 
+def test_maximum_sequence_length():
+    """One sequence of the maximum length (32768 rows, 256 tiles), causal.
+    dO is zero except on a few rows, so dK, dV and dQ over the whole sequence
+    are the sum of those rows' contributions, which the oracle computes one
+    row at a time (the targets-only routine is the full op's row); O is
+    checked on sampled rows the same way, and the visible counts in full."""
+    L, H, D = 32768, 1, 128
+    lens = np.array([L])
+    g = torch.Generator().manual_seed(21)
+    q, k, v = (wl.randn_bf16((L, H, D), g) for _ in range(3))
+    rows = [0, 127, 128, 20000, 32639, L - 1]
+    do = torch.zeros((L, H, D), dtype=torch.bfloat16)
+    do[rows] = wl.randn_bf16((len(rows), H, D), g)
+    func = wl.build_func(wl.Config("c", 1, 0, 0, H, D, "causal", 1), lens, 1)
+    gb = GpuBatch(lens, func, q, k, v, do)
+    out = gb.run()
+    assert np.array_equal(out["counts"].cpu().numpy(), np.arange(L) + 1)
+    hq, hk, hv, hdo = (np64(t) for t in (q, k, v, do))
+    off = np.array([0, L])
+    ref_dk, ref_dv = np.zeros_like(hk), np.zeros_like(hv)
+    ref_dq = np.zeros_like(hq)
+    for r in rows + [1, 129, 4095, 31000]:
+        fc = func[:, r:r + 1]
+        o_r = orc.fwd_targets_only(hq[r:r + 1], hk, hv, off, fc, 1, L, gb.alpha)
+        check_o(np64(out["o"][r:r + 1]), o_r)
+        if r in rows:
+            dq_r, dk_r, dv_r = orc.bwd_targets_only(hdo[r:r + 1], hq[r:r + 1], hk, hv, off, fc, 1, L, gb.alpha)
+            ref_dq[r:r + 1] = dq_r
+            ref_dk += dk_r
+            ref_dv += dv_r
+    check_grad(np64(out["dq"]), ref_dq, "dq")
+    check_grad(np64(out["dk"]), ref_dk, "dk")
+    check_grad(np64(out["dv"]), ref_dv, "dv")
+
+
 def test_results_do_not_depend_on_the_rest_of_the_batch():
     """A sequence's outputs are bitwise the same alone or inside a batch (with
     the same N): every output element is computed by one CTA in a fixed order
