@@ -29,7 +29,12 @@ to rounding, its speed coming only from skipping work):
   for the rows the loss reads", Summary and Read First): one query row per
   sequence, evaluated against the full-length K/V of its sequence; it is the
   same function of the same inputs as that row of the full path, so it calls
-  the same row-block routine with a one-row block.
+  the same row-block routine with a one-row block. Several candidates per
+  sequence (the page's "not exactly one target per sequence" batches) form a
+  row block of their sequence (``fwd_targets`` / ``bwd_targets``).
+* Candidate-row projection (the same page, Summary: U and Q are computed for
+  the candidate rows alone): ``silu(x[rows] W^T + b)`` and its gradients
+  (``project_rows`` / ``project_rows_backward``).
 
 Two independent formulations are provided so that they can pin each other on
 tiny inputs: a per-pair pure-Python loop (``*_loop``) and a dense per-sequence
@@ -276,6 +281,84 @@ def bwd_targets_only(do_c, q_c, k, v, seq_offsets, func_c, nfunc, max_seqlen, al
         dq_c[b:b + 1], dk[o0:o1], dv[o0:o1] = block_backward(
             do_c[b:b + 1], q_c[b:b + 1], k[o0:o1], v[o0:o1], M, alpha, float(max_seqlen))
     return dq_c, dk, dv
+
+
+# ----------------------------------------------------------------------------
+# Several candidates per sequence (MLCommons training PR #903, Gating: a batch
+# that is not exactly one target per sequence). Reading: each candidate row is
+# the same function of its own q row and func column against its sequence's
+# full K/V, so the candidates of a sequence form one row block of that
+# sequence. Candidates cand_offsets[b] .. cand_offsets[b+1] of q_c belong to
+# sequence b.
+# ----------------------------------------------------------------------------
+def fwd_targets(q_c, k, v, seq_offsets, cand_offsets, func_c, nfunc, max_seqlen, alpha):
+    """q_c (C, H, D), func_c (nfunc, C) -> o_c (C, H, Dv)."""
+    q_c = np.asarray(q_c, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    o_c = np.zeros((q_c.shape[0], q_c.shape[1], v.shape[2]))
+    for b, o0, o1 in _seq_iter(seq_offsets):
+        c0, c1 = int(cand_offsets[b]), int(cand_offsets[b + 1])
+        if c1 <= c0:
+            continue
+        M = mask_block(func_c[:, c0:c1], nfunc, o1 - o0)
+        o_c[c0:c1] = block_forward(q_c[c0:c1], k[o0:o1], v[o0:o1], M, alpha, float(max_seqlen))
+    return o_c
+
+
+def bwd_targets(do_c, q_c, k, v, seq_offsets, cand_offsets, func_c, nfunc, max_seqlen, alpha):
+    """-> (dq_c (C, H, D), dk (T, H, D), dv (T, H, Dv)); dk, dv sum over the
+    candidates of each sequence."""
+    do_c = np.asarray(do_c, np.float64)
+    q_c = np.asarray(q_c, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    dq_c = np.zeros_like(q_c)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    for b, o0, o1 in _seq_iter(seq_offsets):
+        c0, c1 = int(cand_offsets[b]), int(cand_offsets[b + 1])
+        if c1 <= c0:
+            continue
+        M = mask_block(func_c[:, c0:c1], nfunc, o1 - o0)
+        dq_c[c0:c1], dk[o0:o1], dv[o0:o1] = block_backward(
+            do_c[c0:c1], q_c[c0:c1], k[o0:o1], v[o0:o1], M, alpha, float(max_seqlen))
+    return dq_c, dk, dv
+
+
+# ----------------------------------------------------------------------------
+# Candidate-row projection of the targets-only layer (MLCommons training PR
+# #903, Summary: the last layer computes U and Q for the candidate row alone,
+# K and V stay full length). The pages do not spell the projection out;
+# reading: U and Q of a row come from that row of the layer input through the
+# layer's pointwise-SiLU input projection, y = silu(x W^T + b) with W laid
+# out (out features, in features), so the targets-only layer evaluates it on
+# the candidate rows only.
+# ----------------------------------------------------------------------------
+def project_rows(x, rows, w, bias):
+    """x (T, d_in), rows (C,) int, w (d_out, d_in), bias (d_out,) or None ->
+    (y (C, d_out), z (C, d_out)) with z = x[rows] w^T + bias, y = silu(z)."""
+    x = np.asarray(x, np.float64)
+    w = np.asarray(w, np.float64)
+    z = x[np.asarray(rows, dtype=np.int64)] @ w.T
+    if bias is not None:
+        z = z + np.asarray(bias, np.float64)[None, :]
+    with np.errstate(over="ignore"):
+        return _silu(z), z
+
+
+def project_rows_backward(dy, x, rows, w, bias):
+    """Gradients of sum(y * dy) -> (dx (T, d_in): zero on rows not selected,
+    dw (d_out, d_in), db (d_out,))."""
+    dy = np.asarray(dy, np.float64)
+    x = np.asarray(x, np.float64)
+    w = np.asarray(w, np.float64)
+    rows = np.asarray(rows, dtype=np.int64)
+    _, z = project_rows(x, rows, w, bias)
+    g = dy * _silu_grad(z)
+    dx = np.zeros_like(x)
+    np.add.at(dx, rows, g @ w)
+    return dx, g.T @ x[rows], g.sum(axis=0)
 
 
 def useful_pairs(seq_offsets, func, nfunc) -> int:

@@ -332,3 +332,120 @@ def test_rows_with_no_visible_column_are_zero():
     assert not o.any()
     dq, dk, dv = orc.bwd_dense(do, q, k, v, off, func, 3, 9, 0.25)
     assert not dq.any() and not dk.any() and not dv.any()
+
+
+# ---------------------------------------------------------------- several candidates per sequence
+def test_multi_candidates_equal_the_full_paths_rows():
+    """Candidate rows taken from inside each sequence (any rows, any number,
+    none for one sequence) give exactly the full path's rows; the gradients
+    equal the full path's when dO is zero off those rows."""
+    cfg = wl.CONFIGS["tiny"]
+    lens, off, q, k, v, do = _small_batch(12, [40, 17, 64, 3], H=2, D=16)
+    func = wl.build_func(cfg, lens, 5)
+    picks = [[0, 7, 39], [], [5, 6, 63, 20], [2]]
+    rows = np.array([off[b] + i for b, p in enumerate(picks) for i in p])
+    cand_off = np.concatenate([[0], np.cumsum([len(p) for p in picks])])
+    N, alpha = 64, 0.25
+    o = orc.fwd_dense(q, k, v, off, func, 5, N, alpha)
+    oc = orc.fwd_targets(q[rows], k, v, off, cand_off, func[:, rows], 5, N, alpha)
+    np.testing.assert_allclose(oc, o[rows], rtol=1e-13, atol=1e-15)
+    do_full = np.zeros_like(do)
+    do_full[rows] = do[rows]
+    dq, dk, dv = orc.bwd_dense(do_full, q, k, v, off, func, 5, N, alpha)
+    dqc, dkc, dvc = orc.bwd_targets(do[rows], q[rows], k, v, off, cand_off, func[:, rows], 5, N, alpha)
+    np.testing.assert_allclose(dqc, dq[rows], rtol=1e-12, atol=1e-15)
+    np.testing.assert_allclose(dkc, dk, rtol=1e-12, atol=1e-15)
+    np.testing.assert_allclose(dvc, dv, rtol=1e-12, atol=1e-15)
+
+
+def test_one_candidate_per_sequence_is_the_targets_only_form():
+    cfg = wl.CONFIGS["dlrm_b1024"]
+    lens, off, q, k, v, do = _small_batch(13, [30, 9, 50], H=2, D=8)
+    fc = wl.build_func_candidates(lens, 3)
+    g = torch.Generator().manual_seed(2)
+    q_c, do_c = (_np64(wl.randn_bf16((3, 2, 8), g)) for _ in range(2))
+    one = np.arange(4)
+    np.testing.assert_array_equal(orc.fwd_targets(q_c, k, v, off, one, fc, 3, 50, 0.3),
+                                  orc.fwd_targets_only(q_c, k, v, off, fc, 3, 50, 0.3))
+    for a, b in zip(orc.bwd_targets(do_c, q_c, k, v, off, one, fc, 3, 50, 0.3),
+                    orc.bwd_targets_only(do_c, q_c, k, v, off, fc, 3, 50, 0.3)):
+        np.testing.assert_array_equal(a, b)
+
+
+def test_multi_candidate_gradients_match_central_differences():
+    lens = np.array([11, 7])
+    off = wl.offsets_from_lengths(lens)
+    _, _, _, k, v, _ = _small_batch(14, lens, H=1, D=4)
+    g = torch.Generator().manual_seed(5)
+    q_c, do_c = (_np64(wl.randn_bf16((5, 1, 4), g)) for _ in range(2))
+    cand_off = np.array([0, 3, 5])
+    fc = np.array([[11, 4, 6, 7, 2], [2, 0, 1, 3, 0], [9, 11, 3, 7, 7]], dtype=np.int32)  # NFUNC=3
+    N, alpha, h = 11, 0.7, 1e-6
+
+    def loss(q_, k_, v_):
+        return float((orc.fwd_targets(q_, k_, v_, off, cand_off, fc, 3, N, alpha) * do_c).sum())
+
+    grads = orc.bwd_targets(do_c, q_c, k, v, off, cand_off, fc, 3, N, alpha)
+    rng = np.random.default_rng(1)
+    for which, grad in enumerate(grads):
+        base = (q_c, k, v)[which]
+        for _ in range(10):
+            idx = tuple(int(rng.integers(0, s_)) for s_ in base.shape)
+            args = [q_c.copy(), k.copy(), v.copy()]
+            args[which][idx] += h
+            lp = loss(*args)
+            args[which][idx] -= 2 * h
+            lm = loss(*args)
+            fd = (lp - lm) / (2 * h)
+            assert abs(fd - grad[idx]) <= 1e-6 * max(1.0, abs(grad[idx])) + 1e-9, (which, idx)
+
+
+# ---------------------------------------------------------------- candidate-row projection
+def test_projection_matches_a_per_element_loop():
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((9, 5))
+    w = rng.standard_normal((4, 5))
+    b = rng.standard_normal(4)
+    rows = np.array([7, 0, 3])
+    y, z = orc.project_rows(x, rows, w, b)
+    for i, r in enumerate(rows):
+        for o in range(4):
+            zz = b[o]
+            for d in range(5):
+                zz += x[r, d] * w[o, d]
+            assert abs(z[i, o] - zz) < 1e-12
+            assert abs(y[i, o] - zz / (1.0 + math.exp(-zz))) < 1e-12
+
+
+def test_projection_identity_weights_give_silu_of_the_rows():
+    x = np.linspace(-6, 6, 30).reshape(6, 5)
+    rows = np.array([5, 2])
+    y, _ = orc.project_rows(x, rows, np.eye(5), None)
+    np.testing.assert_allclose(y, x[rows] * torch.sigmoid(torch.tensor(x[rows])).numpy(), rtol=1e-14)
+
+
+def test_projection_gradients_match_central_differences():
+    rng = np.random.default_rng(4)
+    x = rng.standard_normal((8, 6))
+    w = rng.standard_normal((5, 6))
+    b = rng.standard_normal(5)
+    rows = np.array([1, 6, 1, 3])  # a repeated row accumulates
+    dy = rng.standard_normal((4, 5))
+    dx, dw, db = orc.project_rows_backward(dy, x, rows, w, b)
+    assert not dx[[0, 2, 4, 5, 7]].any()
+    h = 1e-6
+
+    def loss(x_, w_, b_):
+        return float((orc.project_rows(x_, rows, w_, b_)[0] * dy).sum())
+
+    for which, grad in ((0, dx), (1, dw), (2, db)):
+        for _ in range(8):
+            base = (x, w, b)[which]
+            idx = tuple(int(rng.integers(0, s_)) for s_ in base.shape)
+            args = [x.copy(), w.copy(), b.copy()]
+            args[which][idx] += h
+            lp = loss(*args)
+            args[which][idx] -= 2 * h
+            lm = loss(*args)
+            fd = (lp - lm) / (2 * h)
+            assert abs(fd - grad[idx]) <= 1e-6 * max(1.0, abs(grad[idx])) + 1e-9, (which, idx)
