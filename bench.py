@@ -4,15 +4,23 @@
 A step is one pass of the whole hot path over one synthetic batch: the plan
 (offset validation, tile classification, longest-first work lists), the
 forward kernel and the backward kernel, all through the C ABI. The headline
-workload is the SLA mask of TorchEasyRec PR #670 at B=32, S=1024, H=4, D=128
-with NFUNC=5 (third interval padded empty); the NFUNC=3 leg of the same batch
-runs interleaved with it to give the padding overhead.
+workload is the DLRMv4 last-layer shape of MLCommons training PR #903
+(layer-timing table): B=1024 sequences of 2663 +-50% ragged length (about
+2.77 M tokens), H=4, D=128, causal with one candidate per sequence. Two
+sub-measurements ride on the same JSON line:
+
+  padding       the SLA mask of TorchEasyRec PR #670 at B=32, S=1024, H=4,
+                D=128, NFUNC=5 (third interval padded empty) against NFUNC=3
+                on the same batch, legs interleaved: the cost of the padding;
+  targets_only  the same DLRM batch in targets-only mode (one candidate row
+                per sequence against full-length K/V), HBM-bound.
 
 Metric: useful TFLOP/s = visible (row, column) pairs x heads x (4 D forward +
 10 D backward) / step time. Prints one JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-  python bench.py --config onerank_b64|sla_b16_s2048|dlrm_b1024 ...
+  python bench.py --config onerank_b64|sla_b16_s2048|sla_b32_s1024 ...
+  python bench.py --mode targets ...      (targets-only line on its own)
 """
 from __future__ import annotations
 
@@ -33,14 +41,22 @@ sys.path.insert(0, ROOT)
 
 METRIC = "HSTU masked attn fwd+bwd ms and useful TFLOP/s (% bf16 TC peak), 1xGB300"
 UNIT = "TFLOP/s"
-DEFAULT_CONFIG = "sla_b32_s1024"
+DEFAULT_CONFIG = "dlrm_b1024"
+PADDING_CONFIG = "sla_b32_s1024"
 L2_FLUSH_BYTES = 512 << 20
 
-# DRAM bytes (read + write) per launch of the backward kernel on the default
-# workload, from one ncu capture of that kernel, with the hash of the kernel
-# sources it was taken on; reported only for that workload and while the
+# DRAM bytes (read + write) of the backward kernel per token, by mask family,
+# from one ncu capture of a smaller case of the same family (named in
+# "captured_on"), with the hash of the kernel sources it was taken on. The
+# backward reads q, k, v, dO and writes dq, dk, dv once, so its traffic grows
+# in proportion to the tokens of a launch; it is reported only while the
 # sources are unchanged.
-NCU_TRAFFIC = {"bwd": 135039488 + 67507456, "sources_sha": "8423d3539869318a"}
+NCU_TRAFFIC = {
+    "causal": {"bytes_per_token": (723308288 + 498629888) / 172107,
+               "captured_on": "hstu_bwd_kernel on dlrm_b1024@b64 (172,107 tokens, same length mix and mask), "
+                              "dram__bytes_read.sum + dram__bytes_write.sum, scaled by tokens",
+               "sources_sha": "9f5e4609dafe54bb"},
+}
 
 
 def kernel_sources_sha() -> str:
@@ -50,7 +66,7 @@ def kernel_sources_sha() -> str:
     import re
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "jagged_hstu_attention_gb300", "csrc")
-    for name in ("attn_bwd.cu", "common.cuh", "sm103_primitives.cuh"):
+    for name in ("attn_bwd.cuh", "attn_bwd_bf16.cu", "common.cuh", "sm103_primitives.cuh"):
         with open(os.path.join(csrc, name)) as f:
             code = f.read()
         code = re.sub(r"/\*.*?\*/", " ", code, flags=re.S)
@@ -275,22 +291,29 @@ def e2e_leg(leg, steps, warmup):
 
 
 # ---------------------------------------------------------------- CPU oracle
-def oracle_sample(cfg, seed, budget_s, min_seqs=1, max_seqs=None):
+def oracle_sample(cfg, seed, budget_s, min_seqs=1, max_seqs=None, order="longest"):
     """Times the fp64 oracle (as it stands) on whole sequences of the workload
-    until the time budget is spent; returns (useful flops, seconds, seqs)."""
+    until the time budget is spent. Sequences are taken longest first
+    (order="longest") or in a seeded random order ("random"). Returns
+    (useful flops, seconds, sequences done, sequences in the batch, visible
+    pairs per head done)."""
     import torch
     import oracle.hstu_oracle as orc
     from jagged_hstu_attention_gb300 import workloads as wl
     lens = wl.lengths(cfg, seed)
     N = int(lens.max())
     alpha = 1.0 / math.sqrt(cfg.dim)
-    order = np.argsort(-lens, kind="stable")
+    if order == "longest":
+        seq_order = np.argsort(-lens, kind="stable")
+    else:
+        seq_order = np.random.default_rng(seed + 77).permutation(len(lens))
     g = torch.Generator().manual_seed(seed)
     flops = 0.0
     secs = 0.0
     done = 0
+    pairs_done = 0
     limit = max_seqs if max_seqs is not None else len(lens)
-    for b in order[:limit]:
+    for b in seq_order[:limit]:
         L = int(lens[b])
         f = wl.func_rows(cfg, L)
         shape = (L, cfg.heads, cfg.dim)
@@ -301,11 +324,12 @@ def oracle_sample(cfg, seed, budget_s, min_seqs=1, max_seqs=None):
         orc.bwd_dense(do, q, k, v, off, f, cfg.nfunc, N, alpha)
         secs += time.perf_counter() - t0
         pairs = int(orc.visible_counts(off, f, cfg.nfunc).sum())
+        pairs_done += pairs
         flops += pairs * cfg.heads * 14 * cfg.dim
         done += 1
         if done >= min_seqs and secs >= budget_s:
             break
-    return flops, secs, done, len(lens)
+    return flops, secs, done, len(lens), pairs_done
 
 
 def cpu_model() -> str:
@@ -328,33 +352,79 @@ def cpu_model() -> str:
 
 
 def cpu_cores():
+    """(threads the oracle's BLAS pool runs, cores the OS reports, cores this
+    process may run on)."""
+    blas = 0
     try:
         from threadpoolctl import threadpool_info
-        n = max((i.get("num_threads", 0) for i in threadpool_info()), default=0)
-        if n:
-            return int(n)
+        blas = max((int(i.get("num_threads", 0)) for i in threadpool_info()), default=0)
     except Exception:
         pass
-    return os.cpu_count()
+    try:
+        affinity = len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        affinity = os.cpu_count()
+    return (blas or affinity), os.cpu_count(), affinity
+
+
+def cpu_baseline_record(value, secs, seqs, n_batch, sample, extra=None):
+    used, total, affinity = cpu_cores()
+    rec = {"value": value, "unit": UNIT, "cores": used, "os_cpu_count": total, "affinity_cores": affinity,
+           "cpu": cpu_model(), "kind": "oracle", "sample": sample}
+    if extra:
+        rec.update(extra)
+    return rec
 
 
 # ---------------------------------------------------------------- ranks
-def rank_sequences(cfg, seed, world, rank):
+def job_lengths(cfg, seed, world):
+    """Lengths of the job's batch: cfg.batch * world sequences from `seed`."""
+    import dataclasses
+    from jagged_hstu_attention_gb300 import workloads as wl
+    return wl.lengths(dataclasses.replace(cfg, batch=cfg.batch * world), seed)
+
+
+def job_costs(cfg, seed, world, device):
+    """Visible (row, column) pairs of every sequence of the job's batch, from
+    the plan's per-row counts (hstu_attn_plan on this GPU): the work each
+    sequence brings, whatever its mask."""
+    import torch
+    from jagged_hstu_attention_gb300 import binding as hb
+    from jagged_hstu_attention_gb300 import workloads as wl
+    lens = job_lengths(cfg, seed, world)
+    off = wl.offsets_from_lengths(lens)
+    T = int(off[-1])
+    func = wl.build_func(cfg, lens)
+    d_off = torch.tensor(off, dtype=torch.int32, device=device)
+    d_func = torch.tensor(func, dtype=torch.int32, device=device)
+    shape = hb.make_shape(len(lens), T, cfg.heads, cfg.dim, cfg.nfunc, int(lens.max()))
+    ws = hb.alloc_workspace(shape, hb.WS_FULL, device)
+    counts = torch.empty(max(T, 1), dtype=torch.int32, device=device)
+    hb.plan(d_off, d_func, shape, ws, row_counts=counts)
+    if hb.device_status(ws) != hb.HSTU_OK:
+        raise RuntimeError("plan reported a device-side error")
+    c = torch.cumsum(counts[:T].to(torch.int64), 0).cpu().numpy()
+    c = np.concatenate([[0], c])
+    return c[off[1:]] - c[off[:-1]]
+
+
+def rank_sequences(cfg, seed, world, rank, cost=None):
     """This rank's share of the job's batch: (indices into the job's batch,
     their lengths, the batch-wide max_seqlen).
 
     The job's batch is ``cfg.batch * world`` sequences drawn from ``seed``;
-    hstu_attn_shard_sequences splits it by whole sequences (cost L_b^2), so the
-    work per rank stays fixed as the number of ranks grows (weak scaling). N is
-    the batch-wide maximum on every rank: the op's 1/N scale must not depend
-    on the split."""
-    import dataclasses
+    hstu_attn_shard_sequences splits it by whole sequences with the given
+    per-sequence cost (the bench passes each sequence's visible pairs, see
+    job_costs), so the work per rank stays fixed as the number of ranks grows
+    (weak scaling). N is the batch-wide maximum on every rank: the op's 1/N
+    scale must not depend on the split."""
     from jagged_hstu_attention_gb300 import binding as hb
-    from jagged_hstu_attention_gb300 import workloads as wl
-    lens = wl.lengths(dataclasses.replace(cfg, batch=cfg.batch * world), seed)
+    lens = job_lengths(cfg, seed, world)
     if world == 1:
         return np.arange(len(lens)), lens, int(lens.max())
-    owner, _ = hb.shard_sequences(lens * lens, world)
+    if cost is None:
+        raise ValueError("a split over ranks needs each sequence's cost")
+    owner, _ = hb.shard_sequences(np.asarray(cost, dtype=np.int64), world)
     idx = np.nonzero(owner.numpy() == rank)[0]
     return idx, lens[idx], int(lens.max())
 
@@ -380,22 +450,18 @@ def dist_env():
     return ws, rank, local
 
 
-def run_targets(args, cfg, device, world, rank):
-    """Targets-only mode: one candidate row per sequence (its last row,
-    causal: it sees the whole sequence) against full-length K/V, fwd + bwd.
-    HBM-bound: reports achieved bytes/s against the measured copy bandwidth."""
+def measure_targets(k, v, lens, N, steps, warmup, flush, seed):
+    """Targets-only fwd + bwd over a resident batch: one candidate row per
+    sequence (its last row, causal: it sees the whole sequence) against
+    full-length K/V. Returns the timings and the algorithmic bytes."""
     import torch
-    import torch.distributed as dist
     from jagged_hstu_attention_gb300 import binding as hb
     from jagged_hstu_attention_gb300 import workloads as wl
-    seed = args.seed + rank
-    _, lens, N = rank_sequences(cfg, args.seed, world, rank)
+    device = k.device
     off = wl.offsets_from_lengths(lens)
-    T, B, H, D = int(off[-1]), len(lens), cfg.heads, cfg.dim
+    T, B, H, D = int(off[-1]), len(lens), k.shape[1], k.shape[2]
     gen = torch.Generator(device=device)
-    gen.manual_seed(seed)
-    k = wl.randn_bf16((T, H, D), gen, device)
-    v = wl.randn_bf16((T, H, D), gen, device)
+    gen.manual_seed(seed + 1000)
     q_c = wl.randn_bf16((B, H, D), gen, device)
     do_c = wl.randn_bf16((B, H, D), gen, device)
     d_off = torch.tensor(off, dtype=torch.int32, device=device)
@@ -403,8 +469,8 @@ def run_targets(args, cfg, device, world, rank):
     alpha = 1.0 / math.sqrt(D)
     shape = hb.make_shape(B, T, H, D, 1, N, alpha)
     ws = hb.alloc_workspace(shape, hb.WS_TARGETS, device)
-    o_c, dq_c, dk, dv = torch.empty_like(q_c), torch.empty_like(q_c), torch.empty_like(k), torch.empty_like(v)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    o_c, dq_c = torch.empty_like(q_c), torch.empty_like(q_c)
+    dk, dv = torch.empty_like(k), torch.empty_like(v)
 
     def step(ev):
         ev[0].record()
@@ -413,46 +479,68 @@ def run_targets(args, cfg, device, world, rank):
         hb.bwd_targets_only(do_c, q_c, k, v, d_off, fc, N, alpha, ws=ws, outs=(dq_c, dk, dv))
         ev[2].record()
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         step([torch.cuda.Event(enable_timing=True) for _ in range(3)])
     torch.cuda.synchronize()
-    assert hb.device_status(ws) == hb.HSTU_OK
-    sampler = ClockSampler(torch.cuda.current_device())
-    if world > 1:
-        dist.barrier()
-    sampler.start()
+    if hb.device_status(ws) != hb.HSTU_OK:
+        raise RuntimeError("targets-only reported a device-side error")
     recs = []
-    for _ in range(args.steps):
+    for _ in range(steps):
         flush.zero_()
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
         step(ev)
         recs.append(ev)
     torch.cuda.synchronize()
-    clocks = sampler.stop()
     fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in recs)
     bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in recs)
-    ms_local = fwd_ms + bwd_ms
     row = H * D * 2
     bytes_fwd = 2 * T * row + 2 * B * row   # read K, V, q_c; write o_c
     bytes_bwd = 4 * T * row + 3 * B * row   # read K, V, q_c, dO_c; write dK, dV, dq_c
-    ms, job_bytes = reduce_over_ranks(ms_local, float(bytes_fwd + bytes_bwd), device, world)
+    del dk, dv
+    return {"fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "ms": fwd_ms + bwd_ms, "bytes": bytes_fwd + bytes_bwd,
+            "T": T, "B": B, "H": H, "D": D, "launches": 4 * steps}
+
+
+def run_targets(args, cfg, device, world, rank):
+    """Targets-only mode as a line of its own: HBM-bound, reported as
+    achieved bytes/s against the measured copy bandwidth."""
+    import torch
+    import torch.distributed as dist
+    from jagged_hstu_attention_gb300 import workloads as wl
+    seed = args.seed + rank
+    cost = job_costs(cfg, args.seed, world, device) if world > 1 else None
+    _, lens, N = rank_sequences(cfg, args.seed, world, rank, cost)
+    T = int(np.sum(lens))
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    k = wl.randn_bf16((T, cfg.heads, cfg.dim), gen, device)
+    v = wl.randn_bf16((T, cfg.heads, cfg.dim), gen, device)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    sampler = ClockSampler(torch.cuda.current_device())
+    if world > 1:
+        dist.barrier()
+    sampler.start()
+    m = measure_targets(k, v, lens, N, args.steps, args.warmup, flush, seed)
+    clocks = sampler.stop()
+    ms, job_bytes = reduce_over_ranks(m["ms"], float(m["bytes"]), device, world)
     if rank != 0:
         return
+    H, D = cfg.heads, cfg.dim
     useful = float(T) * H * 14 * D          # every key is visible to its candidate
     peaks = load_peaks()
-    gbs = (bytes_fwd + bytes_bwd) / (ms_local * 1e-3) / 1e9
+    gbs = m["bytes"] / (m["ms"] * 1e-3) / 1e9
     line = {
         "metric": "HSTU targets-only fwd+bwd ms and achieved HBM GB/s (% of measured copy bandwidth)",
         "mode": "targets_only", "value": job_bytes / (ms * 1e-3) / 1e9, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": cfg.name + ":targets_only", "batch": B, "global_batch": cfg.batch * world,
+        "config": {"workload": cfg.name + ":targets_only", "batch": len(lens), "global_batch": cfg.batch * world,
                    "total_tokens": T, "heads": H, "head_dim": D, "candidates_per_seq": 1,
                    "parallelism": f"dp{world}" if world > 1 else "single", "l2": "flushed between steps"},
-        "breakdown_ms": {"fwd": fwd_ms, "bwd": bwd_ms},
-        "useful_tflops": useful / (ms_local * 1e-3) / 1e12,
-        "gpu_launches": 4 * args.steps,
+        "breakdown_ms": {"fwd": m["fwd_ms"], "bwd": m["bwd_ms"]},
+        "useful_tflops": useful / (m["ms"] * 1e-3) / 1e12,
+        "gpu_launches": m["launches"],
         "roofline": {"kernel": "tgt_partial_kernel (fwd + bwd)", "bound": "hbm", "achieved": gbs,
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
                      "traffic": None, "peak_source": peaks["source"] + " copy bandwidth"},
@@ -462,29 +550,74 @@ def run_targets(args, cfg, device, world, rank):
 
 
 def run_reference(args, cfg):
-    """The oracle as it stands on the host cores (bounded sample per step)."""
+    """The oracle as it stands on the host cores. Each step is a bounded
+    sample of the workload: one whole sequence, taken in a seeded random
+    order over the batch, all heads, fwd + bwd."""
     world, rank, _ = dist_env()
     if rank != 0:
         return
+    from jagged_hstu_attention_gb300 import workloads as wl
+    lens = wl.lengths(cfg, args.seed)
+    seq_order = np.random.default_rng(args.seed + 77).permutation(len(lens))
     times, flops_all = [], []
-    per_step_budget = 4.0
     for i in range(args.warmup + args.steps):
-        f, s, n, nb = oracle_sample(cfg, args.seed, per_step_budget, max_seqs=1)
+        one = wl.Config(cfg.name, 1, 0, 0, cfg.heads, cfg.dim, cfg.mask, cfg.nfunc, cfg.k1, cfg.k2)
+        f, s, _, _, _ = oracle_sample_lengths(one, [int(lens[seq_order[i % len(lens)]])], int(lens.max()),
+                                              args.seed + i)
         if i >= args.warmup:
             times.append(s)
             flops_all.append(f)
     value = sum(flops_all) / sum(times) / 1e12
+    sample = (f"1 of {cfg.batch} sequences per step (seeded random order over the batch), all heads, "
+              "fwd+bwd, dense fp64 numpy")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(times),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": cfg.name, "batch": cfg.batch, "seq_len": cfg.len_hi,
-                                            "heads": cfg.heads, "head_dim": cfg.dim, "nfunc": cfg.nfunc},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "cpu": cpu_model(),
-                             "kind": "oracle",
-                             "sample": f"1 of {cfg.batch} sequences (the longest) per step, all heads, "
-                                       "fwd+bwd, dense fp64 numpy"},
+            "data": "synthetic", "config": workload_config(cfg, lens, int(np.sum(lens)), 1),
+            "cpu_baseline": cpu_baseline_record(value, sum(times), args.steps, cfg.batch, sample),
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def oracle_sample_lengths(cfg, lens, N, seed):
+    """Times the oracle on sequences of the given lengths (max_seqlen N)."""
+    import torch
+    import oracle.hstu_oracle as orc
+    from jagged_hstu_attention_gb300 import workloads as wl
+    alpha = 1.0 / math.sqrt(cfg.dim)
+    g = torch.Generator().manual_seed(seed)
+    flops, secs, pairs_done = 0.0, 0.0, 0
+    for L in lens:
+        f = wl.func_rows(cfg, L)
+        shape = (L, cfg.heads, cfg.dim)
+        q, k, v, do = (wl.randn_bf16(shape, g).float().numpy().astype(np.float64) for _ in range(4))
+        off = np.array([0, L])
+        t0 = time.perf_counter()
+        orc.fwd_dense(q, k, v, off, f, cfg.nfunc, N, alpha)
+        orc.bwd_dense(do, q, k, v, off, f, cfg.nfunc, N, alpha)
+        secs += time.perf_counter() - t0
+        pairs = int(orc.visible_counts(off, f, cfg.nfunc).sum())
+        pairs_done += pairs
+        flops += pairs * cfg.heads * 14 * cfg.dim
+    return flops, secs, len(lens), len(lens), pairs_done
+
+
+def workload_config(cfg, lens, T, world):
+    return {"workload": cfg.name, "batch": len(lens), "global_batch": cfg.batch * world,
+            "seq_len": cfg.len_hi if cfg.len_lo == cfg.len_hi else f"U[{cfg.len_lo},{cfg.len_hi}]",
+            "heads": cfg.heads, "head_dim": cfg.dim, "nfunc": cfg.nfunc, "mask": cfg.mask, "total_tokens": T,
+            "parallelism": f"dp{world}" if world > 1 else "single", "l2": "flushed between steps"}
+
+
+def bwd_traffic(cfg, T):
+    """DRAM bytes per backward launch for this workload, scaled from the
+    recorded capture by tokens (the backward's traffic is linear in tokens:
+    q, k, v, dO read and dq, dk, dv written once), while the kernel sources
+    are those the capture was taken on; else None."""
+    rec = NCU_TRAFFIC.get(cfg.mask)
+    if rec is None or rec["sources_sha"] != kernel_sources_sha():
+        return None, None
+    return rec["bytes_per_token"] * T, rec["captured_on"]
 
 
 def main():
@@ -498,6 +631,8 @@ def main():
                     help="override the workload's batch size (small profiling cases only)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="time the main workload only (no padding / targets-only / e2e sub-measurements)")
     ap.add_argument("--mode", default="full", choices=["full", "targets"],
                     help="full: plan + fwd + bwd over every row; targets: targets-only fwd + bwd")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
@@ -531,13 +666,15 @@ def main():
         return
 
     # Each rank runs its share of a batch of cfg.batch * world sequences (whole
-    # sequences, split longest-first); no data-path collective; weak scaling.
-    # Activations are drawn from seed + rank.
+    # sequences, split by visible pairs); no data-path collective; weak
+    # scaling. Activations are drawn from seed + rank.
     seed = args.seed + rank
-    _, lens, n_max = rank_sequences(cfg, args.seed, world, rank)
+    cost = job_costs(cfg, args.seed, world, device) if world > 1 else None
+    _, lens, n_max = rank_sequences(cfg, args.seed, world, rank, cost)
     leg_main = Leg(cfg, seed, cfg.nfunc, device, lens=lens, max_seqlen=n_max)
     legs = [leg_main]
-    if cfg.mask == "sla" and cfg.nfunc == 5:
+    padding_inline = cfg.mask == "sla" and cfg.nfunc == 5
+    if padding_inline:
         legs.append(Leg(cfg, seed, 3, device, shared=leg_main))
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
 
@@ -561,9 +698,21 @@ def main():
     ms_max, job_useful = reduce_over_ranks(ms_step, useful, device, world)
     value = job_useful / (ms_max * 1e-3) / 1e12
 
-    e2e_ms, h2d, d2h = e2e_leg(leg_main, max(3, args.steps // 2), 2)
-    e2e_max, _ = reduce_over_ranks(e2e_ms, useful, device, world)
-    e2e_val = job_useful / (e2e_max * 1e-3) / 1e12
+    extras = {}
+    if not args.no_extras:
+        e2e_ms, h2d, d2h = e2e_leg(leg_main, max(3, args.steps // 2), 2)
+        e2e_max, _ = reduce_over_ranks(e2e_ms, useful, device, world)
+        extras["e2e"] = {"value": job_useful / (e2e_max * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                         "d2h_bytes_per_step": d2h, "ms_per_step": e2e_max}
+        torch.cuda.empty_cache()
+        if rank == 0 and cfg.mask == "causal":
+            extras["targets"] = measure_targets(leg_main.k, leg_main.v, leg_main.lens, leg_main.N, args.steps,
+                                                args.warmup, flush, seed)
+        if rank == 0 and not padding_inline:
+            pcfg = wl.CONFIGS[PADDING_CONFIG]
+            p5 = Leg(pcfg, args.seed, 5, device)
+            p3 = Leg(pcfg, args.seed, 3, device, shared=p5)
+            extras["padding"] = (time_legs([p5, p3], max(args.steps, 20), args.warmup, flush), p5)
 
     if rank != 0:
         if world > 1:
@@ -572,52 +721,76 @@ def main():
 
     peaks = load_peaks()
     ms_bwd = statistics.mean(r["bwd"])
+    ms_fwd = statistics.mean(r["fwd"])
     achieved = f_bwd / (ms_bwd * 1e-3) / 1e12
-    sha = kernel_sources_sha()
-    # The recorded bytes are those of one launch on the default workload only
-    # (equal-length sequences, so every rank's share is that same launch).
-    same_workload = args.config == DEFAULT_CONFIG and args.batch is None
-    traffic = NCU_TRAFFIC["bwd"] if NCU_TRAFFIC["sources_sha"] == sha and same_workload else None
+    traffic, traffic_src = bwd_traffic(cfg, leg_main.T)
+    launches = LAUNCHES_PER_STEP * args.steps * len(legs)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": cfg.name, "batch": len(lens), "global_batch": cfg.batch * world, "seq_len": cfg.len_hi if cfg.len_lo == cfg.len_hi
-                   else f"U[{cfg.len_lo},{cfg.len_hi}]", "heads": cfg.heads, "head_dim": cfg.dim,
-                   "nfunc": cfg.nfunc, "mask": cfg.mask, "total_tokens": leg_main.T,
-                   "parallelism": f"dp{world}" if world > 1 else "single", "l2": "flushed between steps"},
+        "config": workload_config(cfg, lens, leg_main.T, world),
         "pct_of_bf16_peak": 100.0 * value / world / peaks["bf16_tflops"],
         "breakdown_ms": {k: statistics.mean(r[k]) for k in ("plan", "fwd", "bwd")},
         "step_ms_stats": {"mean": ms_step, "median": statistics.median(r["step"]), "min": min(r["step"]),
                           "max": max(r["step"])},
         "useful_gflop_per_step": useful / 1e9,
-        "gpu_launches": LAUNCHES_PER_STEP * args.steps * len(legs),
+        "gpu_launches": launches,
         "roofline": {"kernel": "hstu_bwd_kernel", "bound": "tensor", "achieved": achieved,
                      "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": achieved / peaks["bf16_tflops"], "traffic": traffic,
-                     "peak_source": peaks["source"] + " burst bf16"},
-        "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_max},
+                     "traffic_basis": traffic_src,
+                     "algorithmic_bytes": 7 * leg_main.T * cfg.heads * cfg.dim * 2 + 4 * cfg.nfunc * leg_main.T,
+                     "peak_source": peaks["source"] + " burst bf16",
+                     "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
+                     "fwd": {"kernel": "hstu_fwd_kernel", "achieved": f_fwd / (ms_fwd * 1e-3) / 1e12,
+                             "frac": f_fwd / (ms_fwd * 1e-3) / 1e12 / peaks["bf16_tflops"]}},
         "clocks": clocks,
         "wall_s_timed_region": wall,
     }
+    if "e2e" in extras:
+        line["e2e"] = extras["e2e"]
     if len(legs) > 1:
-        ms3 = statistics.mean(res[1]["step"])
-        med5, med3 = statistics.median(r["step"]), statistics.median(res[1]["step"])
-        line["nfunc3"] = {"ms_per_step": ms3, "breakdown_ms": {k: statistics.mean(res[1][k])
-                                                               for k in ("plan", "fwd", "bwd")},
-                          "median_ms_per_step": {"nfunc5": med5, "nfunc3": med3},
-                          "padding_overhead_pct": 100.0 * (med5 - med3) / med3,
-                          "padding_overhead_basis": "medians over the timed steps; legs alternate order"}
+        line["padding"] = padding_record(res, legs[1], PADDING_CONFIG if args.config == PADDING_CONFIG else cfg.name)
+    elif "padding" in extras:
+        pres, p5 = extras["padding"]
+        line["padding"] = padding_record(pres, p5, PADDING_CONFIG)
+    if "targets" in extras:
+        m = extras["targets"]
+        gbs = m["bytes"] / (m["ms"] * 1e-3) / 1e9
+        line["targets_only"] = {
+            "workload": cfg.name + ":targets_only", "ms_per_step": m["ms"],
+            "breakdown_ms": {"fwd": m["fwd_ms"], "bwd": m["bwd_ms"]}, "achieved_gbs": gbs,
+            "hbm_frac": gbs / peaks["hbm_gbs"], "peak_gbs": peaks["hbm_gbs"],
+            "speedup_vs_full_step": ms_step / m["ms"], "candidates_per_seq": 1,
+            "algorithmic_bytes": m["bytes"], "gpu_launches": m["launches"]}
     if not args.no_cpu_baseline:
-        f, s, n, nb = oracle_sample(cfg, seed, args.cpu_budget)
-        line["cpu_baseline"] = {"value": f / s / 1e12, "unit": UNIT, "cores": cpu_cores(), "cpu": cpu_model(),
-                                "kind": "oracle",
-                                "sample": f"{n} of {nb} sequences (longest first), all heads, fwd+bwd, "
-                                          f"dense fp64 numpy, {s:.1f} s"}
+        f, s, n, nb, pairs = oracle_sample(cfg, seed, args.cpu_budget,
+                                           order="random" if cfg.batch > 64 else "longest")
+        full_s = s * leg_main.pairs / max(pairs, 1)
+        sample = (f"{n} of {nb} sequences ({'seeded random order' if cfg.batch > 64 else 'longest first'}), "
+                  f"all heads, fwd+bwd, dense fp64 numpy, {s:.1f} s")
+        extra = None
+        if n < nb:
+            extra = {"extrapolated_full_step_s": full_s,
+                     "extrapolation": "sample time x (visible pairs of the batch / visible pairs of the sample)"}
+        line["cpu_baseline"] = cpu_baseline_record(f / s / 1e12, s, n, nb, sample, extra)
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def padding_record(res, leg, workload):
+    r5, r3 = res[0], res[1]
+    med5, med3 = statistics.median(r5["step"]), statistics.median(r3["step"])
+    return {"workload": workload, "ms_per_step": {"nfunc5": statistics.mean(r5["step"]),
+                                                  "nfunc3": statistics.mean(r3["step"])},
+            "breakdown_ms": {"nfunc5": {k: statistics.mean(r5[k]) for k in ("plan", "fwd", "bwd")},
+                             "nfunc3": {k: statistics.mean(r3[k]) for k in ("plan", "fwd", "bwd")}},
+            "median_ms_per_step": {"nfunc5": med5, "nfunc3": med3},
+            "padding_overhead_pct": 100.0 * (med5 - med3) / med3,
+            "useful_tflops_nfunc5": sum(leg.flops()) / (med5 * 1e-3) / 1e12,
+            "padding_overhead_basis": "medians over the timed steps; legs alternate order"}
 
 
 if __name__ == "__main__":

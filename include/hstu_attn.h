@@ -23,9 +23,12 @@
  *   that row of the full op.
  *
  * Conventions (all entry points):
- *   - q, k, v, o, dout, dq, dk, dv: DEVICE pointers, bf16, contiguous
- *     (tokens, num_heads, head_dim); row stride num_heads*head_dim elements.
- *     Base addresses must be 16-byte aligned.
+ *   - q, k, v, o, dout, dq, dk, dv: DEVICE pointers, all bf16 or all fp16
+ *     (shape->dtype), contiguous (tokens, num_heads, width): q, k, dq, dk are
+ *     head_dim (D_qk) wide, v, o, dout, dv head_dim_v (D_v) wide. Products run
+ *     on the tensor cores in the input type with fp32 accumulation; P and dS
+ *     are rounded to the input type before their MMAs. Base addresses must be
+ *     16-byte aligned.
  *   - seq_offsets: DEVICE int32 (batch+1), seq_offsets[0] = 0, non-decreasing,
  *     seq_offsets[batch] = total, every length <= max_seqlen.
  *   - func: DEVICE int32 (nfunc, total), shared by all heads (read once per
@@ -65,21 +68,29 @@ extern "C" {
 typedef enum {
   HSTU_OK = 0,
   HSTU_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misaligned pointer */
-  HSTU_ERR_UNSUPPORTED = 2,  /* nfunc or head_dim the library has no kernel for */
+  HSTU_ERR_UNSUPPORTED = 2,  /* nfunc, head dims or dtype the library has no kernel for */
   HSTU_ERR_WORKSPACE = 3,    /* workspace null, too small or misaligned */
   HSTU_ERR_CUDA = 4,         /* a CUDA runtime call failed (launch, sync) */
   HSTU_ERR_DEVICE_INPUT = 5, /* device-side input check failed (offsets) */
   HSTU_ERR_TIMEOUT = 6       /* a bounded in-kernel wait gave up */
 } hstu_status_t;
 
+/* Input and output element types (all tensors of a call share one). */
+#define HSTU_DTYPE_BF16 0
+#define HSTU_DTYPE_F16 1
+
 typedef struct {
   int32_t batch;      /* B, number of sequences (>= 1) */
   int64_t total;      /* T = seq_offsets[B], rows of k and v (and of q, o) */
   int32_t num_heads;  /* H >= 1 */
-  int32_t head_dim;   /* D = D_qk = D_v, one of 32, 64, 128 */
+  int32_t head_dim;   /* D_qk, width of q and k rows (and dq, dk): 32, 64 or 128 */
   int32_t nfunc;      /* rows of func: odd, 1 to 9 */
   int32_t max_seqlen; /* N: >= every L_b, <= 32768; also the 1/N scale */
   float alpha;        /* scale on q.k, usually 1/sqrt(head_dim) */
+  int32_t head_dim_v; /* D_v, width of v, o, dout and dv rows: 32, 64 or 128;
+                         0 means D_v = D_qk (the attention dim and the linear
+                         dim of an HSTU layer may differ) */
+  int32_t dtype;      /* HSTU_DTYPE_BF16 (0) or HSTU_DTYPE_F16 (1) */
 } hstu_attn_shape_t;
 
 /* Workspace modes for hstu_attn_workspace_size. */
@@ -145,6 +156,68 @@ HSTU_API hstu_status_t hstu_attn_bwd_targets_only(const void* dout_c, const void
                                          const hstu_attn_shape_t* shape, void* ws,
                                          size_t ws_bytes, void* stream);
 
+/* Several candidates per sequence (MLCommons training PR #903, Gating: the
+ * targets-only rewrite must cope with batches that are not exactly one target
+ * per sequence). Candidates cand_offsets[b] .. cand_offsets[b+1] of q_c belong
+ * to sequence b; each has its own func column and sees the full-length K/V of
+ * its sequence. A sequence may have none.
+ *   q_c      DEVICE (num_candidates, H, D_qk); o_c (num_candidates, H, D_v)
+ *   cand_offsets  DEVICE int32 (batch+1): 0, non-decreasing, last =
+ *            num_candidates (checked on the device: HSTU_ERR_DEVICE_INPUT)
+ *   func_c   DEVICE int32 (nfunc, num_candidates)
+ *   ws       at least hstu_attn_targets_workspace_size(shape, num_candidates)
+ * The backward writes dq_c (num_candidates, H, D_qk) and every row of dk, dv
+ * (total, H, ...): each key row sums its sequence's candidates in candidate
+ * order, once, without atomics (bitwise repeatable); rows no candidate sees
+ * are zero. */
+HSTU_API size_t hstu_attn_targets_workspace_size(const hstu_attn_shape_t* shape, int64_t num_candidates);
+HSTU_API hstu_status_t hstu_attn_fwd_targets(const void* q_c, const void* k, const void* v, void* o_c,
+                                             const int32_t* seq_offsets, const int32_t* cand_offsets,
+                                             int64_t num_candidates, const int32_t* func_c,
+                                             const hstu_attn_shape_t* shape, void* ws, size_t ws_bytes,
+                                             void* stream);
+HSTU_API hstu_status_t hstu_attn_bwd_targets(const void* dout_c, const void* q_c, const void* k, const void* v,
+                                             void* dq_c, void* dk, void* dv, const int32_t* seq_offsets,
+                                             const int32_t* cand_offsets, int64_t num_candidates,
+                                             const int32_t* func_c, const hstu_attn_shape_t* shape, void* ws,
+                                             size_t ws_bytes, void* stream);
+
+/* Candidate-row projection of the targets-only layer (MLCommons training PR
+ * #903, Summary: the last layer computes U and Q for the candidate rows
+ * alone; K and V stay full length). The pages leave the projection itself
+ * open; it is read as the layer's pointwise-SiLU input projection of a row,
+ *     y = silu(x w^T + bias),  z = x w^T + bias,
+ * evaluated on the listed rows of x only. GEMMs run on the tensor cores in
+ * the input type with fp32 accumulation; y, z and the gradients are rounded
+ * to the input type.
+ *   x      DEVICE (x_rows, d_in); rows DEVICE int32 (num_rows) row indices
+ *          into x, or NULL for all rows in order (num_rows = x_rows)
+ *   w      DEVICE (d_out, d_in) (out features, in features); bias DEVICE
+ *          (d_out) or NULL
+ *   y, z   DEVICE (num_rows, d_out), written; z may be NULL (the backward
+ *          needs it)
+ *   d_in, d_out  multiples of 64; dtype HSTU_DTYPE_BF16 or HSTU_DTYPE_F16
+ *          for every tensor
+ *   ws     DEVICE, hstu_attn_project_workspace_size(rows ? num_rows : 0,
+ *          d_in, d_out, 0) bytes, 256-byte aligned
+ * A row index outside [0, x_rows) sets HSTU_ERR_DEVICE_INPUT in ws's error
+ * word (read with hstu_attn_get_device_status) and gives a zero input row. */
+HSTU_API size_t hstu_attn_project_workspace_size(int64_t num_rows, int32_t d_in, int32_t d_out, int32_t backward);
+HSTU_API hstu_status_t hstu_attn_project_rows(const void* x, int64_t x_rows, const int32_t* rows, int64_t num_rows,
+                                              const void* w, const void* bias, int32_t d_in, int32_t d_out,
+                                              int32_t dtype, void* y, void* z, void* ws, size_t ws_bytes,
+                                              void* stream);
+/* Backward of sum(y * dy) for hstu_attn_project_rows: dx_rows (num_rows,
+ * d_in) is the gradient of each listed row of x (a caller adds it into its
+ * dx at those rows), dw (d_out, d_in) and dbias (d_out, nullable) are
+ * written. z is the forward's pre-activation. dbias sums the rows in a fixed
+ * order (deterministic). ws: hstu_attn_project_workspace_size(num_rows, d_in,
+ * d_out, 1) bytes. */
+HSTU_API hstu_status_t hstu_attn_project_rows_bwd(const void* dy, const void* z, const void* x, int64_t x_rows,
+                                                  const int32_t* rows, int64_t num_rows, const void* w,
+                                                  int32_t d_in, int32_t d_out, int32_t dtype, void* dx_rows,
+                                                  void* dw, void* dbias, void* ws, size_t ws_bytes, void* stream);
+
 /* Scratch capacity of hstu_attn_fwd_noalloc, in bytes (8 MiB). */
 #define HSTU_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
 
@@ -161,8 +234,11 @@ HSTU_API hstu_status_t hstu_attn_bwd_targets_only(const void* dout_c, const void
  *     hstu_attn_workspace_size with HSTU_WS_FULL) returns HSTU_ERR_WORKSPACE
  *     and enqueues nothing.
  *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     (cudaGetSymbolAddress) with that device current, and caches it for that
+ *     device's current CUDA context; make that first call before any stream
+ *     capture. A context rebuilt later (after cudaDeviceReset) is a new one:
+ *     its first call looks the address up again, so make it outside a
+ *     capture too.
  *   - No cudaMalloc, cudaFree or allocating library routine is called.
  *   - All calls on a device share the array, which keeps the last call's
  *     contents; each call clears what must start at zero. Calls whose work
@@ -175,6 +251,58 @@ HSTU_API hstu_status_t hstu_attn_fwd_noalloc(const void* q, const void* k, const
                                              const int32_t* seq_offsets, const int32_t* func,
                                              const hstu_attn_shape_t* shape, int32_t* row_counts,
                                              void* stream);
+
+/* Mask families whose func the library can build on the device. */
+typedef enum {
+  HSTU_FUNC_CAUSAL = 0,  /* row i: [0, i+1) (MLCommons training PR #903: causal,
+                            one candidate at the end of each sequence) */
+  HSTU_FUNC_SLA = 1,     /* TorchEasyRec PR #670, build_sla_func_tensor: a global
+                            prefix [0, min(k1, i+1)) and a causal window
+                            [max(0, i-k2+1), i+1) */
+  HSTU_FUNC_ONERANK = 2  /* TorchEasyRec PR #670, OneRank: history prefix,
+                            candidate and task-token intervals (see below) */
+} hstu_func_kind_t;
+
+typedef struct {
+  int32_t kind;        /* hstu_func_kind_t */
+  int32_t k1, k2;      /* SLA: prefix and window widths, >= 0 */
+  int32_t groups;      /* OneRank: candidate groups at the end of a sequence, >= 1 */
+  int32_t task_tokens; /* OneRank: task tokens per group, >= 1 */
+} hstu_func_spec_t;
+
+/* Builds func (nfunc, total) on the device for a mask family, so that it is
+ * never assembled on the host (the pages build it on the host and, in the
+ * reference wheel, once per head; TorchEasyRec PR #670, PR body). One thread
+ * writes one row; the values are local column bounds as func expects.
+ *   - CAUSAL:  row i -> [i+1, i+1, ...]: interval 0 = [0, i+1), the rest empty.
+ *   - SLA:     row i -> [min(k1, i+1), max(0, i-k2+1), i+1, i+1, ...]; the
+ *              padded intervals repeat the window end (empty). nfunc >= 3.
+ *   - ONERANK: each sequence ends in `groups` groups of 1 + task_tokens rows
+ *              after a history of Lp = L - groups (1 + task_tokens) rows. Group
+ *              g opens with its candidate e_g = Lp + g (1 + task_tokens). A
+ *              history row i -> [i+1, e, e+1, t, t+1] with e = e_(i mod groups)
+ *              and t = e + 1 + (i mod task_tokens) (its prefix, a candidate and
+ *              one of that candidate's task tokens); a group row r of group g
+ *              -> [Lp, e_g, e_g+1, r, r+1] (the history, its candidate, itself).
+ *              Sequences with Lp <= 0 get causal rows. nfunc >= 5; rows past
+ *              the fifth repeat the fifth (empty).
+ * Arguments: seq_offsets DEVICE int32 (batch+1); total = seq_offsets[batch];
+ * max_seqlen >= every length (rows of a longer sequence past max_seqlen are
+ * not written); func DEVICE int32 (nfunc, total), written. A sequence whose
+ * offsets are out of order or out of [0, total] is skipped (the plan reports
+ * such offsets). Returns HSTU_ERR_INVALID_ARG for null or misaligned
+ * pointers, bad sizes or spec values, HSTU_ERR_UNSUPPORTED for an nfunc the
+ * family cannot fill; nothing is enqueued then. */
+HSTU_API hstu_status_t hstu_attn_build_func(const hstu_func_spec_t* spec, const int32_t* seq_offsets,
+                                            int32_t batch, int64_t total, int32_t max_seqlen, int32_t nfunc,
+                                            int32_t* func, void* stream);
+
+/* Builds func_c (nfunc, batch) for the targets-only entry points on the
+ * device: the candidate of sequence b is its last row and sees [0, L_b);
+ * every further interval repeats L_b (empty). seq_offsets DEVICE int32
+ * (batch+1); func_c DEVICE int32, written. */
+HSTU_API hstu_status_t hstu_attn_build_func_candidates(const int32_t* seq_offsets, int32_t batch, int32_t nfunc,
+                                                       int32_t* func_c, void* stream);
 
 /* Synchronises the stream, then returns the status recorded in the
  * workspace error word (HSTU_OK, HSTU_ERR_DEVICE_INPUT, HSTU_ERR_TIMEOUT) or

@@ -19,7 +19,7 @@ BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_NAME = "libhstu_attn.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
 
-SOURCES = ["plan.cu", "attn_fwd.cu", "attn_bwd.cu", "targets_only.cu", "api.cu", "noalloc.cu", "selftest.cu",
+SOURCES = ["plan.cu", "attn_fwd_bf16.cu", "attn_fwd_f16.cu", "attn_bwd_bf16.cu", "attn_bwd_f16.cu", "targets_only.cu", "api.cu", "noalloc.cu", "selftest.cu", "func_build.cu", "project.cu",
            "shard.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",

@@ -3,7 +3,9 @@
 // Nothing here allocates device memory or synchronises, except
 // hstu_attn_get_device_status.
 #include <cudaTypedefs.h>
+#include <nvtx3/nvToolsExt.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "../../include/hstu_attn.h"
@@ -14,7 +16,20 @@ namespace {
 
 using hstu::kBlock;
 
+// NVTX range around one entry point's host work (checks, tensor maps and the
+// launches it enqueues), so a profiler timeline shows which call issued
+// which kernels. NVTX is header-only and does nothing unless a tool is
+// attached.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
+
 bool aligned(const void* ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
+
+bool dim_ok(int d) { return d == 32 || d == 64 || d == 128; }
 
 hstu_status_t check_shape(const hstu_attn_shape_t* s) {
   if (!s) return HSTU_ERR_INVALID_ARG;
@@ -24,10 +39,14 @@ hstu_status_t check_shape(const hstu_attn_shape_t* s) {
   if (s->max_seqlen > hstu::kMaxSeqlen) return HSTU_ERR_UNSUPPORTED;
   if (s->batch > (1 << 22) - 1) return HSTU_ERR_UNSUPPORTED;  // work-list encoding
   if (!hstu_attn_nfunc_supported(s->nfunc)) return HSTU_ERR_UNSUPPORTED;
-  if (s->head_dim != 32 && s->head_dim != 64 && s->head_dim != 128) return HSTU_ERR_UNSUPPORTED;
+  if (!dim_ok(s->head_dim) || (s->head_dim_v != 0 && !dim_ok(s->head_dim_v))) return HSTU_ERR_UNSUPPORTED;
+  if (s->dtype != HSTU_DTYPE_BF16 && s->dtype != HSTU_DTYPE_F16) return HSTU_ERR_UNSUPPORTED;
   if (!(s->alpha == s->alpha)) return HSTU_ERR_INVALID_ARG;  // NaN
   return HSTU_OK;
 }
+
+// D_v of a shape (0 stands for D_v = D_qk).
+int dim_v(const hstu_attn_shape_t* s) { return s->head_dim_v != 0 ? s->head_dim_v : s->head_dim; }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -43,13 +62,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// (tokens, H, D) bf16 viewed as a 4-D tensor {64 columns, tokens, H, D / 64
+// (tokens, H, D) 16-bit elements viewed as a 4-D tensor {64 columns, tokens, H, D / 64
 // chunks} with the chunk stride (128 B) below the row stride. One box of
 // 64 columns x box_rows rows x 1 head x all chunks, with 128-byte swizzle,
 // lands in shared memory as [chunk][row][128 B]: the K-major layout of the
 // kernels' UMMA descriptors, in one TMA instruction per tile. For D = 32 the
 // box is wider than the tensor and TMA fills the missing columns with zeros.
-bool make_map(CUtensorMap* m, const void* ptr, int64_t tokens, int heads, int dim,
+bool make_map(CUtensorMap* m, const void* ptr, int64_t tokens, int heads, int dim, int dtype,
               int box_rows = kBlock) {
   auto fn = encode_fn();
   if (!fn) return false;
@@ -59,7 +78,9 @@ bool make_map(CUtensorMap* m, const void* ptr, int64_t tokens, int heads, int di
   cuuint64_t strides[3] = {static_cast<cuuint64_t>(heads) * dim * 2, static_cast<cuuint64_t>(dim) * 2, 128};
   cuuint32_t box[4] = {64, static_cast<cuuint32_t>(box_rows), 1, static_cast<cuuint32_t>(chunks)};
   cuuint32_t es[4] = {1, 1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, es,
+  const CUtensorMapDataType type =
+      dtype == HSTU_DTYPE_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  return fn(m, type, 4, const_cast<void*>(ptr), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -129,15 +150,14 @@ int hstu_attn_nfunc_supported(int32_t nfunc) {
 size_t hstu_attn_workspace_size(const hstu_attn_shape_t* shape, int32_t mode) {
   if (check_shape(shape) != HSTU_OK) return 0;
   if (mode == HSTU_WS_FULL) return hstu::full_layout(shape->batch, shape->max_seqlen).total;
-  if (mode == HSTU_WS_TARGETS)
-    return hstu::targets_layout(shape->batch, shape->num_heads, shape->head_dim, shape->max_seqlen)
-        .total;
+  if (mode == HSTU_WS_TARGETS) return hstu_attn_targets_workspace_size(shape, shape->batch);
   return 0;
 }
 
 hstu_status_t hstu_attn_plan(const int32_t* seq_offsets, const int32_t* func,
                              const hstu_attn_shape_t* shape, int32_t* row_counts, void* ws,
                              size_t ws_bytes, void* stream) {
+  NvtxRange nvtx("hstu_attn_plan");
   hstu_status_t st = check_common(seq_offsets, func, shape, ws, ws_bytes);
   if (st != HSTU_OK) return st;
   if (row_counts && !aligned(row_counts, 4)) return HSTU_ERR_INVALID_ARG;
@@ -148,6 +168,7 @@ hstu_status_t hstu_attn_fwd(const void* q, const void* k, const void* v, void* o
                             const int32_t* seq_offsets, const int32_t* func,
                             const hstu_attn_shape_t* shape, int32_t* row_counts, void* ws,
                             size_t ws_bytes, uint32_t flags, void* stream) {
+  NvtxRange nvtx("hstu_attn_fwd");
   hstu_status_t st = check_common(seq_offsets, func, shape, ws, ws_bytes);
   if (st != HSTU_OK) return st;
   if (shape->total > 0 && !(tensor_ok(q) && tensor_ok(k) && tensor_ok(v) && tensor_ok(o)))
@@ -162,32 +183,35 @@ hstu_status_t hstu_attn_fwd(const void* q, const void* k, const void* v, void* o
   const hstu::FullLayout l = hstu::full_layout(shape->batch, shape->max_seqlen);
   uint8_t* base = static_cast<uint8_t*>(ws);
   hstu::AttnParams p{};
-  if (!make_map(&p.tm_q, q, shape->total, shape->num_heads, shape->head_dim) ||
-      !make_map(&p.tm_k, k, shape->total, shape->num_heads, shape->head_dim) ||
-      !make_map(&p.tm_v, v, shape->total, shape->num_heads, shape->head_dim))
+  const int T = static_cast<int>(shape->total), H = shape->num_heads, Dq = shape->head_dim, Dv = dim_v(shape);
+  const int dt = shape->dtype;
+  if (!make_map(&p.tm_q, q, T, H, Dq, dt) || !make_map(&p.tm_k, k, T, H, Dq, dt) ||
+      !make_map(&p.tm_v, v, T, H, Dv, dt))
     return HSTU_ERR_CUDA;
   p.tm_do = p.tm_q;
   p.seq_offsets = seq_offsets;
   p.func = func;
-  p.out0 = static_cast<__nv_bfloat16*>(o);
+  p.out0 = o;
   p.cls = base + l.cls;
   p.ivmask = base + l.ivmask;
   p.list = reinterpret_cast<const int32_t*>(base + l.fwd_list);
   p.header = reinterpret_cast<int32_t*>(base + l.header);
   p.total = shape->total;
   p.heads = shape->num_heads;
-  p.dim = shape->head_dim;
+  p.dim = Dq;
+  p.dim_v = Dv;
   p.nt = l.nt;
   p.max_seqlen = shape->max_seqlen;
   p.alpha = shape->alpha;
   p.inv_n = 1.0f / static_cast<float>(shape->max_seqlen);
-  return from_cuda(hstu::launch_fwd(p, (shape->nfunc + 1) / 2, grid_items(shape, l.nt), cs));
+  return from_cuda(hstu::launch_fwd(p, (shape->nfunc + 1) / 2, dt, grid_items(shape, l.nt), cs));
 }
 
 hstu_status_t hstu_attn_bwd(const void* dout, const void* q, const void* k, const void* v,
                             void* dq, void* dk, void* dv, const int32_t* seq_offsets,
                             const int32_t* func, const hstu_attn_shape_t* shape, void* ws,
                             size_t ws_bytes, uint32_t flags, void* stream) {
+  NvtxRange nvtx("hstu_attn_bwd");
   hstu_status_t st = check_common(seq_offsets, func, shape, ws, ws_bytes);
   if (st != HSTU_OK) return st;
   if (shape->total > 0 && !(tensor_ok(dout) && tensor_ok(q) && tensor_ok(k) && tensor_ok(v) &&
@@ -202,61 +226,66 @@ hstu_status_t hstu_attn_bwd(const void* dout, const void* q, const void* k, cons
   const hstu::FullLayout l = hstu::full_layout(shape->batch, shape->max_seqlen);
   uint8_t* base = static_cast<uint8_t*>(ws);
   hstu::AttnParams p{};
-  if (!make_map(&p.tm_q, q, shape->total, shape->num_heads, shape->head_dim) ||
-      !make_map(&p.tm_k, k, shape->total, shape->num_heads, shape->head_dim) ||
-      !make_map(&p.tm_v, v, shape->total, shape->num_heads, shape->head_dim) ||
-      !make_map(&p.tm_do, dout, shape->total, shape->num_heads, shape->head_dim) ||
-      !make_map(&p.tm_q64, q, shape->total, shape->num_heads, shape->head_dim, kBlock / 2) ||
-      !make_map(&p.tm_k64, k, shape->total, shape->num_heads, shape->head_dim, kBlock / 2) ||
-      !make_map(&p.tm_v64, v, shape->total, shape->num_heads, shape->head_dim, kBlock / 2) ||
-      !make_map(&p.tm_do64, dout, shape->total, shape->num_heads, shape->head_dim, kBlock / 2))
+  const int T = static_cast<int>(shape->total), H = shape->num_heads, Dq = shape->head_dim, Dv = dim_v(shape);
+  const int dt = shape->dtype;
+  // q, k (and dq, dk) are D_qk wide; v and dout (and dv) D_v wide.
+  if (!make_map(&p.tm_q, q, T, H, Dq, dt) || !make_map(&p.tm_k, k, T, H, Dq, dt) ||
+      !make_map(&p.tm_v, v, T, H, Dv, dt) || !make_map(&p.tm_do, dout, T, H, Dv, dt) ||
+      !make_map(&p.tm_q64, q, T, H, Dq, dt, kBlock / 2) || !make_map(&p.tm_k64, k, T, H, Dq, dt, kBlock / 2) ||
+      !make_map(&p.tm_v64, v, T, H, Dv, dt, kBlock / 2) || !make_map(&p.tm_do64, dout, T, H, Dv, dt, kBlock / 2))
     return HSTU_ERR_CUDA;
   p.seq_offsets = seq_offsets;
   p.func = func;
-  p.out0 = static_cast<__nv_bfloat16*>(dq);
-  p.out1 = static_cast<__nv_bfloat16*>(dk);
-  p.out2 = static_cast<__nv_bfloat16*>(dv);
+  p.out0 = dq;
+  p.out1 = dk;
+  p.out2 = dv;
   p.cls = base + l.cls;
   p.ivmask = base + l.ivmask;
   p.list = reinterpret_cast<const int32_t*>(base + l.bwd_list);
   p.header = reinterpret_cast<int32_t*>(base + l.header);
   p.total = shape->total;
   p.heads = shape->num_heads;
-  p.dim = shape->head_dim;
+  p.dim = Dq;
+  p.dim_v = Dv;
   p.nt = l.nt;
   p.max_seqlen = shape->max_seqlen;
   p.alpha = shape->alpha;
   p.inv_n = 1.0f / static_cast<float>(shape->max_seqlen);
-  return from_cuda(hstu::launch_bwd(p, (shape->nfunc + 1) / 2, grid_items(shape, l.nt), cs));
+  return from_cuda(hstu::launch_bwd(p, (shape->nfunc + 1) / 2, dt, grid_items(shape, l.nt), cs));
 }
 
 static hstu_status_t targets_common(const void* q_c, const void* k, const void* v,
-                                    const int32_t* seq_offsets, const int32_t* func_c,
-                                    const hstu_attn_shape_t* shape, void* ws, size_t ws_bytes,
-                                    hstu::TgtParams* p) {
+                                    const int32_t* seq_offsets, const int32_t* cand_offsets, int64_t num_cand,
+                                    const int32_t* func_c, const hstu_attn_shape_t* shape, void* ws,
+                                    size_t ws_bytes, hstu::TgtParams* p) {
   hstu_status_t st = check_shape(shape);
   if (st != HSTU_OK) return st;
-  if (!seq_offsets || !func_c || !aligned(seq_offsets, 4) || !aligned(func_c, 4))
+  if (num_cand < 0 || num_cand > INT32_MAX) return HSTU_ERR_INVALID_ARG;
+  if (!seq_offsets || (num_cand > 0 && !func_c) || !aligned(seq_offsets, 4) || !aligned(func_c, 4) ||
+      !aligned(cand_offsets, 4))
     return HSTU_ERR_INVALID_ARG;
-  if (!tensor_ok(q_c) || (shape->total > 0 && !(tensor_ok(k) && tensor_ok(v))))
+  if ((num_cand > 0 && !tensor_ok(q_c)) || (shape->total > 0 && !(tensor_ok(k) && tensor_ok(v))))
     return HSTU_ERR_INVALID_ARG;
-  st = check_ws(ws, ws_bytes, hstu_attn_workspace_size(shape, HSTU_WS_TARGETS));
+  st = check_ws(ws, ws_bytes, hstu_attn_targets_workspace_size(shape, num_cand));
   if (st != HSTU_OK) return st;
-  const hstu::TargetsLayout l =
-      hstu::targets_layout(shape->batch, shape->num_heads, shape->head_dim, shape->max_seqlen);
+  const hstu::TargetsLayout l = hstu::targets_layout(static_cast<int>(num_cand), shape->num_heads,
+                                                     std::max(shape->head_dim, dim_v(shape)), shape->max_seqlen);
   uint8_t* base = static_cast<uint8_t*>(ws);
   *p = hstu::TgtParams{};
-  p->q_c = static_cast<const __nv_bfloat16*>(q_c);
-  p->k = static_cast<const __nv_bfloat16*>(k);
-  p->v = static_cast<const __nv_bfloat16*>(v);
+  p->q_c = q_c;
+  p->k = k;
+  p->v = v;
   p->seq_offsets = seq_offsets;
+  p->cand_offsets = cand_offsets;
   p->func_c = func_c;
   p->partial = reinterpret_cast<float*>(base + l.partial);
   p->header = reinterpret_cast<int32_t*>(base + l.header);
   p->total = shape->total;
   p->batch = shape->batch;
+  p->num_cand = static_cast<int32_t>(num_cand);
   p->heads = shape->num_heads;
   p->dim = shape->head_dim;
+  p->dim_v = dim_v(shape);
   p->nfunc = shape->nfunc;
   p->nc = l.nc;
   p->max_seqlen = shape->max_seqlen;
@@ -265,16 +294,50 @@ static hstu_status_t targets_common(const void* q_c, const void* k, const void* 
   return HSTU_OK;
 }
 
+static hstu_status_t targets_fwd(const void* q_c, const void* k, const void* v, void* o_c,
+                                 const int32_t* seq_offsets, const int32_t* cand_offsets, int64_t num_cand,
+                                 const int32_t* func_c, const hstu_attn_shape_t* shape, void* ws, size_t ws_bytes,
+                                 void* stream) {
+  hstu::TgtParams p;
+  hstu_status_t st = targets_common(q_c, k, v, seq_offsets, cand_offsets, num_cand, func_c, shape, ws, ws_bytes, &p);
+  if (st != HSTU_OK) return st;
+  if (num_cand > 0 && !tensor_ok(o_c)) return HSTU_ERR_INVALID_ARG;
+  p.o_c = o_c;
+  return from_cuda(hstu::launch_targets_fwd(p, shape->dtype, static_cast<cudaStream_t>(stream)));
+}
+
+static hstu_status_t targets_bwd(const void* dout_c, const void* q_c, const void* k, const void* v, void* dq_c,
+                                 void* dk, void* dv, const int32_t* seq_offsets, const int32_t* cand_offsets,
+                                 int64_t num_cand, const int32_t* func_c, const hstu_attn_shape_t* shape, void* ws,
+                                 size_t ws_bytes, void* stream) {
+  hstu::TgtParams p;
+  hstu_status_t st = targets_common(q_c, k, v, seq_offsets, cand_offsets, num_cand, func_c, shape, ws, ws_bytes, &p);
+  if (st != HSTU_OK) return st;
+  if ((num_cand > 0 && !(tensor_ok(dout_c) && tensor_ok(dq_c))) ||
+      (shape->total > 0 && !(tensor_ok(dk) && tensor_ok(dv))))
+    return HSTU_ERR_INVALID_ARG;
+  p.do_c = dout_c;
+  p.dq_c = dq_c;
+  p.dk = dk;
+  p.dv = dv;
+  return from_cuda(hstu::launch_targets_bwd(p, shape->dtype, static_cast<cudaStream_t>(stream)));
+}
+
+size_t hstu_attn_targets_workspace_size(const hstu_attn_shape_t* shape, int64_t num_candidates) {
+  if (check_shape(shape) != HSTU_OK || num_candidates < 0 || num_candidates > INT32_MAX) return 0;
+  return hstu::targets_layout(static_cast<int>(num_candidates), shape->num_heads,
+                              std::max(shape->head_dim, dim_v(shape)), shape->max_seqlen)
+      .total;
+}
+
 hstu_status_t hstu_attn_fwd_targets_only(const void* q_c, const void* k, const void* v, void* o_c,
                                          const int32_t* seq_offsets, const int32_t* func_c,
                                          const hstu_attn_shape_t* shape, void* ws,
                                          size_t ws_bytes, void* stream) {
-  hstu::TgtParams p;
-  hstu_status_t st = targets_common(q_c, k, v, seq_offsets, func_c, shape, ws, ws_bytes, &p);
-  if (st != HSTU_OK) return st;
-  if (!tensor_ok(o_c)) return HSTU_ERR_INVALID_ARG;
-  p.o_c = static_cast<__nv_bfloat16*>(o_c);
-  return from_cuda(hstu::launch_targets_fwd(p, static_cast<cudaStream_t>(stream)));
+  NvtxRange nvtx("hstu_attn_fwd_targets_only");
+  if (!shape) return HSTU_ERR_INVALID_ARG;
+  if (!q_c || !func_c) return HSTU_ERR_INVALID_ARG;
+  return targets_fwd(q_c, k, v, o_c, seq_offsets, nullptr, shape->batch, func_c, shape, ws, ws_bytes, stream);
 }
 
 hstu_status_t hstu_attn_bwd_targets_only(const void* dout_c, const void* q_c, const void* k,
@@ -282,16 +345,31 @@ hstu_status_t hstu_attn_bwd_targets_only(const void* dout_c, const void* q_c, co
                                          const int32_t* seq_offsets, const int32_t* func_c,
                                          const hstu_attn_shape_t* shape, void* ws,
                                          size_t ws_bytes, void* stream) {
-  hstu::TgtParams p;
-  hstu_status_t st = targets_common(q_c, k, v, seq_offsets, func_c, shape, ws, ws_bytes, &p);
-  if (st != HSTU_OK) return st;
-  if (!tensor_ok(dout_c) || !tensor_ok(dq_c) || (shape->total > 0 && !(tensor_ok(dk) && tensor_ok(dv))))
-    return HSTU_ERR_INVALID_ARG;
-  p.do_c = static_cast<const __nv_bfloat16*>(dout_c);
-  p.dq_c = static_cast<__nv_bfloat16*>(dq_c);
-  p.dk = static_cast<__nv_bfloat16*>(dk);
-  p.dv = static_cast<__nv_bfloat16*>(dv);
-  return from_cuda(hstu::launch_targets_bwd(p, static_cast<cudaStream_t>(stream)));
+  NvtxRange nvtx("hstu_attn_bwd_targets_only");
+  if (!shape) return HSTU_ERR_INVALID_ARG;
+  if (!q_c || !func_c) return HSTU_ERR_INVALID_ARG;
+  return targets_bwd(dout_c, q_c, k, v, dq_c, dk, dv, seq_offsets, nullptr, shape->batch, func_c, shape, ws,
+                     ws_bytes, stream);
+}
+
+hstu_status_t hstu_attn_fwd_targets(const void* q_c, const void* k, const void* v, void* o_c,
+                                    const int32_t* seq_offsets, const int32_t* cand_offsets, int64_t num_candidates,
+                                    const int32_t* func_c, const hstu_attn_shape_t* shape, void* ws,
+                                    size_t ws_bytes, void* stream) {
+  NvtxRange nvtx("hstu_attn_fwd_targets");
+  if (!cand_offsets) return HSTU_ERR_INVALID_ARG;
+  return targets_fwd(q_c, k, v, o_c, seq_offsets, cand_offsets, num_candidates, func_c, shape, ws, ws_bytes,
+                     stream);
+}
+
+hstu_status_t hstu_attn_bwd_targets(const void* dout_c, const void* q_c, const void* k, const void* v, void* dq_c,
+                                    void* dk, void* dv, const int32_t* seq_offsets, const int32_t* cand_offsets,
+                                    int64_t num_candidates, const int32_t* func_c, const hstu_attn_shape_t* shape,
+                                    void* ws, size_t ws_bytes, void* stream) {
+  NvtxRange nvtx("hstu_attn_bwd_targets");
+  if (!cand_offsets) return HSTU_ERR_INVALID_ARG;
+  return targets_bwd(dout_c, q_c, k, v, dq_c, dk, dv, seq_offsets, cand_offsets, num_candidates, func_c, shape,
+                     ws, ws_bytes, stream);
 }
 
 hstu_status_t hstu_attn_get_device_status(const void* ws, void* stream) {
@@ -309,7 +387,7 @@ const char* hstu_status_string(hstu_status_t status) {
   switch (status) {
     case HSTU_OK: return "ok";
     case HSTU_ERR_INVALID_ARG: return "invalid argument";
-    case HSTU_ERR_UNSUPPORTED: return "unsupported nfunc, head_dim or size";
+    case HSTU_ERR_UNSUPPORTED: return "unsupported nfunc, head dims, dtype or size";
     case HSTU_ERR_WORKSPACE: return "workspace null, misaligned or too small";
     case HSTU_ERR_CUDA: return "CUDA runtime error";
     case HSTU_ERR_DEVICE_INPUT: return "device-side input check failed (seq_offsets)";

@@ -51,6 +51,14 @@
 // per kv row turns the bits into that row's 32-q-row words. No warp needs
 // another's result, and the cost does not depend on the number of intervals,
 // so empty padded intervals stay free.
+//
+// Template parameters: T the 16-bit input type (bf16 or fp16; P and dS are
+// packed in the same type), DPQ / DPV the head dims of q/k and of v/dO
+// rounded up to 64, NINT the number of func intervals. Resident and streamed
+// operands of the q/k width (res0, str0) hold DPQ columns, those of the v/dO
+// width (res1, str1) DPV columns: dV accumulates DPV columns, dK and dQ DPQ.
+#pragma once
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -62,20 +70,24 @@ struct BwdItem {
   uint16_t idx[kMaxTiles];  // visiting (dK/dV) or visited (dQ) tile | 0x100 if partial
 };
 
-template <int DP>
+template <int DPQ, int DPV>
 struct BwdSmem {
-  static constexpr int kChunks = DP / 64;
-  static constexpr int kTile = kChunks * kBlock * 128;           // 128 rows
-  static constexpr int kHalfTile = kChunks * (kBlock / 2) * 128;  // 64 rows
-  static constexpr int kSlots = 5;                               // streamed half tiles
+  static constexpr int kTileQ = (DPQ / 64) * kBlock * 128;        // 128 rows of the q/k width
+  static constexpr int kTileV = (DPV / 64) * kBlock * 128;        // 128 rows of the v/dO width
+  static constexpr int kHalfQ = (DPQ / 64) * (kBlock / 2) * 128;  // 64 rows
+  static constexpr int kHalfV = (DPV / 64) * (kBlock / 2) * 128;
+  // Streamed half tiles: as many as fit next to the residents (5 at
+  // DPQ = DPV = 128), at most 8.
+  static constexpr int kFitSlots = (230400 - kTileQ - kTileV) / (kHalfQ + kHalfV);
+  static constexpr int kSlots = kFitSlots < 8 ? kFitSlots : 8;
   // dK/dV role: res0 = K, res1 = V, str0 = Q, str1 = dO.
   // dQ role:    res0 = Q, res1 = dO, str0 = K, str1 = V.
   // Streamed tiles travel as 64-row halves through a ring of kSlots, each
   // slot freed as soon as the accumulating MMAs of its half have completed.
-  alignas(1024) uint8_t res0[kTile];
-  alignas(1024) uint8_t res1[kTile];
-  alignas(1024) uint8_t str0[kSlots][kHalfTile];
-  alignas(1024) uint8_t str1[kSlots][kHalfTile];
+  alignas(1024) uint8_t res0[kTileQ];
+  alignas(1024) uint8_t res1[kTileV];
+  alignas(1024) uint8_t str0[kSlots][kHalfQ];
+  alignas(1024) uint8_t str1[kSlots][kHalfV];
   static constexpr int kSSlots = 3;  // S slots in TMEM
   alignas(8) uint64_t bar_res_full, bar_res_empty, bar_full[kSlots], bar_empty[kSlots],
       bar_s_full[kSSlots], bar_p_full[kSSlots], bar_dp_free, bar_acc_full, bar_acc_empty,
@@ -86,7 +98,11 @@ struct BwdSmem {
 };
 
 // 227 KB of dynamic shared memory per CTA, with 1 KB of alignment slack.
-static_assert(sizeof(BwdSmem<128>) + 1024 <= 232448, "backward shared memory over the per-CTA limit");
+static_assert(sizeof(BwdSmem<128, 128>) + 1024 <= 232448, "backward shared memory over the per-CTA limit");
+static_assert(sizeof(BwdSmem<128, 64>) + 1024 <= 232448, "backward shared memory over the per-CTA limit");
+static_assert(sizeof(BwdSmem<64, 128>) + 1024 <= 232448, "backward shared memory over the per-CTA limit");
+static_assert(sizeof(BwdSmem<64, 64>) + 1024 <= 232448, "backward shared memory over the per-CTA limit");
+static_assert(BwdSmem<128, 128>::kSlots == 5, "five streamed slots at D = 128");
 
 template <typename S>
 __device__ __forceinline__ S& smem_as_b(uint8_t* raw) {
@@ -99,11 +115,11 @@ __device__ __forceinline__ bool warp_wait_b(uint32_t bar, uint32_t parity, volat
 }
 
 // Writes this warp's half of TMEM columns [taddr, taddr + DP) of its lane (or
-// zeros), times `scale`, into a bf16 row of `dim` elements. Both 32-column
+// zeros), times `scale`, into a row of `dim` elements of T. Both 32-column
 // chunks are read before the first store.
-template <int DP>
-__device__ __forceinline__ void store_acc_half(uint32_t taddr, int half, bool have, bool valid,
-                                               __nv_bfloat16* dst, int dim, float scale, bool wide) {
+template <typename T, int DP>
+__device__ __forceinline__ void store_acc_half(uint32_t taddr, int half, bool have, bool valid, T* dst,
+                                               int dim, float scale, bool wide) {
   constexpr int kNc = DP / 64;
   uint32_t a[kNc][32];
   if (have) {
@@ -120,16 +136,16 @@ __device__ __forceinline__ void store_acc_half(uint32_t taddr, int half, bool ha
 #pragma unroll
   for (int c = 0; c < kNc; ++c) {
     const int col = half * (DP / 2) + c * 32;
-    if (valid && col < dim) store_row32(dst + col, a[c], scale, wide);
+    if (valid && col < dim) store_row32<T>(dst + col, a[c], scale, wide);
   }
 }
 
-// 16 columns [C0, C0 + 16) of 32 loaded S and dP columns -> packed bf16
+// 16 columns [C0, C0 + 16) of 32 loaded S and dP columns -> packed T
 // P' = s (1 + t) (when WANT_P) and G' = dP (1 + t)(1 + h - h t), h = alpha s / 2,
 // t = tanh(h): the backward quantities up to the factor alpha / (2N) applied
 // to dV, dK and dQ at their store. MASKED zeroes the columns whose bit (of
 // the 32-column word) is clear.
-template <int C0, bool MASKED, bool WANT_P>
+template <typename T, int C0, bool MASKED, bool WANT_P>
 __device__ __forceinline__ void epilogue16(const uint32_t (&sv)[32], const uint32_t (&dv)[32],
                                            uint32_t mask, float half_alpha, uint32_t (&pp)[8],
                                            uint32_t (&pd)[8]) {
@@ -148,8 +164,8 @@ __device__ __forceinline__ void epilogue16(const uint32_t (&sv)[32], const uint3
         g[x] = on ? g[x] : 0.0f;
       }
     }
-    if (WANT_P) pp[e / 2] = pack_bf16x2(pv[0], pv[1]);
-    pd[e / 2] = pack_bf16x2(g[0], g[1]);
+    if (WANT_P) pp[e / 2] = Elem<T>::pack2(pv[0], pv[1]);
+    pd[e / 2] = Elem<T>::pack2(g[0], g[1]);
   }
 }
 
@@ -158,22 +174,21 @@ __device__ __forceinline__ void epilogue16(const uint32_t (&sv)[32], const uint3
 // K-step ks of the accumulating MMAs reads P^T from slot columns
 // [16ks, 16ks + 8) and dS^T from [16ks + 8, 16ks + 16); dQ role: dS from
 // [8ks, 8ks + 8).
-template <bool MASKED, bool DKDV>
+template <typename T, bool MASKED, bool DKDV>
 __device__ __forceinline__ void convert_chunk(const uint32_t (&sv)[32], const uint32_t (&dv)[32],
                                               uint32_t mask, float half_alpha, uint32_t xs, int c) {
   uint32_t pp[8], pd[8];
-  epilogue16<0, MASKED, DKDV>(sv, dv, mask, half_alpha, pp, pd);
+  epilogue16<T, 0, MASKED, DKDV>(sv, dv, mask, half_alpha, pp, pd);
   if (DKDV) tmem_st8x2(xs + 32 * c, pp, pd);
   else tmem_st8(xs + 16 * c, pd);
-  epilogue16<16, MASKED, DKDV>(sv, dv, mask, half_alpha, pp, pd);
+  epilogue16<T, 16, MASKED, DKDV>(sv, dv, mask, half_alpha, pp, pd);
   if (DKDV) tmem_st8x2(xs + 32 * c + 16, pp, pd);
   else tmem_st8(xs + 16 * c + 8, pd);
 }
 
-template <int DP, int NINT>
+template <typename T, int DPQ, int DPV, int NINT>
 __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant__ AttnParams p) {
-  using Smem = BwdSmem<DP>;
-  constexpr int kTile = Smem::kTile;
+  using Smem = BwdSmem<DPQ, DPV>;
   constexpr int kChunkBytes = kBlock * 128;       // one 64-column chunk of a 128-row tile
   constexpr int kHalfChunk = (kBlock / 2) * 128;  // one 64-column chunk of a 64-row half
   extern __shared__ uint8_t smem_raw[];
@@ -309,7 +324,7 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
             ok = false;
           if (ok) {
             const uint32_t br = smem_u32(&s.bar_res_full);
-            mbar_expect_tx(br, 2 * kTile);
+            mbar_expect_tx(br, Smem::kTileQ + Smem::kTileV);
             const int row0 = o0 + tile * kBlock;
             tma_load_4d(smem_u32(s.res0), m_res0, br, 0, row0, h, 0);
             tma_load_4d(smem_u32(s.res1), m_res1, br, 0, row0, h, 0);
@@ -323,7 +338,7 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
             }
             const int srow0 = o0 + (it_slot.idx[t >> 1] & 0xff) * kBlock + (t & 1) * (kBlock / 2);
             const uint32_t bar = smem_u32(&s.bar_full[st]);
-            mbar_expect_tx(bar, 2 * Smem::kHalfTile);
+            mbar_expect_tx(bar, Smem::kHalfQ + Smem::kHalfV);
             tma_load_4d(smem_u32(s.str0[st]), m_str0, bar, 0, srow0, h, 0);
             tma_load_4d(smem_u32(s.str1[st]), m_str1, bar, 0, srow0, h, 0);
             str_last[st] = use;
@@ -345,8 +360,10 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
     if (elect_one_sync()) {
       // Half-step pipeline: step v covers the 64-column half (v & 1) of tile
       // v >> 1. S/dP run three steps ahead of the accumulating MMAs.
-      constexpr uint32_t idesc_s = idesc_bf16(128, 64, false, false);
-      constexpr uint32_t idesc_acc = idesc_bf16(128, DP, false, true);
+      constexpr uint32_t idesc_s = idesc_f16kind(128, 64, false, false, Elem<T>::kUmma);
+      // dV accumulates DPV columns (B = dO); dK and dQ DPQ columns (B = Q or K).
+      constexpr uint32_t idesc_accv = idesc_f16kind(128, DPV, false, true, Elem<T>::kUmma);
+      constexpr uint32_t idesc_accq = idesc_f16kind(128, DPQ, false, true, Elem<T>::kUmma);
       // Descriptors are built once; each MMA only advances a start address.
       const uint64_t dr0 = sdesc_sw128(smem_u32(s.res0), 16, 1024);
       const uint64_t dr1 = sdesc_sw128(smem_u32(s.res1), 16, 1024);
@@ -377,10 +394,9 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
           const int gv = gv0 + v, st = gv % Smem::kSlots, k = gv % Smem::kSSlots;
           if (!mbar_wait(smem_u32(&s.bar_full[st]), (gv / Smem::kSlots) & 1, abort_flag)) return false;
           tc_fence_after();
-          const uint32_t hoff = st * Smem::kHalfTile;
-          const uint64_t b0 = sdesc_advance(ds0, hoff), b1 = sdesc_advance(ds1, hoff);
+          const uint64_t b0 = sdesc_advance(ds0, st * Smem::kHalfQ), b1 = sdesc_advance(ds1, st * Smem::kHalfV);
 #pragma unroll
-          for (int kk = 0; kk < DP / 16; ++kk) {
+          for (int kk = 0; kk < DPQ / 16; ++kk) {
             const uint32_t aoff = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
             const uint32_t boff = (kk >> 2) * kHalfChunk + (kk & 3) * 32;
             umma_ss(tS + 64 * k, sdesc_advance(dr0, aoff), sdesc_advance(b0, boff), idesc_s, kk > 0);
@@ -388,7 +404,7 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
           if (gv > 0 && !mbar_wait(smem_u32(&s.bar_dp_free), (gv - 1) & 1, abort_flag)) return false;
           tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < DP / 16; ++kk) {
+          for (int kk = 0; kk < DPV / 16; ++kk) {
             const uint32_t aoff = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
             const uint32_t boff = (kk >> 2) * kHalfChunk + (kk & 3) * 32;
             umma_ss(tdP, sdesc_advance(dr1, aoff), sdesc_advance(b1, boff), idesc_s, kk > 0);
@@ -412,8 +428,8 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
             break;
           }
           tc_fence_after();
-          const uint32_t boff0 = pst * Smem::kHalfTile;
-          const uint64_t m0 = sdesc_advance(ds0_mn, boff0), m1 = sdesc_advance(ds1_mn, boff0);
+          const uint64_t m0 = sdesc_advance(ds0_mn, pst * Smem::kHalfQ);
+          const uint64_t m1 = sdesc_advance(ds1_mn, pst * Smem::kHalfV);
           const uint32_t first = v > 0 ? 1u : 0u;
           const uint32_t xs = tS + 64 * k;
 #pragma unroll
@@ -421,11 +437,11 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
             const uint32_t acc = ks > 0 ? 1u : first;
             if (dkdv) {
               // dV += P^T dO (dO = str1, MN-major); dK += dS^T Q (Q = str0, MN-major)
-              umma_ts(t_acc0, xs + 16 * ks, sdesc_advance(m1, ks * 16 * 128), idesc_acc, acc);
-              umma_ts(t_acc1, xs + 16 * ks + 8, sdesc_advance(m0, ks * 16 * 128), idesc_acc, acc);
+              umma_ts(t_acc0, xs + 16 * ks, sdesc_advance(m1, ks * 16 * 128), idesc_accv, acc);
+              umma_ts(t_acc1, xs + 16 * ks + 8, sdesc_advance(m0, ks * 16 * 128), idesc_accq, acc);
             } else {
               // dQ += dS K (K = str0, MN-major)
-              umma_ts(t_acc0, xs + 8 * ks, sdesc_advance(m0, ks * 16 * 128), idesc_acc, acc);
+              umma_ts(t_acc0, xs + 8 * ks, sdesc_advance(m0, ks * 16 * 128), idesc_accq, acc);
             }
           }
           umma_commit(smem_u32(&s.bar_empty[pst]));  // this half's slot is free
@@ -449,7 +465,7 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
     const float half_alpha = 0.5f * p.alpha;
     const float out_scale = 0.5f * p.alpha * p.inv_n;  // hc = alpha / (2N)
     // 32-byte stores need every output row to start on a 32-byte boundary.
-    const bool wide = wide_rows_ok(p.out0, p.out1, p.out2, p.dim);
+    const bool wide = wide_rows_ok(p.out0, p.out1, p.out2, p.dim, p.dim_v);
     const int hh = half;  // this warp group converts half `half` of every tile
     int g0 = 0;           // tiles over all items
     int acc_uses = 0;
@@ -526,11 +542,11 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
           if (partial) {  // item-uniform: full tiles run no mask arithmetic
             const uint32_t mask = dkdv ? (c == 0 ? qmask0 : qmask1)
                                        : row_mask_word<NINT>(lo, hi, other * kBlock + chunk * 32);
-            if (dkdv) convert_chunk<true, true>(sv, dv, mask, half_alpha, xs, c);
-            else convert_chunk<true, false>(sv, dv, mask, half_alpha, xs, c);
+            if (dkdv) convert_chunk<T, true, true>(sv, dv, mask, half_alpha, xs, c);
+            else convert_chunk<T, true, false>(sv, dv, mask, half_alpha, xs, c);
           } else {
-            if (dkdv) convert_chunk<false, true>(sv, dv, 0u, half_alpha, xs, c);
-            else convert_chunk<false, false>(sv, dv, 0u, half_alpha, xs, c);
+            if (dkdv) convert_chunk<T, false, true>(sv, dv, 0u, half_alpha, xs, c);
+            else convert_chunk<T, false, false>(sv, dv, 0u, half_alpha, xs, c);
           }
         }
         tmem_st_wait();
@@ -545,13 +561,13 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
       if (*abort_flag) break;
       const int64_t row = static_cast<int64_t>(o0 + own_loc) * p.heads + h;
       if (dkdv) {
-        store_acc_half<DP>(t_acc0 + lane_addr, half, nt > 0, valid, p.out2 + row * p.dim, p.dim,
-                           out_scale, wide);  // dV
-        store_acc_half<DP>(t_acc1 + lane_addr, half, nt > 0, valid, p.out1 + row * p.dim, p.dim,
-                           out_scale, wide);  // dK
+        store_acc_half<T, DPV>(t_acc0 + lane_addr, half, nt > 0, valid, static_cast<T*>(p.out2) + row * p.dim_v,
+                               p.dim_v, out_scale, wide);  // dV
+        store_acc_half<T, DPQ>(t_acc1 + lane_addr, half, nt > 0, valid, static_cast<T*>(p.out1) + row * p.dim,
+                               p.dim, out_scale, wide);  // dK
       } else {
-        store_acc_half<DP>(t_acc0 + lane_addr, half, nt > 0, valid, p.out0 + row * p.dim, p.dim,
-                           out_scale, wide);  // dQ
+        store_acc_half<T, DPQ>(t_acc0 + lane_addr, half, nt > 0, valid, static_cast<T*>(p.out0) + row * p.dim,
+                               p.dim, out_scale, wide);  // dQ
       }
       if (nt > 0) {
         tc_fence_before();
@@ -573,11 +589,11 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
   if (threadIdx.x == 0 && !uniform) finish_work(p.header, kHdrBwdNext, kHdrBwdDone);
 }
 
-template <int DP, int NINT>
+template <typename T, int DPQ, int DPV, int NINT>
 static cudaError_t launch_bwd_t(const AttnParams& p, int grid_items, cudaStream_t stream) {
-  const int smem = static_cast<int>(sizeof(BwdSmem<DP>)) + 1024;
+  const int smem = static_cast<int>(sizeof(BwdSmem<DPQ, DPV>)) + 1024;
   static std::atomic<uint64_t> configured{0};  // devices with the limit raised
-  cudaError_t e0 = ensure_smem_limit(hstu_bwd_kernel<DP, NINT>, smem, configured);
+  cudaError_t e0 = ensure_smem_limit(hstu_bwd_kernel<T, DPQ, DPV, NINT>, smem, configured);
   if (e0 != cudaSuccess) return e0;
   const long long work = 2LL * grid_items * p.heads;
   if (work <= 0) return cudaSuccess;
@@ -586,24 +602,30 @@ static cudaError_t launch_bwd_t(const AttnParams& p, int grid_items, cudaStream_
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const long long ctas = work < sms ? work : sms;  // persistent: one CTA per SM
-  hstu_bwd_kernel<DP, NINT><<<static_cast<unsigned>(ctas), 320, smem, stream>>>(p);
+  hstu_bwd_kernel<T, DPQ, DPV, NINT><<<static_cast<unsigned>(ctas), 320, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
-template <int DP>
-static cudaError_t launch_bwd_dp(const AttnParams& p, int nint, int grid_items, cudaStream_t stream) {
+template <typename T, int DPQ, int DPV>
+static cudaError_t launch_bwd_dims(const AttnParams& p, int nint, int grid_items, cudaStream_t stream) {
   switch (nint) {
-    case 1: return launch_bwd_t<DP, 1>(p, grid_items, stream);
-    case 2: return launch_bwd_t<DP, 2>(p, grid_items, stream);
-    case 3: return launch_bwd_t<DP, 3>(p, grid_items, stream);
-    case 4: return launch_bwd_t<DP, 4>(p, grid_items, stream);
-    default: return launch_bwd_t<DP, 5>(p, grid_items, stream);
+    case 1: return launch_bwd_t<T, DPQ, DPV, 1>(p, grid_items, stream);
+    case 2: return launch_bwd_t<T, DPQ, DPV, 2>(p, grid_items, stream);
+    case 3: return launch_bwd_t<T, DPQ, DPV, 3>(p, grid_items, stream);
+    case 4: return launch_bwd_t<T, DPQ, DPV, 4>(p, grid_items, stream);
+    default: return launch_bwd_t<T, DPQ, DPV, 5>(p, grid_items, stream);
   }
 }
 
-cudaError_t launch_bwd(const AttnParams& p, int nint, int grid_items, cudaStream_t stream) {
-  return p.dim > 64 ? launch_bwd_dp<128>(p, nint, grid_items, stream)
-                    : launch_bwd_dp<64>(p, nint, grid_items, stream);
+// Dispatch on the padded head dims (64 for D <= 64, else 128).
+template <typename T>
+static cudaError_t launch_bwd_typed(const AttnParams& p, int nint, int grid_items, cudaStream_t stream) {
+  if (p.dim > 64) {
+    return p.dim_v > 64 ? launch_bwd_dims<T, 128, 128>(p, nint, grid_items, stream)
+                        : launch_bwd_dims<T, 128, 64>(p, nint, grid_items, stream);
+  }
+  return p.dim_v > 64 ? launch_bwd_dims<T, 64, 128>(p, nint, grid_items, stream)
+                      : launch_bwd_dims<T, 64, 64>(p, nint, grid_items, stream);
 }
 
 }  // namespace hstu

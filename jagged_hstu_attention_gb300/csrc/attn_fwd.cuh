@@ -35,10 +35,17 @@
 //               a third epilogue group hides more TMEM and MUFU latency than
 //               two groups at 168 registers.
 //
-// TMEM (512 columns): S0 [0,128), S1 [128,256), S2 [256,384), O [384, 384+DP).
+// TMEM (512 columns): S0 [0,128), S1 [128,256), S2 [256,384), O [384, 384+DPV).
 // Packed P of buffer b occupies columns [128b, 128b+64).
-// SMEM: Q (DP/64 chunks of 128 rows x 128 B, 128-byte swizzle), K and V
-// stages of the same shape, two item slots.
+// SMEM: Q (DPQ/64 chunks of 128 rows x 128 B, 128-byte swizzle), K stages of
+// the same shape, V stages of DPV/64 chunks, two item slots.
+//
+// Template parameters: T the 16-bit input type (bf16 or fp16; P is packed in
+// the same type, since one kind::f16 MMA takes one input type), DPQ / DPV
+// the head dims of q/k and of v/o rounded up to 64 (32 is a 64-wide box half
+// filled with zeros by TMA), NINT the number of func intervals.
+#pragma once
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -50,14 +57,14 @@ struct FwdItem {
   uint16_t tile[kMaxTiles];  // visited kv tile index | 0x100 if partial
 };
 
-template <int DP>
+template <int DPQ, int DPV>
 struct FwdSmem {
-  static constexpr int kChunks = DP / 64;
-  static constexpr int kTile = kChunks * kBlock * 128;  // bytes of a 128 x DP bf16 tile
-  static constexpr int kStages = DP == 128 ? 3 : 4;     // K/V ring depth
-  alignas(1024) uint8_t q[kTile];
-  alignas(1024) uint8_t k[kStages][kTile];
-  alignas(1024) uint8_t v[kStages][kTile];
+  static constexpr int kTileQ = (DPQ / 64) * kBlock * 128;  // bytes of a 128 x DPQ tile
+  static constexpr int kTileV = (DPV / 64) * kBlock * 128;  // bytes of a 128 x DPV tile
+  static constexpr int kStages = (DPQ == 128 && DPV == 128) ? 3 : 4;  // K/V ring depth
+  alignas(1024) uint8_t q[kTileQ];
+  alignas(1024) uint8_t k[kStages][kTileQ];
+  alignas(1024) uint8_t v[kStages][kTileV];
   alignas(8) uint64_t bar_q_full, bar_q_empty, bar_k_full[kStages], bar_k_empty[kStages],
       bar_v_full[kStages], bar_v_empty[kStages], bar_s_full[3], bar_p_full[3], bar_o_full,
       bar_o_empty, bar_item_full[2], bar_item_empty[2], bar_drain;
@@ -67,7 +74,7 @@ struct FwdSmem {
 };
 
 template <typename S>
-__device__ __forceinline__ S& smem_as(uint8_t* raw) {
+__device__ __forceinline__ S& fwd_smem_as(uint8_t* raw) {
   return *reinterpret_cast<S*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
 }
 
@@ -78,8 +85,8 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 }
 
 // P' = s (1 + tanh(alpha s / 2)) = silu(alpha s) / N / hc for 32 columns,
-// packed to 16 bf16x2 words; MASKED zeroes the columns whose bit is clear.
-template <bool MASKED>
+// packed to 16 pairs of T; MASKED zeroes the columns whose bit is clear.
+template <typename T, bool MASKED>
 __device__ __forceinline__ void silu_pack32(const uint32_t (&s)[32], uint32_t mask, float half_alpha,
                                             uint32_t (&pk)[16]) {
 #pragma unroll
@@ -90,12 +97,12 @@ __device__ __forceinline__ void silu_pack32(const uint32_t (&s)[32], uint32_t ma
       p0 = ((mask >> e) & 1u) ? p0 : 0.0f;
       p1 = ((mask >> (e + 1)) & 1u) ? p1 : 0.0f;
     }
-    pk[e / 2] = pack_bf16x2(p0, p1);
+    pk[e / 2] = Elem<T>::pack2(p0, p1);
   }
 }
 
 // Epilogue of one 128 x 128 S tile for this warp's 32 rows (all 128 columns).
-template <int NINT, bool MASKED>
+template <typename T, int NINT, bool MASKED>
 __device__ __forceinline__ void fwd_tile_epilogue(uint32_t sb, int col0, const int (&lo)[NINT],
                                                   const int (&hi)[NINT], float half_alpha) {
 #pragma unroll
@@ -106,8 +113,8 @@ __device__ __forceinline__ void fwd_tile_epilogue(uint32_t sb, int col0, const i
     tmem_ld_wait(a);
     tmem_ld_wait(c);
     uint32_t pa[16], pc[16];
-    silu_pack32<MASKED>(a, MASKED ? row_mask_word<NINT>(lo, hi, col0 + hf * 64) : 0u, half_alpha, pa);
-    silu_pack32<MASKED>(c, MASKED ? row_mask_word<NINT>(lo, hi, col0 + hf * 64 + 32) : 0u, half_alpha,
+    silu_pack32<T, MASKED>(a, MASKED ? row_mask_word<NINT>(lo, hi, col0 + hf * 64) : 0u, half_alpha, pa);
+    silu_pack32<T, MASKED>(c, MASKED ? row_mask_word<NINT>(lo, hi, col0 + hf * 64 + 32) : 0u, half_alpha,
                         pc);
     // Packed over columns [32 hf, 32 hf + 32) of the buffer, which this warp
     // has already read: K-step kk of the PV MMA reads [8kk, 8kk+8).
@@ -120,14 +127,15 @@ __device__ __forceinline__ void fwd_tile_epilogue(uint32_t sb, int col0, const i
 // idle; 128 registers a thread fill the register file.
 constexpr int kFwdThreads = 512;
 
-template <int DP, int NINT>
+template <typename T, int DPQ, int DPV, int NINT>
 __global__ void __launch_bounds__(kFwdThreads, 1) hstu_fwd_kernel(const __grid_constant__ AttnParams p) {
-  using Smem = FwdSmem<DP>;
+  using Smem = FwdSmem<DPQ, DPV>;
   constexpr int NS = Smem::kStages;
-  constexpr int kTile = Smem::kTile;
+  constexpr int kTileQ = Smem::kTileQ;
+  constexpr int kTileV = Smem::kTileV;
   constexpr int kChunkBytes = kBlock * 128;
   extern __shared__ uint8_t smem_raw[];
-  Smem& s = smem_as<Smem>(smem_raw);
+  Smem& s = fwd_smem_as<Smem>(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int32_t* hdr = p.header;
   if (hdr[kHdrErr] != 0) return;
@@ -169,7 +177,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) hstu_fwd_kernel(const __grid_c
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = s.tmem_base;
-  const uint32_t tO = tbase + 384;  // O accumulator columns [384, 384 + DP)
+  const uint32_t tO = tbase + 384;  // O accumulator columns [384, 384 + DPV)
   volatile int* abort_flag = &s.abort_flag;
 
   if (warp == 12) {
@@ -239,7 +247,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) hstu_fwd_kernel(const __grid_c
         if (n > 0) {
           if (q_uses > 0 && !mbar_wait(smem_u32(&s.bar_q_empty), (q_uses - 1) & 1, abort_flag)) ok = false;
           if (ok) {
-            mbar_expect_tx(smem_u32(&s.bar_q_full), kTile);
+            mbar_expect_tx(smem_u32(&s.bar_q_full), kTileQ);
             tma_load_4d(smem_u32(s.q), &p.tm_q, smem_u32(&s.bar_q_full), 0, o0 + qt * kBlock, h, 0);
             ++q_uses;
           }
@@ -250,7 +258,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) hstu_fwd_kernel(const __grid_c
               break;
             }
             const uint32_t bar = smem_u32(&s.bar_k_full[st]);
-            mbar_expect_tx(bar, kTile);
+            mbar_expect_tx(bar, kTileQ);
             const int row = o0 + (it_slot.tile[t] & 0xff) * kBlock;
             tma_load_4d(smem_u32(s.k[st]), &p.tm_k, bar, 0, row, h, 0);
             k_last[st] = use;
@@ -290,7 +298,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) hstu_fwd_kernel(const __grid_c
             break;
           }
           const uint32_t bar = smem_u32(&s.bar_v_full[st]);
-          mbar_expect_tx(bar, kTile);
+          mbar_expect_tx(bar, kTileV);
           const int row = item.o0 + (item.tile[t] & 0xff) * kBlock;
           tma_load_4d(smem_u32(s.v[st]), &p.tm_v, bar, 0, row, item.h, 0);
           v_last[st] = use;
@@ -308,8 +316,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) hstu_fwd_kernel(const __grid_c
   } else if (warp == 13) {
     // ------------------------------------------------------------ MMA issuer
     if (elect_one_sync()) {
-      constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
-      constexpr uint32_t idesc_o = idesc_bf16(128, DP, false, true);
+      constexpr uint32_t idesc_s = idesc_f16kind(128, 128, false, false, Elem<T>::kUmma);
+      constexpr uint32_t idesc_o = idesc_f16kind(128, DPV, false, true, Elem<T>::kUmma);
       // Descriptors are built once; each MMA only advances a start address.
       const uint64_t dq = sdesc_sw128(smem_u32(s.q), 16, 1024);
       const uint64_t dk0 = sdesc_sw128(smem_u32(s.k[0]), 16, 1024);
@@ -334,10 +342,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) hstu_fwd_kernel(const __grid_c
             const int gg = g + t, kst = gg % NS, sb = gg % 3;
             if (!mbar_wait(smem_u32(&s.bar_k_full[kst]), (gg / NS) & 1, abort_flag)) { ok = false; break; }
             tc_fence_after();
-            const uint64_t dk = sdesc_advance(dk0, kst * kTile);
+            const uint64_t dk = sdesc_advance(dk0, kst * kTileQ);
             const uint32_t d_tmem = tbase + sb * 128;
 #pragma unroll
-            for (int kk = 0; kk < DP / 16; ++kk) {
+            for (int kk = 0; kk < DPQ / 16; ++kk) {
               const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
               umma_ss(d_tmem, sdesc_advance(dq, off), sdesc_advance(dk, off), idesc_s, kk > 0);
             }
@@ -358,7 +366,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) hstu_fwd_kernel(const __grid_c
               break;
             }
             tc_fence_after();
-            const uint64_t dv = sdesc_advance(dv0, pkst * kTile);
+            const uint64_t dv = sdesc_advance(dv0, pkst * kTileV);
             const uint32_t a_tmem = tbase + psb * 128;
             umma_ts(tO, a_tmem, dv, idesc_o, pt > 0 ? 1u : 0u);
 #pragma unroll
@@ -383,7 +391,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) hstu_fwd_kernel(const __grid_c
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     const float half_alpha = 0.5f * p.alpha;
     const float out_scale = 0.5f * p.alpha * p.inv_n;  // hc = alpha / (2N)
-    const bool wide = wide_rows_ok(p.out0, p.out0, p.out0, p.dim);
+    const bool wide = wide_rows_ok(p.out0, p.out0, p.out0, p.dim_v, p.dim_v);
     const int r = quarter * 32 + lane;                 // q row within the tile == TMEM lane
     int g = 0, o_uses = 0;
     bool ok = true;
@@ -406,8 +414,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) hstu_fwd_kernel(const __grid_c
         tc_fence_after();
         const int tile = item.tile[t];
         const uint32_t sb = tbase + lane_addr + sbuf * 128;
-        if (tile & 0x100) fwd_tile_epilogue<NINT, true>(sb, (tile & 0xff) * kBlock, lo, hi, half_alpha);
-        else fwd_tile_epilogue<NINT, false>(sb, (tile & 0xff) * kBlock, lo, hi, half_alpha);
+        if (tile & 0x100) fwd_tile_epilogue<T, NINT, true>(sb, (tile & 0xff) * kBlock, lo, hi, half_alpha);
+        else fwd_tile_epilogue<T, NINT, false>(sb, (tile & 0xff) * kBlock, lo, hi, half_alpha);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(smem_u32(&s.bar_p_full[sbuf]));
@@ -423,10 +431,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1) hstu_fwd_kernel(const __grid_c
         tc_fence_after();
       }
       if (*abort_flag) break;
-      constexpr int kHalfCols = DP / 2;
+      constexpr int kHalfCols = DPV / 2;
       constexpr int kNc = kHalfCols / 32;
-      __nv_bfloat16* dst =
-          p.out0 + (static_cast<int64_t>(o0 + qt * kBlock + r) * p.heads + h) * p.dim;
+      T* dst = static_cast<T*>(p.out0) + (static_cast<int64_t>(o0 + qt * kBlock + r) * p.heads + h) * p.dim_v;
       uint32_t v32[kNc][32];
       if (nt > 0) {
 #pragma unroll
@@ -442,7 +449,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) hstu_fwd_kernel(const __grid_c
 #pragma unroll
       for (int cc = 0; cc < kNc; ++cc) {
         const int col = grp * kHalfCols + cc * 32;
-        if (valid && col < p.dim) store_row32(dst + col, v32[cc], out_scale, wide);
+        if (valid && col < p.dim_v) store_row32<T>(dst + col, v32[cc], out_scale, wide);
       }
       if (nt > 0) {
         tc_fence_before();
@@ -465,18 +472,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1) hstu_fwd_kernel(const __grid_c
 }
 
 // Number of SMs of the current device (looked up per call; cheap).
-static cudaError_t sm_count(int* sms) {
+static inline cudaError_t sm_count(int* sms) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   return cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev);
 }
 
-template <int DP, int NINT>
+template <typename T, int DPQ, int DPV, int NINT>
 static cudaError_t launch_fwd_t(const AttnParams& p, int grid_items, cudaStream_t stream) {
-  const int smem = static_cast<int>(sizeof(FwdSmem<DP>)) + 1024;
+  const int smem = static_cast<int>(sizeof(FwdSmem<DPQ, DPV>)) + 1024;
   static std::atomic<uint64_t> configured{0};  // devices with the limit raised
-  cudaError_t e0 = ensure_smem_limit(hstu_fwd_kernel<DP, NINT>, smem, configured);
+  cudaError_t e0 = ensure_smem_limit(hstu_fwd_kernel<T, DPQ, DPV, NINT>, smem, configured);
   if (e0 != cudaSuccess) return e0;
   const long long work = static_cast<long long>(grid_items) * p.heads;
   if (work <= 0) return cudaSuccess;
@@ -484,24 +491,30 @@ static cudaError_t launch_fwd_t(const AttnParams& p, int grid_items, cudaStream_
   cudaError_t e = sm_count(&sms);
   if (e != cudaSuccess) return e;
   const long long ctas = work < sms ? work : sms;  // persistent: one CTA per SM
-  hstu_fwd_kernel<DP, NINT><<<static_cast<unsigned>(ctas), kFwdThreads, smem, stream>>>(p);
+  hstu_fwd_kernel<T, DPQ, DPV, NINT><<<static_cast<unsigned>(ctas), kFwdThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
-template <int DP>
-static cudaError_t launch_fwd_dp(const AttnParams& p, int nint, int grid_items, cudaStream_t stream) {
+template <typename T, int DPQ, int DPV>
+static cudaError_t launch_fwd_dims(const AttnParams& p, int nint, int grid_items, cudaStream_t stream) {
   switch (nint) {
-    case 1: return launch_fwd_t<DP, 1>(p, grid_items, stream);
-    case 2: return launch_fwd_t<DP, 2>(p, grid_items, stream);
-    case 3: return launch_fwd_t<DP, 3>(p, grid_items, stream);
-    case 4: return launch_fwd_t<DP, 4>(p, grid_items, stream);
-    default: return launch_fwd_t<DP, 5>(p, grid_items, stream);
+    case 1: return launch_fwd_t<T, DPQ, DPV, 1>(p, grid_items, stream);
+    case 2: return launch_fwd_t<T, DPQ, DPV, 2>(p, grid_items, stream);
+    case 3: return launch_fwd_t<T, DPQ, DPV, 3>(p, grid_items, stream);
+    case 4: return launch_fwd_t<T, DPQ, DPV, 4>(p, grid_items, stream);
+    default: return launch_fwd_t<T, DPQ, DPV, 5>(p, grid_items, stream);
   }
 }
 
-cudaError_t launch_fwd(const AttnParams& p, int nint, int grid_items, cudaStream_t stream) {
-  return p.dim > 64 ? launch_fwd_dp<128>(p, nint, grid_items, stream)
-                    : launch_fwd_dp<64>(p, nint, grid_items, stream);
+// Dispatch on the padded head dims (64 for D <= 64, else 128).
+template <typename T>
+static cudaError_t launch_fwd_typed(const AttnParams& p, int nint, int grid_items, cudaStream_t stream) {
+  if (p.dim > 64) {
+    return p.dim_v > 64 ? launch_fwd_dims<T, 128, 128>(p, nint, grid_items, stream)
+                        : launch_fwd_dims<T, 128, 64>(p, nint, grid_items, stream);
+  }
+  return p.dim_v > 64 ? launch_fwd_dims<T, 64, 128>(p, nint, grid_items, stream)
+                      : launch_fwd_dims<T, 64, 64>(p, nint, grid_items, stream);
 }
 
 }  // namespace hstu

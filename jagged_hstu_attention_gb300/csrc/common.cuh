@@ -90,6 +90,7 @@ struct TargetsLayout {
   int nc = 0;
   size_t header = 0, partial = 0, total = 0;
 };
+// dim: the wider of D_qk and D_v (the partials hold O rows or dQ rows).
 inline TargetsLayout targets_layout(int batch, int heads, int dim, int max_seqlen) {
   TargetsLayout l;
   l.nc = (max_seqlen + kTgtChunk - 1) / kTgtChunk;
@@ -114,38 +115,42 @@ struct PlanParams {
   int32_t batch, nfunc, nt, max_seqlen;
 };
 
+// Element types of q, k, v, dO and the outputs (one type for all of them).
+constexpr int kDtypeBf16 = 0, kDtypeF16 = 1;
+
 struct AttnParams {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;          // 128-row boxes
   CUtensorMap tm_q64, tm_k64, tm_v64, tm_do64;  // 64-row boxes (backward streams)
   const int32_t* seq_offsets;
   const int32_t* func;
-  __nv_bfloat16* out0;  // fwd: o; bwd: dq
-  __nv_bfloat16* out1;  // bwd: dk
-  __nv_bfloat16* out2;  // bwd: dv
+  void* out0;  // fwd: o (T, H, dim_v); bwd: dq (T, H, dim)
+  void* out1;  // bwd: dk (T, H, dim)
+  void* out2;  // bwd: dv (T, H, dim_v)
   const uint8_t* cls;
   const uint8_t* ivmask;
   const int32_t* list;
   int32_t* header;
   int64_t total;
-  int32_t heads, dim, nt, max_seqlen;
+  int32_t heads, dim, dim_v, nt, max_seqlen;  // dim = D_qk, dim_v = D_v
   float alpha, inv_n;
 };
 
 struct TgtParams {
-  const __nv_bfloat16* q_c;
-  const __nv_bfloat16* k;
-  const __nv_bfloat16* v;
-  const __nv_bfloat16* do_c;
-  __nv_bfloat16* o_c;   // fwd output
-  __nv_bfloat16* dq_c;  // bwd outputs
-  __nv_bfloat16* dk;
-  __nv_bfloat16* dv;
+  const void* q_c;   // (C, H, dim), C = num_cand candidate rows
+  const void* k;     // (T, H, dim)
+  const void* v;     // (T, H, dim_v)
+  const void* do_c;  // (C, H, dim_v)
+  void* o_c;         // fwd output (C, H, dim_v)
+  void* dq_c;        // bwd outputs: (C, H, dim)
+  void* dk;          // (T, H, dim)
+  void* dv;          // (T, H, dim_v)
   const int32_t* seq_offsets;
-  const int32_t* func_c;
+  const int32_t* cand_offsets;  // (batch + 1) or null: one candidate per sequence
+  const int32_t* func_c;        // (nfunc, num_cand)
   float* partial;
   int32_t* header;
   int64_t total;
-  int32_t batch, heads, dim, nfunc, nc, max_seqlen;
+  int32_t batch, num_cand, heads, dim, dim_v, nfunc, nc, max_seqlen;
   float alpha, inv_n;
 };
 
@@ -228,18 +233,19 @@ __device__ __forceinline__ float silu_gu(float s, float dp, float half_alpha) {
   return u * f;
 }
 
-// Stores 32 fp32 accumulator columns of one row, times `scale`, as bf16:
+// Stores 32 fp32 accumulator columns of one row, times `scale`, as T (bf16
+// or fp16):
 // 64 bytes as two 32-byte stores when `wide` (a 32-byte aligned row), else
 // as four 16-byte stores. Each thread writes its own row, so every store
 // instruction of a warp touches 32 rows; wider stores halve their number.
 // The stores skip L1 allocation: nothing reads the rows back, and the
 // read-out of a tile's accumulators measured about 20% faster that way.
-__device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const uint32_t (&a)[32], float scale,
-                                            bool wide) {
+template <typename T>
+__device__ __forceinline__ void store_row32(T* dst, const uint32_t (&a)[32], float scale, bool wide) {
   uint32_t pk[16];
 #pragma unroll
   for (int e = 0; e < 16; ++e)
-    pk[e] = pack_bf16x2(scale * __uint_as_float(a[2 * e]), scale * __uint_as_float(a[2 * e + 1]));
+    pk[e] = Elem<T>::pack2(scale * __uint_as_float(a[2 * e]), scale * __uint_as_float(a[2 * e + 1]));
   if (wide) {
 #pragma unroll
     for (int e = 0; e < 2; ++e)
@@ -257,12 +263,12 @@ __device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const uint32_t (
   }
 }
 
-// True when 32-byte stores of output rows of `dim` bf16 elements from these
-// bases stay aligned.
-__device__ __forceinline__ bool wide_rows_ok(const void* a, const void* b, const void* c, int dim) {
+// True when 32-byte stores of output rows of `dim` 16-bit elements from
+// these bases stay aligned.
+__device__ __forceinline__ bool wide_rows_ok(const void* a, const void* b, const void* c, int dim, int dim2) {
   return ((reinterpret_cast<uintptr_t>(a) | reinterpret_cast<uintptr_t>(b) | reinterpret_cast<uintptr_t>(c)) &
           31u) == 0 &&
-         (dim % 16) == 0;
+         (dim % 16) == 0 && (dim2 % 16) == 0;
 }
 
 }  // namespace hstu

@@ -27,9 +27,21 @@ cudaError_t ensure_smem_limit(Kernel kernel, int smem, std::atomic<uint64_t>& do
 
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream);
 // grid_items: upper bound on the number of work items (CTAs = items * heads).
-cudaError_t launch_fwd(const AttnParams& p, int nint, int grid_items, cudaStream_t stream);
-cudaError_t launch_bwd(const AttnParams& p, int nint, int grid_items, cudaStream_t stream);
-cudaError_t launch_targets_fwd(const TgtParams& p, cudaStream_t stream);
-cudaError_t launch_targets_bwd(const TgtParams& p, cudaStream_t stream);
+// One translation unit per input type keeps the many kernel variants
+// compiling in parallel.
+cudaError_t launch_fwd_bf16(const AttnParams& p, int nint, int grid_items, cudaStream_t stream);
+cudaError_t launch_fwd_f16(const AttnParams& p, int nint, int grid_items, cudaStream_t stream);
+cudaError_t launch_bwd_bf16(const AttnParams& p, int nint, int grid_items, cudaStream_t stream);
+cudaError_t launch_bwd_f16(const AttnParams& p, int nint, int grid_items, cudaStream_t stream);
+inline cudaError_t launch_fwd(const AttnParams& p, int nint, int dtype, int grid_items, cudaStream_t stream) {
+  return dtype == kDtypeF16 ? launch_fwd_f16(p, nint, grid_items, stream)
+                            : launch_fwd_bf16(p, nint, grid_items, stream);
+}
+inline cudaError_t launch_bwd(const AttnParams& p, int nint, int dtype, int grid_items, cudaStream_t stream) {
+  return dtype == kDtypeF16 ? launch_bwd_f16(p, nint, grid_items, stream)
+                            : launch_bwd_bf16(p, nint, grid_items, stream);
+}
+cudaError_t launch_targets_fwd(const TgtParams& p, int dtype, cudaStream_t stream);
+cudaError_t launch_targets_bwd(const TgtParams& p, int dtype, cudaStream_t stream);
 
 }  // namespace hstu

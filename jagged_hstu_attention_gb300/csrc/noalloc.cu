@@ -12,6 +12,8 @@
 // calls on a device share it and it keeps the last call's contents; the plan
 // clears the parts that must start at zero at the beginning of every call.
 // Calls whose work overlaps on the GPU (two streams at once) race on it.
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "../../include/hstu_attn.h"
@@ -23,22 +25,70 @@ constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
+// The array's device address, looked up once per CUDA context of a device.
+// A context has a unique id for the life of the process; a device whose
+// context was torn down and rebuilt (cudaDeviceReset) gets a new one, in
+// which the module is loaded again and the array may sit elsewhere, so the
+// cached address is only reused while the current context's id matches.
+struct ScratchSlot {
+  unsigned long long ctx_id = 0;
+  void* ptr = nullptr;
+};
 std::mutex g_setup_mutex;
-void* g_scratch_ptr[kMaxDevices] = {};
+ScratchSlot g_scratch[kMaxDevices];
 
-// Device address of the scratch array on the current device. Host code only
-// sees a host-side stand-in under the array's name, so the address is looked
-// up once per device, with that device current, and cached.
+struct CtxFns {
+  PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  PFN_cuCtxGetId_v12000 get_id = nullptr;
+};
+const CtxFns& ctx_fns() {
+  static CtxFns fns;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fns.get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fns.get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(f);
+  });
+  return fns;
+}
+
+// Unique id of the current context (0 if none can be read).
+unsigned long long current_ctx_id() {
+  const CtxFns& fns = ctx_fns();
+  if (!fns.get_current || !fns.get_id) return 0;
+  CUcontext ctx = nullptr;
+  if (fns.get_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+  unsigned long long id = 0;
+  if (fns.get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// Device address of the scratch array in the current device's context. Host
+// code only sees a host-side stand-in under the array's name, so the address
+// is looked up with cudaGetSymbolAddress, with that device current, on the
+// first call in each context, and cached.
 hstu_status_t scratch_for_current_device(void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return HSTU_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_setup_mutex);
-  if (!g_scratch_ptr[dev]) {
+  ScratchSlot& slot = g_scratch[dev];
+  unsigned long long id = current_ctx_id();
+  if (!slot.ptr || id == 0 || id != slot.ctx_id) {
     void* ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return HSTU_ERR_CUDA;
-    g_scratch_ptr[dev] = ptr;
+    if (id == 0) id = current_ctx_id();  // the lookup may have made the context current
+    slot.ptr = ptr;
+    slot.ctx_id = id;  // 0: not cacheable, looked up again next call
+    *out = ptr;
+    return HSTU_OK;
   }
-  *out = g_scratch_ptr[dev];
+  *out = slot.ptr;
   return HSTU_OK;
 }
 

@@ -96,7 +96,8 @@ __device__ void classify_tile(const PlanParams& p, int b, int qt) {
   if (tid == 0) p.ivmask[static_cast<size_t>(b) * p.nt + qt] = static_cast<uint8_t>(active_iv);
 }
 
-// Exclusive scan of cnt[0..n) in place (one block of 1024 threads).
+// Exclusive scan of cnt[0..n) in place, by one block (any multiple of 32
+// threads up to 1024), in chunks of blockDim.x entries.
 __device__ void block_exclusive_scan(int* cnt, int n) {
   __shared__ int carry;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;

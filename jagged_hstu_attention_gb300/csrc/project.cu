@@ -1,0 +1,494 @@
+// Candidate-row projection of the targets-only layer (MLCommons training PR
+// #903, Summary: the last layer computes U and Q for the candidate rows
+// alone; K and V stay full length). The projection of a row is the layer's
+// pointwise-SiLU input projection, y = silu(x W^T + b), W laid out (out
+// features, in features); here it runs on a list of rows only.
+//
+//   forward   gather the listed rows of x (one small copy kernel), then one
+//             tcgen05 GEMM Z = X_c W^T with the bias and SiLU fused into its
+//             epilogue (y, and optionally z for the backward);
+//   backward  G = dY * silu'(Z) and the bias gradient's column partials (one
+//             elementwise kernel, a fixed-order fold), then two tcgen05 GEMMs:
+//             dX_c = G W and dW = G^T X_c.
+//
+// The GEMM: C[M x N] = A[M x K] B[N x K]^T with fp32 accumulation in TMEM. A
+// and B come from row-major 2-D tensors; an operand is K-major when K runs
+// along the tensor's rows (A = X_c, A = G, B = W in the forward) and
+// MN-major when K runs down its columns (B = W in dX_c; A = G and B = X_c in
+// dW). Tiles of 128 x 256 outputs, 64-deep K blocks through a 3-stage TMA
+// ring (48 KB a stage, 128-byte swizzle), one elected thread issuing
+// M=128, N=256, K=16 MMAs, four epilogue warps reading the accumulator out
+// of TMEM, one row per thread.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "../../include/hstu_attn.h"
+#include "common.cuh"
+
+namespace hstu {
+
+namespace {
+
+constexpr int kGemmBM = 128, kGemmBN = 256, kGemmBK = 64, kGemmStages = 3;
+constexpr int kGemmThreads = 192;  // warps 0-3 epilogue, 4 TMA producer, 5 MMA issuer
+
+// Epilogues.
+constexpr int kEpiStore = 0;     // out = acc
+constexpr int kEpiBiasSilu = 1;  // z = acc + bias; out = silu(z); out2 = z (optional)
+
+struct GemmParams {
+  CUtensorMap tm_a, tm_b;
+  void* out;
+  void* out2;
+  const void* bias;
+  int32_t* err;  // error word (nullable): kErrTimeout on a timed-out wait
+  int32_t M, N, K, ldo;
+};
+
+struct GemmSmem {
+  alignas(1024) uint8_t a[kGemmStages][kGemmBM * kGemmBK * 2];  // 16 KB a stage
+  alignas(1024) uint8_t b[kGemmStages][kGemmBN * kGemmBK * 2];  // 32 KB a stage
+  alignas(8) uint64_t bar_full[kGemmStages], bar_empty[kGemmStages], bar_acc, bar_drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y,
+                                            int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+
+// Loads one stage of an operand tile covering MN rows [mn0, mn0 + rows) and
+// K [k0, k0 + 64). K-major: a 2-D box {64 K columns, rows}, landing as
+// [row][128 B]. MN-major: a 3-D box {64 MN columns, 64 K rows, rows / 64
+// groups}, landing as [group][K row][128 B]. x is 0 or k0, both multiples of
+// 64 elements (128 bytes).
+template <bool MN>
+__device__ __forceinline__ void load_operand(uint32_t dst, const CUtensorMap* map, uint32_t bar, int mn0, int k0) {
+  if (MN) tma_load_3d(dst, map, bar, 0, k0, mn0 / 64);
+  else tma_load_2d(dst, map, bar, k0, mn0);
+}
+
+// Shared-memory descriptor of K-step kk (16 deep) of a stage tile.
+template <bool MN>
+__device__ __forceinline__ uint64_t operand_desc(uint32_t base, int kk) {
+  if (MN) return sdesc_sw128(base + kk * 16 * 128, 64 * 128, 1024);  // LBO: between 64-wide MN groups
+  return sdesc_sw128(base + kk * 32, 16, 1024);
+}
+
+template <typename T, bool A_MN, bool B_MN, int EPI>
+__global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  GemmSmem& s = *reinterpret_cast<GemmSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m0 = blockIdx.x * kGemmBM, n0 = blockIdx.y * kGemmBN;
+  const int nk = (p.K + kGemmBK - 1) / kGemmBK;
+  constexpr uint32_t kStageBytes = (kGemmBM + kGemmBN) * kGemmBK * 2;
+  if (threadIdx.x == 0) {
+    s.abort_flag = 0;
+    for (int i = 0; i < kGemmStages; ++i) {
+      mbar_init(smem_u32(&s.bar_full[i]), 1);
+      mbar_init(smem_u32(&s.bar_empty[i]), 1);
+    }
+    mbar_init(smem_u32(&s.bar_acc), 1);
+    mbar_init(smem_u32(&s.bar_drain), 1);
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(&s.tmem_base), kGemmBN);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tacc = s.tmem_base;
+  volatile int* abort_flag = &s.abort_flag;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_map(&p.tm_a);
+      tma_prefetch_map(&p.tm_b);
+      int last[kGemmStages] = {-1, -1, -1};
+      for (int kb = 0; kb < nk; ++kb) {
+        const int st = kb % kGemmStages, use = kb / kGemmStages;
+        if (use > 0 && !mbar_wait(smem_u32(&s.bar_empty[st]), (use - 1) & 1, abort_flag)) break;
+        const uint32_t bar = smem_u32(&s.bar_full[st]);
+        mbar_expect_tx(bar, kStageBytes);
+        load_operand<A_MN>(smem_u32(s.a[st]), &p.tm_a, bar, m0, kb * kGemmBK);
+        load_operand<B_MN>(smem_u32(s.b[st]), &p.tm_b, bar, n0, kb * kGemmBK);
+        last[st] = use;
+      }
+      for (int st = 0; st < kGemmStages; ++st)  // never leave with a copy in flight
+        if (last[st] >= 0) mbar_wait_drain(smem_u32(&s.bar_full[st]), last[st] & 1);
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (elect_one_sync()) {
+      constexpr uint32_t idesc = idesc_f16kind(kGemmBM, kGemmBN, A_MN, B_MN, Elem<T>::kUmma);
+      bool ok = true;
+      for (int kb = 0; kb < nk; ++kb) {
+        const int st = kb % kGemmStages;
+        if (!mbar_wait(smem_u32(&s.bar_full[st]), (kb / kGemmStages) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kGemmBK / 16; ++kk)
+          umma_ss(tacc, operand_desc<A_MN>(smem_u32(s.a[st]), kk), operand_desc<B_MN>(smem_u32(s.b[st]), kk),
+                  idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(smem_u32(&s.bar_empty[st]));
+      }
+      if (ok) umma_commit(smem_u32(&s.bar_acc));
+      umma_commit(smem_u32(&s.bar_drain));  // every MMA issued above has completed (also on abort)
+      mbar_wait_drain(smem_u32(&s.bar_drain), 0);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const bool ok = mbar_wait(smem_u32(&s.bar_acc), 0, abort_flag);
+    if (__all_sync(0xffffffffu, ok)) {
+      tc_fence_after();
+      const int row = m0 + warp * 32 + lane;
+      const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
+      T* out = static_cast<T*>(p.out) + static_cast<int64_t>(row) * p.ldo;
+      T* out2 = p.out2 ? static_cast<T*>(p.out2) + static_cast<int64_t>(row) * p.ldo : nullptr;
+      const T* bias = static_cast<const T*>(p.bias);
+      for (int c = 0; c < kGemmBN / 32; ++c) {
+        const int col = n0 + c * 32;
+        uint32_t a[32];
+        tmem_ld32(tacc + lane_addr + c * 32, a);
+        tmem_ld_wait(a);
+        if (row >= p.M || col >= p.N) continue;  // N is a multiple of 32
+        uint32_t pk[16], pz[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          float x0 = __uint_as_float(a[2 * e]), x1 = __uint_as_float(a[2 * e + 1]);
+          if (EPI == kEpiBiasSilu) {
+            if (bias) {
+              const uint32_t bw = *reinterpret_cast<const uint32_t*>(bias + col + 2 * e);
+              x0 += Elem<T>::lo(bw);
+              x1 += Elem<T>::hi(bw);
+            }
+            pz[e] = Elem<T>::pack2(x0, x1);
+            pk[e] = Elem<T>::pack2(x0 * sigmoidf_fast(x0), x1 * sigmoidf_fast(x1));
+          } else {
+            pk[e] = Elem<T>::pack2(x0, x1);
+          }
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          *reinterpret_cast<uint4*>(out + col + 8 * e) = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+        if (EPI == kEpiBiasSilu && out2) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            *reinterpret_cast<uint4*>(out2 + col + 8 * e) =
+                make_uint4(pz[4 * e], pz[4 * e + 1], pz[4 * e + 2], pz[4 * e + 3]);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tacc, kGemmBN);
+  }
+  if (threadIdx.x == 0 && s.abort_flag && p.err) atomicOr(p.err, kErrTimeout);
+}
+
+// X_c[i] = x[rows[i]] (16-byte copies); a row index outside [0, x_rows)
+// sets kErrInput and gives a zero row.
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ x, int64_t x_rows,
+                                                          const int32_t* __restrict__ rows, int64_t n,
+                                                          int row_vecs, uint4* __restrict__ xc, int32_t* err) {
+  const int64_t i = blockIdx.x;
+  if (i >= n) return;
+  const int r = rows[i];
+  const bool ok = r >= 0 && r < x_rows;
+  if (!ok && threadIdx.x == 0) atomicOr(err, kErrInput);
+  for (int v = threadIdx.x; v < row_vecs; v += blockDim.x)
+    xc[i * row_vecs + v] = ok ? x[static_cast<int64_t>(r) * row_vecs + v] : make_uint4(0, 0, 0, 0);
+}
+
+// G = dY * silu'(Z) for a chunk of 128 rows and 256 columns (one column a
+// thread), and the chunk's column sums of G (the bias gradient's partials).
+template <typename T>
+__global__ void __launch_bounds__(256) silu_grad_kernel(const T* __restrict__ dy, const T* __restrict__ z,
+                                                        int64_t rows, int cols, T* __restrict__ g,
+                                                        float* __restrict__ part) {
+  const int col = blockIdx.y * 256 + threadIdx.x;
+  if (col >= cols) return;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * 128;
+  const int64_t r1 = r0 + 128 < rows ? r0 + 128 : rows;
+  float sum = 0.0f;
+  for (int64_t r = r0; r < r1; ++r) {
+    const int64_t idx = r * cols + col;
+    const uint16_t zb = reinterpret_cast<const uint16_t*>(z)[idx];
+    const uint16_t db = reinterpret_cast<const uint16_t*>(dy)[idx];
+    const float zz = Elem<T>::lo(zb), d = Elem<T>::lo(db);
+    const float sg = sigmoidf_fast(zz);
+    const float gv = d * sg * (1.0f + zz * (1.0f - sg));
+    const uint32_t w = Elem<T>::pack2(gv, 0.0f);
+    reinterpret_cast<uint16_t*>(g)[idx] = static_cast<uint16_t>(w & 0xffffu);
+    sum += Elem<T>::lo(w);  // the bias gradient sums the same rounded G the GEMMs read
+  }
+  part[static_cast<int64_t>(blockIdx.x) * cols + col] = sum;
+}
+
+// db[col] = sum of the chunk partials in chunk order.
+template <typename T>
+__global__ void __launch_bounds__(256) column_fold_kernel(const float* __restrict__ part, int chunks, int cols,
+                                                          T* __restrict__ db) {
+  const int col = blockIdx.x * 256 + threadIdx.x;
+  if (col >= cols) return;
+  float s = 0.0f;
+  for (int c = 0; c < chunks; ++c) s += part[static_cast<int64_t>(c) * cols + col];
+  const uint32_t w = Elem<T>::pack2(s, 0.0f);
+  reinterpret_cast<uint16_t*>(db)[col] = static_cast<uint16_t>(w & 0xffffu);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// Tensor map of a row-major (rows, cols) operand: K-major tiles are boxes of
+// {64 columns, box_rows rows}; MN-major tiles are a 3-D view {64 columns,
+// rows, cols / 64 groups} (group stride 128 B) with boxes {64, 64, box_cols /
+// 64}. Rows or groups past the tensor read as zeros.
+bool operand_map(CUtensorMap* m, const void* ptr, int64_t rows, int cols, int dtype, bool mn, int box_mn) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const CUtensorMapDataType type =
+      dtype == HSTU_DTYPE_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const cuuint64_t row_bytes = static_cast<cuuint64_t>(cols) * 2;
+  cuuint32_t es[3] = {1, 1, 1};
+  if (!mn) {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_mn)};
+    return fn(m, type, 2, const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  }
+  cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(cols / 64)};
+  cuuint64_t strides[2] = {row_bytes, 128};
+  cuuint32_t box[3] = {64, 64, static_cast<cuuint32_t>(box_mn / 64)};
+  return fn(m, type, 3, const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <typename T, bool A_MN, bool B_MN, int EPI>
+cudaError_t launch_gemm(const GemmParams& p, cudaStream_t stream) {
+  const int smem = static_cast<int>(sizeof(GemmSmem)) + 1024;
+  static std::atomic<uint64_t> configured{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev < 64 ? (uint64_t{1} << dev) : 0;
+  if (bit == 0 || (configured.load() & bit) == 0) {
+    e = cudaFuncSetAttribute(gemm_kernel<T, A_MN, B_MN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    if (bit) configured.fetch_or(bit);
+  }
+  const dim3 grid((p.M + kGemmBM - 1) / kGemmBM, (p.N + kGemmBN - 1) / kGemmBN);
+  if (grid.x == 0 || grid.y == 0) return cudaSuccess;
+  gemm_kernel<T, A_MN, B_MN, EPI><<<grid, kGemmThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Workspace of the projection: a 256-byte header (error word), then the
+// gathered rows X_c (n x d_in), then (backward) G (n x d_out) and the bias
+// partials (ceil(n / 128) x d_out fp32).
+struct ProjLayout {
+  size_t xc = 0, g = 0, part = 0, total = 0;
+};
+ProjLayout proj_layout(int64_t n, int d_in, int d_out, bool bwd) {
+  ProjLayout l;
+  l.xc = kHdrWords * 4;
+  l.g = l.xc + align_up(static_cast<size_t>(n) * d_in * 2, 256);
+  l.part = l.g + (bwd ? align_up(static_cast<size_t>(n) * d_out * 2, 256) : 0);
+  l.total = l.part + (bwd ? align_up(static_cast<size_t>((n + 127) / 128) * d_out * 4, 256) : 0);
+  return l;
+}
+
+hstu_status_t proj_checks(int64_t x_rows, int64_t n, int d_in, int d_out, int dtype) {
+  if (x_rows < 0 || n < 0 || n > INT32_MAX || x_rows > INT32_MAX) return HSTU_ERR_INVALID_ARG;
+  if (d_in < 64 || d_out < 64 || d_in % 64 || d_out % 64 || d_in > 65536 || d_out > 65536)
+    return HSTU_ERR_UNSUPPORTED;
+  if (dtype != HSTU_DTYPE_BF16 && dtype != HSTU_DTYPE_F16) return HSTU_ERR_UNSUPPORTED;
+  return HSTU_OK;
+}
+
+template <typename T>
+hstu_status_t project_fwd_t(const void* x, int64_t x_rows, const int32_t* rows, int64_t n, const void* w,
+                            const void* bias, int d_in, int d_out, int dtype, void* y, void* z, void* ws,
+                            cudaStream_t stream) {
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  const ProjLayout l = proj_layout(rows ? n : 0, d_in, d_out, false);
+  int32_t* err = reinterpret_cast<int32_t*>(base);
+  if (cudaMemsetAsync(err, 0, kHdrWords * 4, stream) != cudaSuccess) return HSTU_ERR_CUDA;
+  if (n == 0) return HSTU_OK;
+  const void* a = x;
+  if (rows) {
+    gather_rows_kernel<<<static_cast<unsigned>(n), 256, 0, stream>>>(
+        static_cast<const uint4*>(x), x_rows, rows, n, d_in / 8, reinterpret_cast<uint4*>(base + l.xc), err);
+    if (cudaGetLastError() != cudaSuccess) return HSTU_ERR_CUDA;
+    a = base + l.xc;
+  }
+  GemmParams p{};
+  if (!operand_map(&p.tm_a, a, n, d_in, dtype, false, kGemmBM) ||
+      !operand_map(&p.tm_b, w, d_out, d_in, dtype, false, kGemmBN))
+    return HSTU_ERR_CUDA;
+  p.out = y;
+  p.out2 = z;
+  p.bias = bias;
+  p.err = err;
+  p.M = static_cast<int32_t>(n);
+  p.N = d_out;
+  p.K = d_in;
+  p.ldo = d_out;
+  return launch_gemm<T, false, false, kEpiBiasSilu>(p, stream) == cudaSuccess ? HSTU_OK : HSTU_ERR_CUDA;
+}
+
+template <typename T>
+hstu_status_t project_bwd_t(const void* dy, const void* z, const void* x, int64_t x_rows, const int32_t* rows,
+                            int64_t n, const void* w, int d_in, int d_out, int dtype, void* dx_c, void* dw,
+                            void* dbias, void* ws, cudaStream_t stream) {
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  const ProjLayout l = proj_layout(n, d_in, d_out, true);
+  int32_t* err = reinterpret_cast<int32_t*>(base);
+  if (cudaMemsetAsync(err, 0, kHdrWords * 4, stream) != cudaSuccess) return HSTU_ERR_CUDA;
+  if (n == 0) {  // no rows: dW and db are zero
+    if (cudaMemsetAsync(dw, 0, static_cast<size_t>(d_out) * d_in * 2, stream) != cudaSuccess) return HSTU_ERR_CUDA;
+    if (dbias && cudaMemsetAsync(dbias, 0, static_cast<size_t>(d_out) * 2, stream) != cudaSuccess)
+      return HSTU_ERR_CUDA;
+    return HSTU_OK;
+  }
+  T* g = reinterpret_cast<T*>(base + l.g);
+  float* part = reinterpret_cast<float*>(base + l.part);
+  const int chunks = static_cast<int>((n + 127) / 128);
+  silu_grad_kernel<T><<<dim3(chunks, (d_out + 255) / 256), 256, 0, stream>>>(
+      static_cast<const T*>(dy), static_cast<const T*>(z), n, d_out, g, part);
+  if (cudaGetLastError() != cudaSuccess) return HSTU_ERR_CUDA;
+  if (dbias) {
+    column_fold_kernel<T><<<(d_out + 255) / 256, 256, 0, stream>>>(part, chunks, d_out, static_cast<T*>(dbias));
+    if (cudaGetLastError() != cudaSuccess) return HSTU_ERR_CUDA;
+  }
+  const void* xc = x;
+  if (rows) {
+    gather_rows_kernel<<<static_cast<unsigned>(n), 256, 0, stream>>>(
+        static_cast<const uint4*>(x), x_rows, rows, n, d_in / 8, reinterpret_cast<uint4*>(base + l.xc), err);
+    if (cudaGetLastError() != cudaSuccess) return HSTU_ERR_CUDA;
+    xc = base + l.xc;
+  }
+  // dX_c (n x d_in) = G (n x d_out, K-major) . W (d_out x d_in read MN-major: N = d_in, K = d_out)
+  GemmParams p1{};
+  if (!operand_map(&p1.tm_a, g, n, d_out, dtype, false, kGemmBM) ||
+      !operand_map(&p1.tm_b, w, d_out, d_in, dtype, true, kGemmBN))
+    return HSTU_ERR_CUDA;
+  p1.out = dx_c;
+  p1.err = err;
+  p1.M = static_cast<int32_t>(n);
+  p1.N = d_in;
+  p1.K = d_out;
+  p1.ldo = d_in;
+  if (launch_gemm<T, false, true, kEpiStore>(p1, stream) != cudaSuccess) return HSTU_ERR_CUDA;
+  // dW (d_out x d_in) = G^T (M = d_out, K = n: MN-major) . X_c (N = d_in, K = n: MN-major)
+  GemmParams p2{};
+  if (!operand_map(&p2.tm_a, g, n, d_out, dtype, true, kGemmBM) ||
+      !operand_map(&p2.tm_b, xc, n, d_in, dtype, true, kGemmBN))
+    return HSTU_ERR_CUDA;
+  p2.out = dw;
+  p2.err = err;
+  p2.M = d_out;
+  p2.N = d_in;
+  p2.K = static_cast<int32_t>(n);
+  p2.ldo = d_in;
+  return launch_gemm<T, true, true, kEpiStore>(p2, stream) == cudaSuccess ? HSTU_OK : HSTU_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace hstu
+
+extern "C" {
+
+HSTU_API size_t hstu_attn_project_workspace_size(int64_t num_rows, int32_t d_in, int32_t d_out, int32_t backward) {
+  if (hstu::proj_checks(0, num_rows, d_in, d_out, HSTU_DTYPE_BF16) != HSTU_OK) return 0;
+  return hstu::proj_layout(num_rows, d_in, d_out, backward != 0).total;
+}
+
+HSTU_API hstu_status_t hstu_attn_project_rows(const void* x, int64_t x_rows, const int32_t* rows, int64_t num_rows,
+                                              const void* w, const void* bias, int32_t d_in, int32_t d_out,
+                                              int32_t dtype, void* y, void* z, void* ws, size_t ws_bytes,
+                                              void* stream) {
+  hstu_status_t st = hstu::proj_checks(x_rows, num_rows, d_in, d_out, dtype);
+  if (st != HSTU_OK) return st;
+  if (!rows && num_rows != x_rows) return HSTU_ERR_INVALID_ARG;
+  if (num_rows > 0 && (!hstu::aligned16(x) || !hstu::aligned16(w) || !hstu::aligned16(y) ||
+                       (z && !hstu::aligned16(z)) || (bias && (reinterpret_cast<uintptr_t>(bias) & 3u))))
+    return HSTU_ERR_INVALID_ARG;
+  if (rows && (reinterpret_cast<uintptr_t>(rows) & 3u)) return HSTU_ERR_INVALID_ARG;
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) ||
+      ws_bytes < hstu_attn_project_workspace_size(rows ? num_rows : 0, d_in, d_out, 0))
+    return HSTU_ERR_WORKSPACE;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  return dtype == HSTU_DTYPE_F16
+             ? hstu::project_fwd_t<__half>(x, x_rows, rows, num_rows, w, bias, d_in, d_out, dtype, y, z, ws, cs)
+             : hstu::project_fwd_t<__nv_bfloat16>(x, x_rows, rows, num_rows, w, bias, d_in, d_out, dtype, y, z,
+                                                  ws, cs);
+}
+
+HSTU_API hstu_status_t hstu_attn_project_rows_bwd(const void* dy, const void* z, const void* x, int64_t x_rows,
+                                                  const int32_t* rows, int64_t num_rows, const void* w,
+                                                  int32_t d_in, int32_t d_out, int32_t dtype, void* dx_rows,
+                                                  void* dw, void* dbias, void* ws, size_t ws_bytes, void* stream) {
+  hstu_status_t st = hstu::proj_checks(x_rows, num_rows, d_in, d_out, dtype);
+  if (st != HSTU_OK) return st;
+  if (!rows && num_rows != x_rows) return HSTU_ERR_INVALID_ARG;
+  if (!hstu::aligned16(dw) || !dw) return HSTU_ERR_INVALID_ARG;
+  if (num_rows > 0 && (!hstu::aligned16(dy) || !hstu::aligned16(z) || !hstu::aligned16(x) ||
+                       !hstu::aligned16(w) || !hstu::aligned16(dx_rows) || !dy || !z || !x || !w || !dx_rows))
+    return HSTU_ERR_INVALID_ARG;
+  if ((rows && (reinterpret_cast<uintptr_t>(rows) & 3u)) || (dbias && (reinterpret_cast<uintptr_t>(dbias) & 3u)))
+    return HSTU_ERR_INVALID_ARG;
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) ||
+      ws_bytes < hstu_attn_project_workspace_size(num_rows, d_in, d_out, 1))
+    return HSTU_ERR_WORKSPACE;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  return dtype == HSTU_DTYPE_F16
+             ? hstu::project_bwd_t<__half>(dy, z, x, x_rows, rows, num_rows, w, d_in, d_out, dtype, dx_rows, dw,
+                                           dbias, ws, cs)
+             : hstu::project_bwd_t<__nv_bfloat16>(dy, z, x, x_rows, rows, num_rows, w, d_in, d_out, dtype, dx_rows,
+                                                  dw, dbias, ws, cs);
+}
+
+}  // extern "C"

@@ -13,6 +13,7 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 namespace hstu {
 
@@ -198,12 +199,16 @@ __device__ __forceinline__ uint64_t sdesc_advance(uint64_t desc, uint32_t byte_o
   return desc + static_cast<uint64_t>(byte_off >> 4);
 }
 
-// Instruction descriptor, kind::f16: bf16 A and B, fp32 accumulator,
-// a_mn / b_mn select MN-major operands.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool b_mn) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(a_mn) << 15) |
+// Instruction descriptor, kind::f16, fp32 accumulator. `etype` is the type
+// of both A and B (one kind::f16 MMA takes one input type): 0 = fp16,
+// 1 = bf16. a_mn / b_mn select MN-major operands.
+__host__ __device__ constexpr uint32_t idesc_f16kind(int M, int N, bool a_mn, bool b_mn, uint32_t etype) {
+  return (1u << 4) | (etype << 7) | (etype << 10) | (static_cast<uint32_t>(a_mn) << 15) |
          (static_cast<uint32_t>(b_mn) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
+}
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool b_mn) {
+  return idesc_f16kind(M, N, a_mn, b_mn, 1u);
 }
 
 // D[tmem] (+)= A[smem] * B[smem]
@@ -239,6 +244,33 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// The two 16-bit input types of the kernels: the UMMA type code, packing of
+// two fp32 values (round to nearest even) and the unpacking of a packed pair.
+template <typename T>
+struct Elem;
+template <>
+struct Elem<__nv_bfloat16> {
+  static constexpr uint32_t kUmma = 1;
+  static __device__ __forceinline__ uint32_t pack2(float lo, float hi) { return pack_bf16x2(lo, hi); }
+  static __device__ __forceinline__ float lo(uint32_t w) { return __uint_as_float(w << 16); }
+  static __device__ __forceinline__ float hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+};
+template <>
+struct Elem<__half> {
+  static constexpr uint32_t kUmma = 0;
+  static __device__ __forceinline__ uint32_t pack2(float lo, float hi) { return pack_f16x2(lo, hi); }
+  static __device__ __forceinline__ float lo(uint32_t w) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xffffu)));
+  }
+  static __device__ __forceinline__ float hi(uint32_t w) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16)));
+  }
+};
 __device__ __forceinline__ bool elect_one_sync() {
   uint32_t pred = 0;
   asm volatile(

@@ -98,7 +98,8 @@ def _rows_onerank(L: int, nfunc: int, groups: int = 8, task_tokens: int = 3) -> 
     assert nfunc >= 5
     gsize = task_tokens + 1
     lp = L - groups * gsize
-    assert lp > 0
+    if lp <= 0:  # too short for the group layout: causal rows
+        return _rows_causal(L, nfunc)
     f = np.empty((nfunc, L), dtype=np.int64)
     for r in range(L):
         if r < lp:
@@ -159,6 +160,11 @@ def build_func_candidates(lens: np.ndarray, nfunc: int = 1) -> np.ndarray:
 def randn_bf16(shape, gen: torch.Generator, device="cpu") -> torch.Tensor:
     """N(0, 1) drawn in fp32, rounded to bf16."""
     return torch.randn(shape, generator=gen, dtype=torch.float32, device=device).to(torch.bfloat16)
+
+
+def randn(shape, gen: torch.Generator, device="cpu", dtype=torch.bfloat16) -> torch.Tensor:
+    """N(0, 1) drawn in fp32, rounded to ``dtype`` (bf16 or fp16)."""
+    return torch.randn(shape, generator=gen, dtype=torch.float32, device=device).to(dtype)
 
 
 @dataclasses.dataclass

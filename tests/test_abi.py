@@ -40,10 +40,22 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def _shape(**kw):
-    s = dict(batch=4, total=1000, heads=2, dim=128, nfunc=5, max_seqlen=300, alpha=0.1)
+    s = dict(batch=4, total=1000, heads=2, dim=128, nfunc=5, max_seqlen=300, alpha=0.1, dim_v=0, dtype=0)
     s.update(kw)
     return hb.make_shape(s["batch"], s["total"], s["heads"], s["dim"], s["nfunc"], s["max_seqlen"],
-                         s["alpha"])
+                         s["alpha"], dim_v=s["dim_v"], dtype=s["dtype"])
+
+
+def test_shape_variants_accepted_and_rejected(lib):
+    for dim in (32, 64, 128):
+        for dim_v in (0, 32, 64, 128):
+            for dtype in (0, 1):
+                assert hb.workspace_size(_shape(dim=dim, dim_v=dim_v, dtype=dtype), hb.WS_FULL) > 0
+    # targets-only partials hold rows of the wider of D_qk and D_v
+    assert hb.workspace_size(_shape(dim=32, dim_v=128), hb.WS_TARGETS) == \
+        hb.workspace_size(_shape(dim=128, dim_v=32), hb.WS_TARGETS) == hb.workspace_size(_shape(), hb.WS_TARGETS)
+    for bad in (dict(dim_v=48), dict(dim_v=256), dict(dim=256), dict(dtype=2), dict(dtype=-1)):
+        assert hb.workspace_size(_shape(**bad), hb.WS_FULL) == 0, bad
 
 
 def test_nfunc_supported(lib):
@@ -120,3 +132,34 @@ def test_binding_has_no_cpu_path():
         hb.fwd(q, q, q, off, func, 4)
     with pytest.raises(ValueError, match="CUDA"):
         hb.bwd(q, q, q, q, off, func, 4)
+
+
+def _spec(kind=0, k1=0, k2=0, groups=8, task_tokens=3):
+    return hb.FuncSpec(kind, k1, k2, groups, task_tokens)
+
+
+def test_build_func_rejects_bad_arguments_on_the_host(lib):
+    vp = ctypes.c_void_p
+    fake = vp(256)  # never dereferenced: every case fails its host check first
+    cases = [
+        (None, fake, 2, 100, 64, 5, fake, 1),                      # no spec
+        (_spec(), None, 2, 100, 64, 5, fake, 1),                   # no offsets
+        (_spec(), fake, 0, 100, 64, 5, fake, 1),                   # batch < 1
+        (_spec(), fake, 2, -1, 64, 5, fake, 1),                    # total < 0
+        (_spec(), fake, 2, 100, 0, 5, fake, 1),                    # max_seqlen < 1
+        (_spec(), fake, 2, 100, 64, 4, fake, 2),                   # even nfunc
+        (_spec(), fake, 2, 100, 64, 5, None, 1),                   # no func
+        (_spec(), vp(258), 2, 100, 64, 5, fake, 1),                # misaligned offsets
+        (_spec(kind=7), fake, 2, 100, 64, 5, fake, 1),             # unknown family
+        (_spec(kind=1, k1=-1), fake, 2, 100, 64, 5, fake, 1),      # negative prefix
+        (_spec(kind=1, k1=4, k2=2), fake, 2, 100, 64, 1, fake, 2),  # SLA needs two intervals
+        (_spec(kind=2, groups=0), fake, 2, 100, 64, 5, fake, 1),   # no groups
+        (_spec(kind=2), fake, 2, 100, 64, 3, fake, 2),             # OneRank needs three intervals
+    ]
+    for spec, off, batch, total, n, nfunc, func, want in cases:
+        st = lib.hstu_attn_build_func(ctypes.byref(spec) if spec is not None else None, off, batch, total, n,
+                                      nfunc, func, None)
+        assert st == want, (spec and spec.kind, batch, total, n, nfunc, st)
+    assert lib.hstu_attn_build_func_candidates(None, 2, 1, fake, None) == 1
+    assert lib.hstu_attn_build_func_candidates(fake, 2, 2, fake, None) == 2
+    assert lib.hstu_attn_build_func_candidates(fake, 0, 1, fake, None) == 1

@@ -98,7 +98,11 @@ def _rank_main(rank, port, out_dir):
     dist.init_process_group("gloo", rank=rank, world_size=WORLD)
     try:
         hb.load()
-        idx, lens, n_max = bench.rank_sequences(CFG, SEED, WORLD, rank)
+        job = bench.job_lengths(CFG, SEED, WORLD)
+        jcfg = wl.Config(CFG.name, 1, 0, 0, CFG.heads, CFG.dim, CFG.mask, CFG.nfunc)
+        cost = [int(orc.visible_counts(np.array([0, int(L)]), wl.func_rows(jcfg, int(L)), CFG.nfunc).sum())
+                for L in job]
+        idx, lens, n_max = bench.rank_sequences(CFG, SEED, WORLD, rank, cost)
         # The job's batch, built the same way on every rank; this rank keeps
         # only its own sequences.
         gcfg = wl.Config(CFG.name, CFG.batch * WORLD, CFG.len_lo, CFG.len_hi, CFG.heads, CFG.dim,
