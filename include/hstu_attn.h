@@ -325,6 +325,19 @@ HSTU_API const char* hstu_status_string(hstu_status_t status);
  * HSTU_ERR_INVALID_ARG for a limit out of range; nothing is enqueued then. */
 HSTU_API hstu_status_t hstu_attn_test_wait_timeout(void* ws, int32_t limit_ms, void* stream);
 
+/* Test hook for the abort path inside the attention kernels. Sets the limit
+ * of one bounded wait of hstu_attn_fwd and hstu_attn_bwd launched after the
+ * call: the MMA-issuing thread's wait for the epilogue to have read out the
+ * previous work item's accumulators. A limit of 1 ns makes that wait give up
+ * at once, while the next item's copies and MMAs are in flight; the kernel
+ * then raises its abort flag, every role drains what it issued (bounded
+ * waits), TMEM is freed and the workspace error word gets HSTU_ERR_TIMEOUT --
+ * no fault, no hang, the context stays usable.
+ *   limit_ns: 1 .. 2e9; 0 restores the kernels' normal limit (2 s).
+ * Process-wide and meant for tests only; returns HSTU_ERR_INVALID_ARG above
+ * 2e9. */
+HSTU_API hstu_status_t hstu_attn_test_set_handoff_limit(uint64_t limit_ns);
+
 /* Splits a batch over `world` data-parallel ranks, by whole sequences. Every
  * (sequence, head) unit of the op is independent in the forward and the
  * backward pass, so the ranks need no exchange; each runs the op on its own

@@ -33,7 +33,7 @@ EXPORTED = (
     "hstu_attn_shard_sequences", "hstu_attn_test_wait_timeout", "hstu_attn_build_func",
     "hstu_attn_build_func_candidates", "hstu_attn_targets_workspace_size", "hstu_attn_fwd_targets",
     "hstu_attn_bwd_targets", "hstu_attn_project_workspace_size", "hstu_attn_project_rows",
-    "hstu_attn_project_rows_bwd",
+    "hstu_attn_project_rows_bwd", "hstu_attn_test_set_handoff_limit",
 )
 FUNC_CAUSAL, FUNC_SLA, FUNC_ONERANK = 0, 1, 2
 NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -97,6 +97,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "hstu_attn_fwd_noalloc": (ctypes.c_int, [vp, vp, vp, vp, vp, vp, sp, vp, vp]),
         "hstu_attn_shard_sequences": (ctypes.c_int, [vp, i32, i32, vp, vp]),
         "hstu_attn_test_wait_timeout": (ctypes.c_int, [vp, i32, vp]),
+        "hstu_attn_test_set_handoff_limit": (ctypes.c_int, [ctypes.c_uint64]),
         "hstu_attn_build_func": (ctypes.c_int, [ctypes.POINTER(FuncSpec), vp, i32, ctypes.c_int64, i32, i32, vp,
                                                 vp]),
         "hstu_attn_build_func_candidates": (ctypes.c_int, [vp, i32, i32, vp, vp]),
@@ -463,3 +464,9 @@ def project_rows_bwd(dy, z, x, w, rows=None, want_dbias=True, ws=None, stream=No
                                              d_out, dtype, _ptr(dx), _ptr(dw), _ptr(db), _ptr(ws), ws.numel(),
                                              _stream(stream)), "hstu_attn_project_rows_bwd")
     return dx, dw, db
+
+
+def set_handoff_limit_for_tests(limit_ns: int) -> None:
+    """Test hook (hstu_attn_test_set_handoff_limit): shortens the attention
+    kernels' accumulator hand-off wait; 0 restores the normal limit."""
+    _check(load().hstu_attn_test_set_handoff_limit(int(limit_ns)), "hstu_attn_test_set_handoff_limit")

@@ -6,6 +6,7 @@
 #include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "../../include/hstu_attn.h"
@@ -86,6 +87,15 @@ bool make_map(CUtensorMap* m, const void* ptr, int64_t tokens, int heads, int di
 }
 
 hstu_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? HSTU_OK : HSTU_ERR_CUDA; }
+
+// Limit of the attention kernels' accumulator hand-off wait; 0 = the
+// kernels' normal limit. Only hstu_attn_test_set_handoff_limit changes it.
+std::atomic<uint64_t> g_handoff_limit_ns{0};
+
+uint64_t handoff_limit() {
+  const uint64_t v = g_handoff_limit_ns.load(std::memory_order_relaxed);
+  return v != 0 ? v : hstu::kWaitLimitNs;
+}
 
 // Upper bound on the number of (sequence, tile) work items.
 int grid_items(const hstu_attn_shape_t* s, int nt) {
@@ -204,6 +214,7 @@ hstu_status_t hstu_attn_fwd(const void* q, const void* k, const void* v, void* o
   p.max_seqlen = shape->max_seqlen;
   p.alpha = shape->alpha;
   p.inv_n = 1.0f / static_cast<float>(shape->max_seqlen);
+  p.handoff_limit_ns = handoff_limit();
   return from_cuda(hstu::launch_fwd(p, (shape->nfunc + 1) / 2, dt, grid_items(shape, l.nt), cs));
 }
 
@@ -251,6 +262,7 @@ hstu_status_t hstu_attn_bwd(const void* dout, const void* q, const void* k, cons
   p.max_seqlen = shape->max_seqlen;
   p.alpha = shape->alpha;
   p.inv_n = 1.0f / static_cast<float>(shape->max_seqlen);
+  p.handoff_limit_ns = handoff_limit();
   return from_cuda(hstu::launch_bwd(p, (shape->nfunc + 1) / 2, dt, grid_items(shape, l.nt), cs));
 }
 
@@ -370,6 +382,12 @@ hstu_status_t hstu_attn_bwd_targets(const void* dout_c, const void* q_c, const v
   if (!cand_offsets) return HSTU_ERR_INVALID_ARG;
   return targets_bwd(dout_c, q_c, k, v, dq_c, dk, dv, seq_offsets, cand_offsets, num_candidates, func_c, shape,
                      ws, ws_bytes, stream);
+}
+
+hstu_status_t hstu_attn_test_set_handoff_limit(uint64_t limit_ns) {
+  if (limit_ns > hstu::kWaitLimitNs) return HSTU_ERR_INVALID_ARG;
+  g_handoff_limit_ns.store(limit_ns, std::memory_order_relaxed);
+  return HSTU_OK;
 }
 
 hstu_status_t hstu_attn_get_device_status(const void* ws, void* stream) {

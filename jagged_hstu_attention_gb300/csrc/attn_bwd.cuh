@@ -15,8 +15,12 @@
 // dK and dV accumulate in TMEM across the whole item and are stored once:
 // no atomics, fixed order, bitwise repeatable.
 //
-// dQ role -- item (sequence b, q tile qt, head h). Q and dO stay in SMEM; K
-// and V of every visited kv tile stream. Per kv tile (lanes = q rows):
+// dQ role -- item (sequence b, q tile qt, head h). Q and dO arrive in SMEM
+// and are copied into TMEM (tcgen05.cp, into the columns the dK/dV role uses
+// for dK), so that S and dP read their A operand from TMEM and only the
+// streamed K / V half from SMEM (an N=64 MMA with both operands in SMEM is
+// bound by shared-memory reads); K and V of every visited kv tile stream.
+// Per kv tile (lanes = q rows):
 //     S = Q K^T,  dP = dO V^T;  dS = dP * silu'(alpha S) * alpha/N (packed
 //     over S);  dQ += dS K.
 // This recomputes S and dP once more per visible tile pair (14 D instead of
@@ -30,9 +34,9 @@
 // current item finishes; its first accumulating MMA waits until the epilogue
 // has read out the previous item's accumulators.
 //
-// TMEM (512 columns, the same for both roles): acc0 [0,128) (dV or dQ),
-// acc1 [128,256) (dK), three S slots at 256, 320 and 384, one dP slot at
-// 448 (64 columns each).
+// TMEM (512 columns): acc0 [0,128) (dV or dQ), acc1 [128,256) (dK, or the
+// dQ role's Q and dO), three S slots at 256, 320 and 384, one dP slot at 448
+// (64 columns each).
 //
 // Half-step pipeline: every 128-wide tile is handled as two 64-column halves
 // ("half-steps", counted globally as v). S(v) and dP(v) are N=64 MMAs; S(v)
@@ -88,9 +92,16 @@ struct BwdSmem {
   alignas(1024) uint8_t res1[kTileV];
   alignas(1024) uint8_t str0[kSlots][kHalfQ];
   alignas(1024) uint8_t str1[kSlots][kHalfV];
-  static constexpr int kSSlots = 3;  // S slots in TMEM
+  // TMEM slots of 64 columns after the two accumulators: kSSlots for S
+  // (packed P/dS are written over them) and kDpSlots for dP. S/dP of step
+  // v + kSSlots are issued right after the accumulating MMAs of step v.
+  // Two S and two dP slots measured the same as three and one on DLRM and
+  // OneRank and 3% slower on SLA.
+  static constexpr int kSSlots = 3;
+  static constexpr int kDpSlots = 1;
+  static_assert(256 + 64 * (kSSlots + kDpSlots) <= 512, "TMEM holds 512 columns");
   alignas(8) uint64_t bar_res_full, bar_res_empty, bar_full[kSlots], bar_empty[kSlots],
-      bar_s_full[kSSlots], bar_p_full[kSSlots], bar_dp_free, bar_acc_full, bar_acc_empty,
+      bar_s_full[kSSlots], bar_p_full[kSSlots], bar_dp_free[kDpSlots], bar_acc_full, bar_acc_empty,
       bar_item_full[2], bar_item_empty[2], bar_drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -215,7 +226,7 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
       mbar_init(smem_u32(&s.bar_s_full[i]), 1);
       mbar_init(smem_u32(&s.bar_p_full[i]), 128);
     }
-    mbar_init(smem_u32(&s.bar_dp_free), 128);
+    for (int i = 0; i < Smem::kDpSlots; ++i) mbar_init(smem_u32(&s.bar_dp_free[i]), 128);
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&s.bar_item_full[i]), 1);
       mbar_init(smem_u32(&s.bar_item_empty[i]), 1 + 256);  // MMA issuer + epilogue threads
@@ -236,7 +247,7 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
   const uint32_t t_acc0 = tbase;        // dV (dK/dV role) or dQ (dQ role)
   const uint32_t t_acc1 = tbase + 128;  // dK (dK/dV role)
   const uint32_t tS = tbase + 256;      // S slot k at tS + 64 k
-  const uint32_t tdP = tbase + 448;
+  const uint32_t tdP = tS + 64 * Smem::kSSlots;  // dP slot j at tdP + 64 j
   volatile int* abort_flag = &s.abort_flag;
   const size_t nt_all = static_cast<size_t>(p.nt);
 
@@ -371,8 +382,25 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
       const uint64_t ds1 = sdesc_sw128(smem_u32(s.str1[0]), 16, 1024);
       const uint64_t ds0_mn = sdesc_sw128(smem_u32(s.str0[0]), kHalfChunk, 1024);
       const uint64_t ds1_mn = sdesc_sw128(smem_u32(s.str1[0]), kHalfChunk, 1024);
+      // dQ role: Q and dO are copied into TMEM (the columns a dK/dV item
+      // uses for dK), so that its S and dP MMAs read A from TMEM and only the
+      // streamed K / V half from shared memory. With both operands in shared
+      // memory an N=64 MMA is bound by shared-memory reads.
+      const uint32_t tQr = t_acc1, tdOr = t_acc1 + DPQ / 2;
+      // The wait for the epilogue to have read out the previous item's
+      // accumulators (limit p.handoff_limit_ns; a limit of 1 ns, set only by
+      // a test, gives up at once so that the abort path runs with this
+      // item's copies and MMAs in flight).
+      auto handoff_wait = [&](uint32_t bar, uint32_t parity) -> bool {
+        if (p.handoff_limit_ns <= 1) {
+          *abort_flag = 1;
+          return false;
+        }
+        return mbar_wait(bar, parity, abort_flag, p.handoff_limit_ns);
+      };
       int gs = 0;        // streamed tiles over all items
       int res_uses = 0;  // items with at least one tile
+      bool prev_dkdv = false;  // role of the previous item with at least one tile
       bool ok = true;
       int i = 0;
       for (; ok; ++i) {
@@ -385,41 +413,76 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
         if (nt == 0) continue;
         if (!mbar_wait(smem_u32(&s.bar_res_full), res_uses & 1, abort_flag)) break;
         tc_fence_after();
+        if (!dkdv) {
+          // The copy overwrites the dK columns: after a dK/dV item, wait until
+          // the epilogue has read them out. (After a dQ item the columns hold
+          // its Q and dO, whose last readers -- its S/dP MMAs -- completed
+          // before its last accumulating MMA was issued.)
+          if (res_uses > 0 && prev_dkdv && !handoff_wait(smem_u32(&s.bar_acc_empty), (res_uses - 1) & 1))
+            break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < DPQ / 16; ++kk)
+            tmem_cp_128x256b(tQr + 8 * kk, sdesc_advance(dr0, (kk >> 2) * kChunkBytes + (kk & 3) * 32));
+#pragma unroll
+          for (int kk = 0; kk < DPV / 16; ++kk)
+            tmem_cp_128x256b(tdOr + 8 * kk, sdesc_advance(dr1, (kk >> 2) * kChunkBytes + (kk & 3) * 32));
+          umma_commit(smem_u32(&s.bar_res_empty));  // shared-memory residents free once copied
+        }
         const int nsteps = 2 * nt;
         const int gv0 = 2 * gs;  // global index of this item's first half-step
         // S/dP of step v (N = 64 MMAs): S (or S^T) = res0 . str0_h^T into S
         // slot gv % 3, dP (or dP^T) = res1 . str1_h^T into the dP slot once
         // the epilogue has read dP of step gv - 1 out of it.
         auto issue_sdp = [&](int v) -> bool {
-          const int gv = gv0 + v, st = gv % Smem::kSlots, k = gv % Smem::kSSlots;
+          const int gv = gv0 + v, st = gv % Smem::kSlots, k = gv % Smem::kSSlots, j = gv % Smem::kDpSlots;
           if (!mbar_wait(smem_u32(&s.bar_full[st]), (gv / Smem::kSlots) & 1, abort_flag)) return false;
           tc_fence_after();
           const uint64_t b0 = sdesc_advance(ds0, st * Smem::kHalfQ), b1 = sdesc_advance(ds1, st * Smem::kHalfV);
+          if (dkdv) {
 #pragma unroll
-          for (int kk = 0; kk < DPQ / 16; ++kk) {
-            const uint32_t aoff = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-            const uint32_t boff = (kk >> 2) * kHalfChunk + (kk & 3) * 32;
-            umma_ss(tS + 64 * k, sdesc_advance(dr0, aoff), sdesc_advance(b0, boff), idesc_s, kk > 0);
+            for (int kk = 0; kk < DPQ / 16; ++kk) {
+              const uint32_t aoff = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+              const uint32_t boff = (kk >> 2) * kHalfChunk + (kk & 3) * 32;
+              umma_ss(tS + 64 * k, sdesc_advance(dr0, aoff), sdesc_advance(b0, boff), idesc_s, kk > 0);
+            }
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < DPQ / 16; ++kk) {
+              const uint32_t boff = (kk >> 2) * kHalfChunk + (kk & 3) * 32;
+              umma_ts(tS + 64 * k, tQr + 8 * kk, sdesc_advance(b0, boff), idesc_s, kk > 0);
+            }
           }
-          if (gv > 0 && !mbar_wait(smem_u32(&s.bar_dp_free), (gv - 1) & 1, abort_flag)) return false;
+          // dP slot j is free once the epilogue has read out dP of step gv - kDpSlots.
+          if (gv >= Smem::kDpSlots &&
+              !mbar_wait(smem_u32(&s.bar_dp_free[j]), ((gv - Smem::kDpSlots) / Smem::kDpSlots) & 1, abort_flag))
+            return false;
           tc_fence_after();
+          if (dkdv) {
 #pragma unroll
-          for (int kk = 0; kk < DPV / 16; ++kk) {
-            const uint32_t aoff = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-            const uint32_t boff = (kk >> 2) * kHalfChunk + (kk & 3) * 32;
-            umma_ss(tdP, sdesc_advance(dr1, aoff), sdesc_advance(b1, boff), idesc_s, kk > 0);
+            for (int kk = 0; kk < DPV / 16; ++kk) {
+              const uint32_t aoff = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+              const uint32_t boff = (kk >> 2) * kHalfChunk + (kk & 3) * 32;
+              umma_ss(tdP + 64 * j, sdesc_advance(dr1, aoff), sdesc_advance(b1, boff), idesc_s, kk > 0);
+            }
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < DPV / 16; ++kk) {
+              const uint32_t boff = (kk >> 2) * kHalfChunk + (kk & 3) * 32;
+              umma_ts(tdP + 64 * j, tdOr + 8 * kk, sdesc_advance(b1, boff), idesc_s, kk > 0);
+            }
           }
           umma_commit(smem_u32(&s.bar_s_full[k]));
-          if (v == nsteps - 1) umma_commit(smem_u32(&s.bar_res_empty));  // residents free
+          if (dkdv && v == nsteps - 1) umma_commit(smem_u32(&s.bar_res_empty));  // residents free
           return true;
         };
-        // S of step v + 3 reuses the S slot of step v, whose packed P/dS the
-        // accumulating MMAs of step v (issued just before, in order) read.
-        for (int v = 0; ok && v < 3 && v < nsteps; ++v) ok = issue_sdp(v);
+        // S of step v + kSSlots reuses the S slot of step v, whose packed
+        // P/dS the accumulating MMAs of step v (issued just before, in order)
+        // read.
+        for (int v = 0; ok && v < Smem::kSSlots && v < nsteps; ++v) ok = issue_sdp(v);
         for (int v = 0; ok && v < nsteps; ++v) {
           const int gv = gv0 + v, pst = gv % Smem::kSlots, k = gv % Smem::kSSlots;
-          if (v == 0 && res_uses > 0 &&
-              !mbar_wait(smem_u32(&s.bar_acc_empty), (res_uses - 1) & 1, abort_flag)) {
+          if (v == 0 && res_uses > 0 && !handoff_wait(smem_u32(&s.bar_acc_empty), (res_uses - 1) & 1)) {
             ok = false;  // the previous item's accumulators have not been read out
             break;
           }
@@ -445,12 +508,13 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
             }
           }
           umma_commit(smem_u32(&s.bar_empty[pst]));  // this half's slot is free
-          if (v + 3 < nsteps && !issue_sdp(v + 3)) ok = false;
+          if (v + Smem::kSSlots < nsteps && !issue_sdp(v + Smem::kSSlots)) ok = false;
         }
         if (!ok) break;
         umma_commit(smem_u32(&s.bar_acc_full));
         gs += nt;
         ++res_uses;
+        prev_dkdv = dkdv;
       }
       // Arrives once every MMA issued above has completed (also on abort).
       umma_commit(smem_u32(&s.bar_drain));
@@ -514,7 +578,7 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
           }
         }
         const int gv = 2 * (g0 + it) + hh;  // global half-step
-        const int k = gv % Smem::kSSlots;
+        const int k = gv % Smem::kSSlots, j = gv % Smem::kDpSlots;
         const uint32_t xs = tS + 64 * k + lane_addr;
         if (!warp_wait_b(smem_u32(&s.bar_s_full[k]), (gv / Smem::kSSlots) & 1, abort_flag)) {
           ok = false;
@@ -523,14 +587,14 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
         tc_fence_after();
         // All of dP first, so that the dP slot is released for the next step.
         uint32_t dv0[32], dv1[32], sv[32];
-        tmem_ld32(tdP + lane_addr, dv0);
-        tmem_ld32(tdP + lane_addr + 32, dv1);
+        tmem_ld32(tdP + 64 * j + lane_addr, dv0);
+        tmem_ld32(tdP + 64 * j + lane_addr + 32, dv1);
         tmem_ld32(xs, sv);
         tmem_ld_wait(dv0);
         tmem_ld_wait(dv1);
         tmem_ld_wait(sv);
         tc_fence_before();
-        mbar_arrive(smem_u32(&s.bar_dp_free));
+        mbar_arrive(smem_u32(&s.bar_dp_free[j]));
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           const int chunk = 2 * hh + c;  // 32-column chunk of S / dP (of the 128)

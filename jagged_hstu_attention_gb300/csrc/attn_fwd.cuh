@@ -355,8 +355,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1) hstu_fwd_kernel(const __grid_c
           }
           if (t >= 2) {
             const int pt = t - 2, gg = g + pt, psb = gg % 3, pkst = gg % NS;
+            // The wait for the epilogue to have read out the previous item's O
+            // (limit p.handoff_limit_ns; 1 ns, set only by a test, gives up at
+            // once so that the abort path runs with copies and MMAs in flight).
             if (pt == 0 && q_uses > 0 &&
-                !mbar_wait(smem_u32(&s.bar_o_empty), (q_uses - 1) & 1, abort_flag)) {
+                (p.handoff_limit_ns <= 1 ||
+                 !mbar_wait(smem_u32(&s.bar_o_empty), (q_uses - 1) & 1, abort_flag, p.handoff_limit_ns))) {
+              *abort_flag = 1;
               ok = false;  // the previous item's O has not been read out
               break;
             }

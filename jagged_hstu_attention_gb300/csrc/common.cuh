@@ -133,6 +133,10 @@ struct AttnParams {
   int64_t total;
   int32_t heads, dim, dim_v, nt, max_seqlen;  // dim = D_qk, dim_v = D_v
   float alpha, inv_n;
+  // Limit of the MMA thread's wait for the epilogue to have read out the
+  // previous item's accumulators (kWaitLimitNs unless a test shortens it to
+  // make that wait run out with copies and MMAs in flight).
+  uint64_t handoff_limit_ns;
 };
 
 struct TgtParams {

@@ -231,6 +231,17 @@ __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// Copies 128 rows x 32 bytes of a shared-memory operand, described by a
+// UMMA descriptor (swizzle and strides as for an MMA operand), into TMEM
+// lanes 0..127, 8 consecutive 32-bit columns from taddr: the layout a
+// kind::f16 MMA reads its A operand in when A comes from TMEM (lane = row,
+// column c = elements 2c and 2c + 1 of the 16 K elements). Asynchronous,
+// issued by one thread; MMAs issued after it by the same thread see the
+// copied data, and tcgen05.commit tracks its completion.
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
 // Arrives once on the mbarrier when every previously issued tcgen05 op of
 // this thread has completed.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {

@@ -163,3 +163,10 @@ def test_build_func_rejects_bad_arguments_on_the_host(lib):
     assert lib.hstu_attn_build_func_candidates(None, 2, 1, fake, None) == 1
     assert lib.hstu_attn_build_func_candidates(fake, 2, 2, fake, None) == 2
     assert lib.hstu_attn_build_func_candidates(fake, 0, 1, fake, None) == 1
+
+
+def test_handoff_limit_hook_rejects_out_of_range(lib):
+    with pytest.raises(hb.HstuError):
+        hb.set_handoff_limit_for_tests(3_000_000_000)
+    hb.set_handoff_limit_for_tests(5)
+    hb.set_handoff_limit_for_tests(0)  # back to the kernels' normal limit
