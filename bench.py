@@ -52,10 +52,10 @@ L2_FLUSH_BYTES = 512 << 20
 # in proportion to the tokens of a launch; it is reported only while the
 # sources are unchanged.
 NCU_TRAFFIC = {
-    "causal": {"bytes_per_token": (723308288 + 498629888) / 172107,
+    "causal": {"bytes_per_token": (722410240 + 498844928) / 172107,
                "captured_on": "hstu_bwd_kernel on dlrm_b1024@b64 (172,107 tokens, same length mix and mask), "
                               "dram__bytes_read.sum + dram__bytes_write.sum, scaled by tokens",
-               "sources_sha": "9f5e4609dafe54bb"},
+               "sources_sha": "8b7c33a6e6942892"},
 }
 
 
@@ -501,6 +501,90 @@ def measure_targets(k, v, lens, N, steps, warmup, flush, seed):
             "T": T, "B": B, "H": H, "D": D, "launches": 4 * steps}
 
 
+def measure_layer(leg, steps, warmup, flush, seed, d_model=512):
+    """The last HSTU layer's input projection plus attention, full length
+    against targets-only, fwd + bwd (MLCommons training PR #903, layer-timing
+    table: 512-dim layer, 4 heads, qk and linear dim 128).
+
+      full     project all T rows to U, V, Q, K (silu(x W_uvqk^T + b), 4 H D
+               outputs), attention over every row (plan, forward, backward),
+               the projection's backward;
+      targets  project all rows to K, V, only the candidate rows to U, Q,
+               targets-only attention, both projections' backward.
+
+    The attention runs on the leg's resident q, k, v, dO (the projections'
+    outputs have their shapes); the rest of the layer (normalisation, output
+    projection) is the same in both arms and left out."""
+    import torch
+    from jagged_hstu_attention_gb300 import binding as hb
+    from jagged_hstu_attention_gb300 import workloads as wl
+    device = leg.q.device
+    T, H, D = leg.T, leg.cfg.heads, leg.cfg.dim
+    B = len(leg.lens)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed + 2000)
+    x = wl.randn_bf16((T, d_model), gen, device)
+    w_all = (wl.randn_bf16((4 * H * D, d_model), gen, device).float() / math.sqrt(d_model)).to(torch.bfloat16)
+    b_all = torch.zeros(4 * H * D, dtype=torch.bfloat16, device=device)
+    w_kv, w_uq = w_all[: 2 * H * D].contiguous(), w_all[2 * H * D:].contiguous()
+    b_kv, b_uq = b_all[: 2 * H * D].contiguous(), b_all[2 * H * D:].contiguous()
+    cand = torch.tensor(leg.offsets[1:] - 1, dtype=torch.int32, device=device)
+    ws_f = hb.project_workspace(0, d_model, 4 * H * D, False, device)
+    ws_fb = hb.project_workspace(T, d_model, 4 * H * D, True, device)
+    dy_all = wl.randn_bf16((T, 4 * H * D), gen, device)
+    ws_kv = hb.project_workspace(0, d_model, 2 * H * D, False, device)
+    ws_kvb = hb.project_workspace(T, d_model, 2 * H * D, True, device)
+    ws_uq = hb.project_workspace(B, d_model, 2 * H * D, False, device)
+    ws_uqb = hb.project_workspace(B, d_model, 2 * H * D, True, device)
+    dy_kv = dy_all[:, : 2 * H * D].contiguous()
+    dy_uq = wl.randn_bf16((B, 2 * H * D), gen, device)
+    q_c = leg.q.index_select(0, cand.long()).contiguous()
+    do_c = leg.do.index_select(0, cand.long()).contiguous()
+    fc = hb.build_func_candidates(leg.d_off, 1)
+    tws = hb.alloc_workspace(hb.make_shape(B, T, H, D, 1, leg.N, leg.alpha), hb.WS_TARGETS, device)
+    o_c, dq_c = torch.empty_like(q_c), torch.empty_like(q_c)
+
+    def full(ev):
+        ev[0].record()
+        y, z = hb.project_rows(x, w_all, bias=b_all, ws=ws_f)
+        leg.step([torch.cuda.Event(enable_timing=True) for _ in range(4)])
+        hb.project_rows_bwd(dy_all, z, x, w_all, ws=ws_fb)
+        ev[1].record()
+
+    def targets(ev):
+        ev[0].record()
+        _, z_kv = hb.project_rows(x, w_kv, bias=b_kv, ws=ws_kv)
+        _, z_uq = hb.project_rows(x, w_uq, rows=cand, bias=b_uq, ws=ws_uq)
+        hb.fwd_targets_only(q_c, leg.k, leg.v, leg.d_off, fc, leg.N, leg.alpha, ws=tws, out=o_c)
+        hb.bwd_targets_only(do_c, q_c, leg.k, leg.v, leg.d_off, fc, leg.N, leg.alpha, ws=tws,
+                            outs=(dq_c, leg.dk, leg.dv))
+        hb.project_rows_bwd(dy_kv, z_kv, x, w_kv, ws=ws_kvb)
+        hb.project_rows_bwd(dy_uq, z_uq, x, w_uq, rows=cand, ws=ws_uqb)
+        ev[1].record()
+
+    res = {}
+    for name, fn in (("full", full), ("targets_only", targets)):
+        for _ in range(warmup):
+            fn([torch.cuda.Event(enable_timing=True) for _ in range(2)])
+        torch.cuda.synchronize()
+        recs = []
+        for _ in range(steps):
+            flush.zero_()
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            fn(ev)
+            recs.append(ev)
+        torch.cuda.synchronize()
+        res[name] = statistics.mean(e[0].elapsed_time(e[1]) for e in recs)
+    if hb.device_status(tws) != hb.HSTU_OK:
+        raise RuntimeError("targets-only reported a device-side error")
+    gemm_flops = 2.0 * T * d_model * 4 * H * D
+    return {"d_model": d_model, "full_ms": res["full"], "targets_only_ms": res["targets_only"],
+            "speedup": res["full"] / res["targets_only"],
+            "projection_gflop_fwd_full": gemm_flops / 1e9,
+            "parts": "input projection (fwd+bwd, tcgen05 GEMMs) + attention (fwd+bwd)",
+            "source": "MLCommons training PR #903 layer-timing table shape: 512-dim layer, 4 heads, dims 128"}
+
+
 def run_targets(args, cfg, device, world, rank):
     """Targets-only mode as a line of its own: HBM-bound, reported as
     achieved bytes/s against the measured copy bandwidth."""
@@ -708,6 +792,8 @@ def main():
         if rank == 0 and cfg.mask == "causal":
             extras["targets"] = measure_targets(leg_main.k, leg_main.v, leg_main.lens, leg_main.N, args.steps,
                                                 args.warmup, flush, seed)
+            extras["layer"] = measure_layer(leg_main, max(3, args.steps // 4), 2, flush, seed)
+            torch.cuda.empty_cache()
         if rank == 0 and not padding_inline:
             pcfg = wl.CONFIGS[PADDING_CONFIG]
             p5 = Leg(pcfg, args.seed, 5, device)
@@ -764,6 +850,8 @@ def main():
             "hbm_frac": gbs / peaks["hbm_gbs"], "peak_gbs": peaks["hbm_gbs"],
             "speedup_vs_full_step": ms_step / m["ms"], "candidates_per_seq": 1,
             "algorithmic_bytes": m["bytes"], "gpu_launches": m["launches"]}
+    if "layer" in extras:
+        line["layer"] = extras["layer"]
     if not args.no_cpu_baseline:
         f, s, n, nb, pairs = oracle_sample(cfg, seed, args.cpu_budget,
                                            order="random" if cfg.batch > 64 else "longest")

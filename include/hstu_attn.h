@@ -243,10 +243,11 @@ HSTU_API hstu_status_t hstu_attn_project_rows_bwd(const void* dy, const void* z,
  *   - All calls on a device share the array, which keeps the last call's
  *     contents; each call clears what must start at zero. Calls whose work
  *     overlaps on the GPU (for example on two streams at once) race on it.
- *   - Device-side input errors are read with
- *     hstu_attn_get_device_status(ws) where ws is that array; there is no
- *     handle to it, so this entry point is for callers that validate
- *     seq_offsets themselves. */
+ *   - Errors found on the device (bad seq_offsets, a timed-out wait) are
+ *     recorded in the array's error word, which a caller cannot read: there
+ *     is no handle to it. On such an error o is left unwritten. This entry
+ *     point is for callers that validate seq_offsets themselves; one that
+ *     needs the device status uses hstu_attn_fwd with its own workspace. */
 HSTU_API hstu_status_t hstu_attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o,
                                              const int32_t* seq_offsets, const int32_t* func,
                                              const hstu_attn_shape_t* shape, int32_t* row_counts,

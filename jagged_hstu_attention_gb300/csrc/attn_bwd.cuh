@@ -71,7 +71,11 @@ namespace hstu {
 // One work item as the producer publishes it to the other roles.
 struct BwdItem {
   int dkdv, b, tile, h, o0, L, nt;
-  uint16_t idx[kMaxTiles];  // visiting (dK/dV) or visited (dQ) tile | 0x100 if partial
+  int nhs;  // streamed 64-row halves (half-steps) of the item: dead halves are left out
+  // visiting (dK/dV) or visited (dQ) tile | 0x100 if partial | 0x200 / 0x400
+  // if its streamed half 0 / 1 is dead (dK/dV: q rows that see no column of
+  // the kv tile; dQ: kv columns no row of the q tile sees)
+  uint16_t idx[kMaxTiles];
 };
 
 template <int DPQ, int DPV>
@@ -266,7 +270,7 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
     int str_last[Smem::kSlots];  // last use of each ring slot, -1 if never used
     for (int st = 0; st < Smem::kSlots; ++st) str_last[st] = -1;
     int res_uses = 0;  // items with at least one tile (one resident load each)
-    int gs = 0;        // streamed tiles over all items
+    int ghs = 0;       // streamed halves over all items
     bool ok = true;
     int i = 0;
     for (; ok; ++i) {
@@ -301,17 +305,21 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
       BwdItem& it_slot = s.item[slot];
       // dK/dV: q tiles visiting kv tile `tile` (a column of the class matrix);
       // dQ: kv tiles visited by q tile `tile` (a row of it).
-      int n = 0;
+      int n = 0, nhs = 0;
       for (int base = 0; base < ntiles_b; base += 32) {
         const int x = base + lane;
-        uint8_t c = kSkip;
+        uint8_t cb = kSkip;
         if (x < ntiles_b)
-          c = dkdv ? cls_b[static_cast<size_t>(x) * nt_all + tile] : cls_b[static_cast<size_t>(tile) * nt_all + x];
+          cb = dkdv ? cls_b[static_cast<size_t>(x) * nt_all + tile] : cls_b[static_cast<size_t>(tile) * nt_all + x];
+        const uint8_t c = cb & kClassMask;
+        const int dead0 = (cb & (dkdv ? kLoQDead : kLoKvDead)) ? 1 : 0;
+        const int dead1 = (cb & (dkdv ? kHiQDead : kHiKvDead)) ? 1 : 0;
         const unsigned m = __ballot_sync(0xffffffffu, c != kSkip);
         if (c != kSkip)
           it_slot.idx[n + __popc(m & ((1u << lane) - 1u))] =
-              static_cast<uint16_t>(x | (c == kPartial ? 0x100 : 0));
+              static_cast<uint16_t>(x | (c == kPartial ? 0x100 : 0) | (dead0 << 9) | (dead1 << 10));
         n += __popc(m);
+        nhs += __reduce_add_sync(0xffffffffu, c != kSkip ? 2 - dead0 - dead1 : 0);
       }
       if (lane == 0) {
         it_slot.dkdv = dkdv ? 1 : 0;
@@ -321,6 +329,7 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
         it_slot.o0 = o0;
         it_slot.L = L;
         it_slot.nt = n;
+        it_slot.nhs = nhs;
       }
       __threadfence_block();
       __syncwarp();
@@ -341,20 +350,21 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
             tma_load_4d(smem_u32(s.res1), m_res1, br, 0, row0, h, 0);
             ++res_uses;
           }
-          for (int t = 0; ok && t < 2 * n; ++t) {  // 64-row halves
-            const int gh = 2 * gs + t, st = gh % Smem::kSlots, use = gh / Smem::kSlots;
+          for (int t = 0; ok && t < 2 * n; ++t) {  // 64-row halves that are not dead
+            const int e = it_slot.idx[t >> 1];
+            if (e & (0x200 << (t & 1))) continue;
+            const int gh = ghs++, st = gh % Smem::kSlots, use = gh / Smem::kSlots;
             if (use > 0 && !mbar_wait(smem_u32(&s.bar_empty[st]), (use - 1) & 1, abort_flag)) {
               ok = false;
               break;
             }
-            const int srow0 = o0 + (it_slot.idx[t >> 1] & 0xff) * kBlock + (t & 1) * (kBlock / 2);
+            const int srow0 = o0 + (e & 0xff) * kBlock + (t & 1) * (kBlock / 2);
             const uint32_t bar = smem_u32(&s.bar_full[st]);
             mbar_expect_tx(bar, Smem::kHalfQ + Smem::kHalfV);
             tma_load_4d(smem_u32(s.str0[st]), m_str0, bar, 0, srow0, h, 0);
             tma_load_4d(smem_u32(s.str1[st]), m_str1, bar, 0, srow0, h, 0);
             str_last[st] = use;
           }
-          gs += n;
         }
       }
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -398,7 +408,7 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
         }
         return mbar_wait(bar, parity, abort_flag, p.handoff_limit_ns);
       };
-      int gs = 0;        // streamed tiles over all items
+      int ghs = 0;       // half-steps over all items
       int res_uses = 0;  // items with at least one tile
       bool prev_dkdv = false;  // role of the previous item with at least one tile
       bool ok = true;
@@ -429,8 +439,8 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
             tmem_cp_128x256b(tdOr + 8 * kk, sdesc_advance(dr1, (kk >> 2) * kChunkBytes + (kk & 3) * 32));
           umma_commit(smem_u32(&s.bar_res_empty));  // shared-memory residents free once copied
         }
-        const int nsteps = 2 * nt;
-        const int gv0 = 2 * gs;  // global index of this item's first half-step
+        const int nsteps = s.item[slot].nhs;
+        const int gv0 = ghs;  // global index of this item's first half-step
         // S/dP of step v (N = 64 MMAs): S (or S^T) = res0 . str0_h^T into S
         // slot gv % 3, dP (or dP^T) = res1 . str1_h^T into the dP slot once
         // the epilogue has read dP of step gv - 1 out of it.
@@ -512,7 +522,7 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
         }
         if (!ok) break;
         umma_commit(smem_u32(&s.bar_acc_full));
-        gs += nt;
+        ghs += nsteps;
         ++res_uses;
         prev_dkdv = dkdv;
       }
@@ -530,8 +540,8 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
     const float out_scale = 0.5f * p.alpha * p.inv_n;  // hc = alpha / (2N)
     // 32-byte stores need every output row to start on a 32-byte boundary.
     const bool wide = wide_rows_ok(p.out0, p.out1, p.out2, p.dim, p.dim_v);
-    const int hh = half;  // this warp group converts half `half` of every tile
-    int g0 = 0;           // tiles over all items
+    const int hh = half;  // this warp group takes the half-steps whose global index has parity hh
+    int g0 = 0;           // half-steps over all items
     int acc_uses = 0;
     bool ok = true;
     int i = 0;
@@ -549,17 +559,26 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
       if (!dkdv)
         load_row_intervals<NINT>(p.func, p.total, static_cast<int64_t>(o0) + own_loc, L, valid, lo, hi,
                                  iv_b[tile]);
-      for (int it = 0; it < nt; ++it) {
-        const int other = item.idx[it] & 0xff;
-        const bool partial = (item.idx[it] & 0x100) != 0;
+      // Walk the item's half-steps in order (dead halves are not streamed);
+      // this group takes those with an odd or even global index, hh.
+      int lhs = 0;  // half-steps of this item so far
+      for (int hs_t = 0; ok && hs_t < 2 * nt; ++hs_t) {
+        const int it = hs_t >> 1, hsel = hs_t & 1;  // tile entry and its half
+        const int e = item.idx[it];
+        if (e & (0x200 << hsel)) continue;  // dead half
+        const int gv = g0 + lhs++;          // global half-step
+        if ((gv & 1) != hh) continue;       // the other group's
+        const int other = e & 0xff;
+        const bool partial = (e & 0x100) != 0;
         uint32_t qmask0 = 0, qmask1 = 0;
         if (dkdv && partial) {
-          // Lane l takes q rows 64h + l and 64h + 32 + l of the visiting q
-          // tile and finds which of this warp's 32 kv rows each of them sees;
-          // one ballot per kv row turns the bits around, so that lane j holds
-          // the q-row masks of kv row 32 quarter + j for both chunks of half h.
+          // Lane l takes q rows 64 hsel + l and 64 hsel + 32 + l of the
+          // visiting q tile and finds which of this warp's 32 kv rows each of
+          // them sees; one ballot per kv row turns the bits around, so that
+          // lane j holds the q-row masks of kv row 32 quarter + j for both
+          // chunks of the half.
           int flo[NINT], fhi[NINT];
-          const int qa = other * kBlock + 64 * hh + lane;
+          const int qa = other * kBlock + 64 * hsel + lane;
           const int kv0 = tile * kBlock + 32 * quarter;
           load_row_intervals<NINT>(p.func, p.total, static_cast<int64_t>(o0) + qa, L, qa < L, flo, fhi,
                                    iv_b[other]);
@@ -577,7 +596,6 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
             }
           }
         }
-        const int gv = 2 * (g0 + it) + hh;  // global half-step
         const int k = gv % Smem::kSSlots, j = gv % Smem::kDpSlots;
         const uint32_t xs = tS + 64 * k + lane_addr;
         if (!warp_wait_b(smem_u32(&s.bar_s_full[k]), (gv / Smem::kSSlots) & 1, abort_flag)) {
@@ -597,7 +615,7 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
         mbar_arrive(smem_u32(&s.bar_dp_free[j]));
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          const int chunk = 2 * hh + c;  // 32-column chunk of S / dP (of the 128)
+          const int chunk = 2 * hsel + c;  // 32-column chunk of the tile's 128
           if (c == 1) {
             tmem_ld32(xs + 32, sv);
             tmem_ld_wait(sv);
@@ -639,7 +657,7 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
         ++acc_uses;
       }
       mbar_arrive(smem_u32(&s.bar_item_empty[slot]));
-      g0 += nt;
+      g0 += lhs;
     }
   }
 

@@ -101,12 +101,15 @@ __device__ __forceinline__ void silu_pack32(const uint32_t (&s)[32], uint32_t ma
   }
 }
 
-// Epilogue of one 128 x 128 S tile for this warp's 32 rows (all 128 columns).
-template <typename T, int NINT, bool MASKED>
+// Epilogue of one S tile for this warp's 32 rows: HALVES = 2 for all 128
+// columns, 1 for a tile whose other 64-column half no row sees (its S MMA
+// computed the live half alone into the first 64 columns; col0 is that
+// half's first column).
+template <typename T, int NINT, bool MASKED, int HALVES = 2>
 __device__ __forceinline__ void fwd_tile_epilogue(uint32_t sb, int col0, const int (&lo)[NINT],
                                                   const int (&hi)[NINT], float half_alpha) {
 #pragma unroll
-  for (int hf = 0; hf < 2; ++hf) {
+  for (int hf = 0; hf < HALVES; ++hf) {
     uint32_t a[32], c[32];
     tmem_ld32(sb + hf * 64, a);
     tmem_ld32(sb + hf * 64 + 32, c);
@@ -225,11 +228,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1) hstu_fwd_kernel(const __grid_c
       int n = 0;
       for (int base = 0; base < ntiles_b; base += 32) {
         const int j = base + lane;
-        const uint8_t c = j < ntiles_b ? cls_row[j] : kSkip;
+        const uint8_t cb = j < ntiles_b ? cls_row[j] : kSkip;
+        const uint8_t c = cb & kClassMask;
         const unsigned m = __ballot_sync(0xffffffffu, c != kSkip);
+        // entry: kv tile | 0x100 partial | 0x200 / 0x400 its columns 0..63 /
+        // 64..127 seen by no row of the q tile
         if (c != kSkip)
           it_slot.tile[n + __popc(m & ((1u << lane) - 1u))] =
-              static_cast<uint16_t>(j | (c == kPartial ? 0x100 : 0));
+              static_cast<uint16_t>(j | (c == kPartial ? 0x100 : 0) | ((cb & kLoKvDead) ? 0x200 : 0) |
+                                    ((cb & kHiKvDead) ? 0x400 : 0));
         n += __popc(m);
       }
       if (lane == 0) {
@@ -317,6 +324,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) hstu_fwd_kernel(const __grid_c
     // ------------------------------------------------------------ MMA issuer
     if (elect_one_sync()) {
       constexpr uint32_t idesc_s = idesc_f16kind(128, 128, false, false, Elem<T>::kUmma);
+      constexpr uint32_t idesc_s64 = idesc_f16kind(128, 64, false, false, Elem<T>::kUmma);
       constexpr uint32_t idesc_o = idesc_f16kind(128, DPV, false, true, Elem<T>::kUmma);
       // Descriptors are built once; each MMA only advances a start address.
       const uint64_t dq = sdesc_sw128(smem_u32(s.q), 16, 1024);
@@ -344,10 +352,22 @@ __global__ void __launch_bounds__(kFwdThreads, 1) hstu_fwd_kernel(const __grid_c
             tc_fence_after();
             const uint64_t dk = sdesc_advance(dk0, kst * kTileQ);
             const uint32_t d_tmem = tbase + sb * 128;
+            const int entry = s.item[slot].tile[t];
+            if (entry & 0x600) {
+              // One live 64-row half of the K tile: an N=64 MMA into the
+              // buffer's first 64 columns.
+              const uint32_t live = (entry & 0x200) ? 64u * 128u : 0u;
 #pragma unroll
-            for (int kk = 0; kk < DPQ / 16; ++kk) {
-              const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-              umma_ss(d_tmem, sdesc_advance(dq, off), sdesc_advance(dk, off), idesc_s, kk > 0);
+              for (int kk = 0; kk < DPQ / 16; ++kk) {
+                const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+                umma_ss(d_tmem, sdesc_advance(dq, off), sdesc_advance(dk, off + live), idesc_s64, kk > 0);
+              }
+            } else {
+#pragma unroll
+              for (int kk = 0; kk < DPQ / 16; ++kk) {
+                const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+                umma_ss(d_tmem, sdesc_advance(dq, off), sdesc_advance(dk, off), idesc_s, kk > 0);
+              }
             }
             umma_commit(smem_u32(&s.bar_s_full[sb]));
             umma_commit(smem_u32(&s.bar_k_empty[kst]));  // K stage free once QK^T is done
@@ -373,10 +393,20 @@ __global__ void __launch_bounds__(kFwdThreads, 1) hstu_fwd_kernel(const __grid_c
             tc_fence_after();
             const uint64_t dv = sdesc_advance(dv0, pkst * kTileV);
             const uint32_t a_tmem = tbase + psb * 128;
-            umma_ts(tO, a_tmem, dv, idesc_o, pt > 0 ? 1u : 0u);
+            const int pentry = s.item[slot].tile[pt];
+            if (pentry & 0x600) {
+              // The live half's 64 V rows: four K steps.
+              const uint32_t live = (pentry & 0x200) ? 64u : 0u;
 #pragma unroll
-            for (int kk = 1; kk < kBlock / 16; ++kk)
-              umma_ts(tO, a_tmem + kk * 8, sdesc_advance(dv, kk * 16 * 128), idesc_o, 1u);
+              for (int kk = 0; kk < kBlock / 32; ++kk)
+                umma_ts(tO, a_tmem + kk * 8, sdesc_advance(dv, (live + kk * 16) * 128), idesc_o,
+                        (pt > 0 || kk > 0) ? 1u : 0u);
+            } else {
+              umma_ts(tO, a_tmem, dv, idesc_o, pt > 0 ? 1u : 0u);
+#pragma unroll
+              for (int kk = 1; kk < kBlock / 16; ++kk)
+                umma_ts(tO, a_tmem + kk * 8, sdesc_advance(dv, kk * 16 * 128), idesc_o, 1u);
+            }
             umma_commit(smem_u32(&s.bar_v_empty[pkst]));
           }
         }
@@ -419,8 +449,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1) hstu_fwd_kernel(const __grid_c
         tc_fence_after();
         const int tile = item.tile[t];
         const uint32_t sb = tbase + lane_addr + sbuf * 128;
-        if (tile & 0x100) fwd_tile_epilogue<T, NINT, true>(sb, (tile & 0xff) * kBlock, lo, hi, half_alpha);
-        else fwd_tile_epilogue<T, NINT, false>(sb, (tile & 0xff) * kBlock, lo, hi, half_alpha);
+        if (tile & 0x600) {  // a half tile (partial by construction): its live 64 columns
+          const int col0 = (tile & 0xff) * kBlock + ((tile & 0x200) ? kBlock / 2 : 0);
+          fwd_tile_epilogue<T, NINT, true, 1>(sb, col0, lo, hi, half_alpha);
+        } else if (tile & 0x100) {
+          fwd_tile_epilogue<T, NINT, true>(sb, (tile & 0xff) * kBlock, lo, hi, half_alpha);
+        } else {
+          fwd_tile_epilogue<T, NINT, false>(sb, (tile & 0xff) * kBlock, lo, hi, half_alpha);
+        }
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(smem_u32(&s.bar_p_full[sbuf]));

@@ -38,8 +38,11 @@ constexpr int kHdrWords = 64;  // 256 bytes
 constexpr int kErrInput = 1;
 constexpr int kErrTimeout = 2;
 
-// Tile classes written by the plan.
-constexpr uint8_t kSkip = 0, kPartial = 1, kFull = 2;
+// Tile classes written by the plan (bits 0-1), with the dead 64-wide halves
+// of a partial pair: kv columns 0..63 / 64..127 seen by no row, q rows
+// 0..63 / 64..127 seeing no column of the tile.
+constexpr uint8_t kSkip = 0, kPartial = 1, kFull = 2, kClassMask = 3;
+constexpr uint8_t kLoKvDead = 4, kHiKvDead = 8, kLoQDead = 16, kHiQDead = 32;
 
 // Backward work-list entries: bit 30 = role (1: dK/dV for a kv tile,
 // 0: dQ for a q tile), bits 8..29 = sequence, bits 0..7 = tile.

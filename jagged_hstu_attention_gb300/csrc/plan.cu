@@ -16,6 +16,11 @@
 //   skip    -- no valid row sees any column of the tile,
 //   full    -- every row of the q tile is valid and sees all 128 columns,
 //   partial -- anything else (the kernels then apply the per-row mask).
+// A partial pair also records which 64-wide halves are dead: the kv half no
+// row sees (kLoKvDead / kHiKvDead) and the q half that sees no column of the
+// tile (kLoQDead / kHiQDead). The kernels skip the MMAs and the epilogue of a
+// dead half; on a causal window of 32 columns that saves one half-tile of
+// every four.
 #include "common.cuh"
 #include "internal.h"
 
@@ -35,13 +40,17 @@ __device__ void classify_tile(const PlanParams& p, int b, int qt) {
   const int ntiles = (L + kBlock - 1) / kBlock;
   if (qt >= ntiles) return;
 
-  __shared__ uint32_t any_bits[4][kMaxTiles / 32];
+  // Per warp (32 rows) and kv tile: some row sees kv columns 0..63 (lo),
+  // 64..127 (hi); every row sees all 128 (all).
   __shared__ uint32_t all_bits[4][kMaxTiles / 32];
+  __shared__ uint32_t lo_bits[4][kMaxTiles / 32];
+  __shared__ uint32_t hi_bits[4][kMaxTiles / 32];
   __shared__ uint32_t active_iv;
   if (tid == 0) active_iv = 0;
   for (int x = tid; x < 4 * (kMaxTiles / 32); x += 128) {
-    (&any_bits[0][0])[x] = 0;
     (&all_bits[0][0])[x] = 0;
+    (&lo_bits[0][0])[x] = 0;
+    (&hi_bits[0][0])[x] = 0;
   }
   __syncthreads();
 
@@ -67,17 +76,21 @@ __device__ void classify_tile(const PlanParams& p, int b, int qt) {
       none = none && (hi[t] <= s0 || lo[t] >= s0 + kBlock);
       cover = cover || (lo[t] <= s0 && hi[t] >= s0 + kBlock);
     }
-    int c = cover ? kBlock : 0;
+    int c_lo = cover ? kBlock / 2 : 0, c_hi = c_lo;
     if (!cover && !none) {
-#pragma unroll
-      for (int w = 0; w < 4; ++w) c += __popc(row_mask_word<NINT>(lo, hi, s0 + 32 * w));
+      c_lo = __popc(row_mask_word<NINT>(lo, hi, s0)) + __popc(row_mask_word<NINT>(lo, hi, s0 + 32));
+      c_hi = __popc(row_mask_word<NINT>(lo, hi, s0 + 64)) + __popc(row_mask_word<NINT>(lo, hi, s0 + 96));
     }
+    const int c = c_lo + c_hi;
     count += c;
-    const unsigned any = __ballot_sync(0xffffffffu, c > 0);
     const unsigned all = __ballot_sync(0xffffffffu, c == kBlock);
+    const unsigned any_lo = __ballot_sync(0xffffffffu, c_lo > 0);
+    const unsigned any_hi = __ballot_sync(0xffffffffu, c_hi > 0);
     if (lane == 0) {
-      if (any) any_bits[warp][j >> 5] |= 1u << (j & 31);
-      if (all == 0xffffffffu) all_bits[warp][j >> 5] |= 1u << (j & 31);
+      const uint32_t bit = 1u << (j & 31);
+      if (all == 0xffffffffu) all_bits[warp][j >> 5] |= bit;
+      if (any_lo) lo_bits[warp][j >> 5] |= bit;
+      if (any_hi) hi_bits[warp][j >> 5] |= bit;
     }
   }
   if (valid && p.row_counts) p.row_counts[o0 + i] = count;
@@ -87,11 +100,22 @@ __device__ void classify_tile(const PlanParams& p, int b, int qt) {
   for (int j = tid; j < ntiles; j += 128) {
     const uint32_t bit = 1u << (j & 31);
     const int word = j >> 5;
-    const bool any = ((any_bits[0][word] | any_bits[1][word] | any_bits[2][word] |
-                       any_bits[3][word]) & bit) != 0;
+    uint32_t wany[4];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) wany[w] = lo_bits[w][word] | hi_bits[w][word];
+    const bool any = ((wany[0] | wany[1] | wany[2] | wany[3]) & bit) != 0;
     const bool all = ((all_bits[0][word] & all_bits[1][word] & all_bits[2][word] &
                        all_bits[3][word]) & bit) != 0;
-    p.cls[row_base + j] = all ? kFull : (any ? kPartial : kSkip);
+    uint8_t c = all ? kFull : (any ? kPartial : kSkip);
+    if (c == kPartial) {
+      const uint32_t lo_kv = lo_bits[0][word] | lo_bits[1][word] | lo_bits[2][word] | lo_bits[3][word];
+      const uint32_t hi_kv = hi_bits[0][word] | hi_bits[1][word] | hi_bits[2][word] | hi_bits[3][word];
+      if (!(lo_kv & bit)) c |= kLoKvDead;
+      if (!(hi_kv & bit)) c |= kHiKvDead;
+      if (!((wany[0] | wany[1]) & bit)) c |= kLoQDead;  // q rows 0..63
+      if (!((wany[2] | wany[3]) & bit)) c |= kHiQDead;  // q rows 64..127
+    }
+    p.cls[row_base + j] = c;
   }
   if (tid == 0) p.ivmask[static_cast<size_t>(b) * p.nt + qt] = static_cast<uint8_t>(active_iv);
 }

@@ -15,10 +15,14 @@
 // and B come from row-major 2-D tensors; an operand is K-major when K runs
 // along the tensor's rows (A = X_c, A = G, B = W in the forward) and
 // MN-major when K runs down its columns (B = W in dX_c; A = G and B = X_c in
-// dW). Tiles of 128 x 256 outputs, 64-deep K blocks through a 3-stage TMA
+// dW). Tiles of 128 x 256 outputs, 64-deep K blocks through a 2-stage TMA
 // ring (48 KB a stage, 128-byte swizzle), one elected thread issuing
 // M=128, N=256, K=16 MMAs, four epilogue warps reading the accumulator out
-// of TMEM, one row per thread.
+// of TMEM, one row per thread. Two CTAs share an SM (96 KB of shared memory
+// and 256 TMEM columns each), so one CTA's epilogue overlaps the other's
+// main loop. dW, whose K is the number of rows, splits K over up to eight
+// CTAs per output tile; their fp32 partial tiles are summed in split order
+// (deterministic) by a fold kernel.
 #include <cudaTypedefs.h>
 
 #include <atomic>
@@ -31,12 +35,15 @@ namespace hstu {
 
 namespace {
 
-constexpr int kGemmBM = 128, kGemmBN = 256, kGemmBK = 64, kGemmStages = 3;
+constexpr int kGemmBM = 128, kGemmBN = 256, kGemmBK = 64, kGemmStages = 2;
+constexpr int kMaxKSplits = 8;
+constexpr int kGradRows = 1024;  // rows of one chunk of the bias gradient's partial sums
 constexpr int kGemmThreads = 192;  // warps 0-3 epilogue, 4 TMA producer, 5 MMA issuer
 
 // Epilogues.
 constexpr int kEpiStore = 0;     // out = acc
 constexpr int kEpiBiasSilu = 1;  // z = acc + bias; out = silu(z); out2 = z (optional)
+constexpr int kEpiPartial = 2;   // partial[split] = acc in fp32 (split K)
 
 struct GemmParams {
   CUtensorMap tm_a, tm_b;
@@ -44,7 +51,8 @@ struct GemmParams {
   void* out2;
   const void* bias;
   int32_t* err;  // error word (nullable): kErrTimeout on a timed-out wait
-  int32_t M, N, K, ldo;
+  float* partial;  // kEpiPartial: (k_splits, M, N) fp32
+  int32_t M, N, K, ldo, k_splits;
 };
 
 struct GemmSmem {
@@ -90,12 +98,17 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t base, int kk) {
 }
 
 template <typename T, bool A_MN, bool B_MN, int EPI>
-__global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
+__global__ void __launch_bounds__(kGemmThreads, 2) gemm_kernel(const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   GemmSmem& s = *reinterpret_cast<GemmSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m0 = blockIdx.x * kGemmBM, n0 = blockIdx.y * kGemmBN;
-  const int nk = (p.K + kGemmBK - 1) / kGemmBK;
+  // This CTA's K blocks: split blockIdx.z of k_splits (all of K without a split).
+  const int nk_all = (p.K + kGemmBK - 1) / kGemmBK;
+  const int per = (nk_all + p.k_splits - 1) / p.k_splits;
+  const int kb0 = static_cast<int>(blockIdx.z) * per;
+  const int kb1 = kb0 + per < nk_all ? kb0 + per : nk_all;
+  const int nk = kb1 > kb0 ? kb1 - kb0 : 0;
   constexpr uint32_t kStageBytes = (kGemmBM + kGemmBN) * kGemmBK * 2;
   if (threadIdx.x == 0) {
     s.abort_flag = 0;
@@ -122,14 +135,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     if (lane == 0) {
       tma_prefetch_map(&p.tm_a);
       tma_prefetch_map(&p.tm_b);
-      int last[kGemmStages] = {-1, -1, -1};
+      int last[kGemmStages];
+      for (int st = 0; st < kGemmStages; ++st) last[st] = -1;
       for (int kb = 0; kb < nk; ++kb) {
         const int st = kb % kGemmStages, use = kb / kGemmStages;
         if (use > 0 && !mbar_wait(smem_u32(&s.bar_empty[st]), (use - 1) & 1, abort_flag)) break;
         const uint32_t bar = smem_u32(&s.bar_full[st]);
         mbar_expect_tx(bar, kStageBytes);
-        load_operand<A_MN>(smem_u32(s.a[st]), &p.tm_a, bar, m0, kb * kGemmBK);
-        load_operand<B_MN>(smem_u32(s.b[st]), &p.tm_b, bar, n0, kb * kGemmBK);
+        load_operand<A_MN>(smem_u32(s.a[st]), &p.tm_a, bar, m0, (kb0 + kb) * kGemmBK);
+        load_operand<B_MN>(smem_u32(s.b[st]), &p.tm_b, bar, n0, (kb0 + kb) * kGemmBK);
         last[st] = use;
       }
       for (int st = 0; st < kGemmStages; ++st)  // never leave with a copy in flight
@@ -161,7 +175,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    const bool ok = mbar_wait(smem_u32(&s.bar_acc), 0, abort_flag);
+    // (a split with no K blocks -- only when k_splits exceeds them -- has
+    // nothing accumulated and writes zeros)
+    const bool ok = nk == 0 || mbar_wait(smem_u32(&s.bar_acc), 0, abort_flag);
     if (__all_sync(0xffffffffu, ok)) {
       tc_fence_after();
       const int row = m0 + warp * 32 + lane;
@@ -174,7 +190,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         uint32_t a[32];
         tmem_ld32(tacc + lane_addr + c * 32, a);
         tmem_ld_wait(a);
+        if (nk == 0)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) a[e] = 0u;
         if (row >= p.M || col >= p.N) continue;  // N is a multiple of 32
+        if (EPI == kEpiPartial) {
+          float* dst = p.partial + (static_cast<int64_t>(blockIdx.z) * p.M + row) * p.N + col;
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            *reinterpret_cast<uint4*>(dst + 4 * e) = make_uint4(a[4 * e], a[4 * e + 1], a[4 * e + 2], a[4 * e + 3]);
+          continue;
+        }
         uint32_t pk[16], pz[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
@@ -186,7 +212,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
               x1 += Elem<T>::hi(bw);
             }
             pz[e] = Elem<T>::pack2(x0, x1);
-            pk[e] = Elem<T>::pack2(x0 * sigmoidf_fast(x0), x1 * sigmoidf_fast(x1));
+            // silu(x) = x/2 (1 + tanh(x/2)): one hardware tanh an element
+            const float h0 = 0.5f * x0, h1 = 0.5f * x1;
+            pk[e] = Elem<T>::pack2(fmaf(h0, tanh_approx(h0), h0), fmaf(h1, tanh_approx(h1), h1));
           } else {
             pk[e] = Elem<T>::pack2(x0, x1);
           }
@@ -226,29 +254,45 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
     xc[i * row_vecs + v] = ok ? x[static_cast<int64_t>(r) * row_vecs + v] : make_uint4(0, 0, 0, 0);
 }
 
-// G = dY * silu'(Z) for a chunk of 128 rows and 256 columns (one column a
-// thread), and the chunk's column sums of G (the bias gradient's partials).
+// G = dY * silu'(Z) for a chunk of kGradRows rows and 2048 columns (8 consecutive
+// columns a thread, 16-byte loads and stores), and the chunk's column sums of
+// G (the bias gradient's partials). cols is a multiple of 64.
 template <typename T>
 __global__ void __launch_bounds__(256) silu_grad_kernel(const T* __restrict__ dy, const T* __restrict__ z,
                                                         int64_t rows, int cols, T* __restrict__ g,
                                                         float* __restrict__ part) {
-  const int col = blockIdx.y * 256 + threadIdx.x;
+  const int col = (blockIdx.y * 256 + threadIdx.x) * 8;
   if (col >= cols) return;
-  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * 128;
-  const int64_t r1 = r0 + 128 < rows ? r0 + 128 : rows;
-  float sum = 0.0f;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * kGradRows;
+  const int64_t r1 = r0 + kGradRows < rows ? r0 + kGradRows : rows;
+  float sum[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) sum[e] = 0.0f;
   for (int64_t r = r0; r < r1; ++r) {
     const int64_t idx = r * cols + col;
-    const uint16_t zb = reinterpret_cast<const uint16_t*>(z)[idx];
-    const uint16_t db = reinterpret_cast<const uint16_t*>(dy)[idx];
-    const float zz = Elem<T>::lo(zb), d = Elem<T>::lo(db);
-    const float sg = sigmoidf_fast(zz);
-    const float gv = d * sg * (1.0f + zz * (1.0f - sg));
-    const uint32_t w = Elem<T>::pack2(gv, 0.0f);
-    reinterpret_cast<uint16_t*>(g)[idx] = static_cast<uint16_t>(w & 0xffffu);
-    sum += Elem<T>::lo(w);  // the bias gradient sums the same rounded G the GEMMs read
+    const uint4 zv = *reinterpret_cast<const uint4*>(z + idx);
+    const uint4 dv = *reinterpret_cast<const uint4*>(dy + idx);
+    const uint32_t zw[4] = {zv.x, zv.y, zv.z, zv.w}, dw[4] = {dv.x, dv.y, dv.z, dv.w};
+    uint32_t gw[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      float gv[2];
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        const float zz = x ? Elem<T>::hi(zw[e]) : Elem<T>::lo(zw[e]);
+        const float d = x ? Elem<T>::hi(dw[e]) : Elem<T>::lo(dw[e]);
+        const float sg = sigmoidf_fast(zz);
+        gv[x] = d * sg * (1.0f + zz * (1.0f - sg));
+      }
+      gw[e] = Elem<T>::pack2(gv[0], gv[1]);
+      // the bias gradient sums the same rounded G the GEMMs read
+      sum[2 * e] += Elem<T>::lo(gw[e]);
+      sum[2 * e + 1] += Elem<T>::hi(gw[e]);
+    }
+    *reinterpret_cast<uint4*>(g + idx) = make_uint4(gw[0], gw[1], gw[2], gw[3]);
   }
-  part[static_cast<int64_t>(blockIdx.x) * cols + col] = sum;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) part[static_cast<int64_t>(blockIdx.x) * cols + col + e] = sum[e];
 }
 
 // db[col] = sum of the chunk partials in chunk order.
@@ -261,6 +305,25 @@ __global__ void __launch_bounds__(256) column_fold_kernel(const float* __restric
   for (int c = 0; c < chunks; ++c) s += part[static_cast<int64_t>(c) * cols + col];
   const uint32_t w = Elem<T>::pack2(s, 0.0f);
   reinterpret_cast<uint16_t*>(db)[col] = static_cast<uint16_t>(w & 0xffffu);
+}
+
+// out = sum over splits (in order) of the fp32 partials, 8 elements a thread.
+template <typename T>
+__global__ void __launch_bounds__(256) split_fold_kernel(const float* __restrict__ part, int splits, int64_t elems,
+                                                         T* __restrict__ out) {
+  const int64_t i = (static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x) * 8;
+  if (i >= elems) return;
+  float acc[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
+  for (int sp = 0; sp < splits; ++sp) {
+    const float4* src = reinterpret_cast<const float4*>(part + sp * elems + i);
+    const float4 a = src[0], b = src[1];
+    acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+    acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+  }
+  *reinterpret_cast<uint4*>(out + i) = make_uint4(Elem<T>::pack2(acc[0], acc[1]), Elem<T>::pack2(acc[2], acc[3]),
+                                                 Elem<T>::pack2(acc[4], acc[5]), Elem<T>::pack2(acc[6], acc[7]));
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -305,7 +368,9 @@ bool operand_map(CUtensorMap* m, const void* ptr, int64_t rows, int cols, int dt
 }
 
 template <typename T, bool A_MN, bool B_MN, int EPI>
-cudaError_t launch_gemm(const GemmParams& p, cudaStream_t stream) {
+cudaError_t launch_gemm(const GemmParams& p_in, cudaStream_t stream) {
+  GemmParams p = p_in;
+  if (p.k_splits < 1) p.k_splits = 1;
   const int smem = static_cast<int>(sizeof(GemmSmem)) + 1024;
   static std::atomic<uint64_t> configured{0};
   int dev = 0;
@@ -317,7 +382,7 @@ cudaError_t launch_gemm(const GemmParams& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     if (bit) configured.fetch_or(bit);
   }
-  const dim3 grid((p.M + kGemmBM - 1) / kGemmBM, (p.N + kGemmBN - 1) / kGemmBN);
+  const dim3 grid((p.M + kGemmBM - 1) / kGemmBM, (p.N + kGemmBN - 1) / kGemmBN, p.k_splits);
   if (grid.x == 0 || grid.y == 0) return cudaSuccess;
   gemm_kernel<T, A_MN, B_MN, EPI><<<grid, kGemmThreads, smem, stream>>>(p);
   return cudaGetLastError();
@@ -326,17 +391,19 @@ cudaError_t launch_gemm(const GemmParams& p, cudaStream_t stream) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Workspace of the projection: a 256-byte header (error word), then the
-// gathered rows X_c (n x d_in), then (backward) G (n x d_out) and the bias
-// partials (ceil(n / 128) x d_out fp32).
+// gathered rows X_c (n x d_in), then (backward) G (n x d_out), the bias
+// partials (ceil(n / kGradRows) x d_out fp32) and the split-K partials of dW
+// (kMaxKSplits x d_out x d_in fp32).
 struct ProjLayout {
-  size_t xc = 0, g = 0, part = 0, total = 0;
+  size_t xc = 0, g = 0, part = 0, dwp = 0, total = 0;
 };
 ProjLayout proj_layout(int64_t n, int d_in, int d_out, bool bwd) {
   ProjLayout l;
   l.xc = kHdrWords * 4;
   l.g = l.xc + align_up(static_cast<size_t>(n) * d_in * 2, 256);
   l.part = l.g + (bwd ? align_up(static_cast<size_t>(n) * d_out * 2, 256) : 0);
-  l.total = l.part + (bwd ? align_up(static_cast<size_t>((n + 127) / 128) * d_out * 4, 256) : 0);
+  l.dwp = l.part + (bwd ? align_up(static_cast<size_t>((n + kGradRows - 1) / kGradRows) * d_out * 4, 256) : 0);
+  l.total = l.dwp + (bwd ? align_up(static_cast<size_t>(kMaxKSplits) * d_out * d_in * 4, 256) : 0);
   return l;
 }
 
@@ -395,8 +462,8 @@ hstu_status_t project_bwd_t(const void* dy, const void* z, const void* x, int64_
   }
   T* g = reinterpret_cast<T*>(base + l.g);
   float* part = reinterpret_cast<float*>(base + l.part);
-  const int chunks = static_cast<int>((n + 127) / 128);
-  silu_grad_kernel<T><<<dim3(chunks, (d_out + 255) / 256), 256, 0, stream>>>(
+  const int chunks = static_cast<int>((n + kGradRows - 1) / kGradRows);
+  silu_grad_kernel<T><<<dim3(chunks, (d_out / 8 + 255) / 256), 256, 0, stream>>>(
       static_cast<const T*>(dy), static_cast<const T*>(z), n, d_out, g, part);
   if (cudaGetLastError() != cudaSuccess) return HSTU_ERR_CUDA;
   if (dbias) {
@@ -433,7 +500,21 @@ hstu_status_t project_bwd_t(const void* dy, const void* z, const void* x, int64_
   p2.N = d_in;
   p2.K = static_cast<int32_t>(n);
   p2.ldo = d_in;
-  return launch_gemm<T, true, true, kEpiStore>(p2, stream) == cudaSuccess ? HSTU_OK : HSTU_ERR_CUDA;
+  // K (the rows) is long and the output has few tiles: split K so that the
+  // grid covers the SMs twice, then fold the fp32 partials in split order.
+  const int tiles = ((d_out + kGemmBM - 1) / kGemmBM) * ((d_in + kGemmBN - 1) / kGemmBN);
+  const int nk = static_cast<int>((n + kGemmBK - 1) / kGemmBK);
+  int splits = (2 * 152 + tiles - 1) / tiles;
+  splits = splits < 1 ? 1 : (splits > kMaxKSplits ? kMaxKSplits : splits);
+  splits = splits > nk ? nk : splits;
+  if (splits <= 1) return launch_gemm<T, true, true, kEpiStore>(p2, stream) == cudaSuccess ? HSTU_OK : HSTU_ERR_CUDA;
+  p2.k_splits = splits;
+  p2.partial = reinterpret_cast<float*>(base + l.dwp);
+  if (launch_gemm<T, true, true, kEpiPartial>(p2, stream) != cudaSuccess) return HSTU_ERR_CUDA;
+  const int64_t elems = static_cast<int64_t>(d_out) * d_in;
+  split_fold_kernel<T><<<static_cast<unsigned>((elems / 8 + 255) / 256), 256, 0, stream>>>(p2.partial, splits, elems,
+                                                                                          static_cast<T*>(dw));
+  return cudaGetLastError() == cudaSuccess ? HSTU_OK : HSTU_ERR_CUDA;
 }
 
 }  // namespace
