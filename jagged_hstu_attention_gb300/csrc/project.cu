@@ -15,13 +15,14 @@
 // and B come from row-major 2-D tensors; an operand is K-major when K runs
 // along the tensor's rows (A = X_c, A = G, B = W in the forward) and
 // MN-major when K runs down its columns (B = W in dX_c; A = G and B = X_c in
-// dW). Tiles of 128 x 256 outputs, 64-deep K blocks through a 2-stage TMA
-// ring (48 KB a stage, 128-byte swizzle), one elected thread issuing
-// M=128, N=256, K=16 MMAs, four epilogue warps reading the accumulator out
-// of TMEM, one row per thread. Two CTAs share an SM (96 KB of shared memory
-// and 256 TMEM columns each), so one CTA's epilogue overlaps the other's
-// main loop. dW, whose K is the number of rows, splits K over up to eight
-// CTAs per output tile; their fp32 partial tiles are summed in split order
+// dW). Persistent: one CTA per SM takes output tiles of 128 x 256 in turn
+// (M fastest, so CTAs running together share the B tile in L2); 64-deep K
+// blocks flow through a 4-stage TMA ring (48 KB a stage, 128-byte swizzle)
+// that runs on across tiles; one elected thread issues M=128, N=256, K=16
+// MMAs into one of two 256-column TMEM accumulators, so that four epilogue
+// warps read one tile out (a row per thread) while the next accumulates.
+// dW, whose K is the number of rows, splits K over up to eight tiles per
+// output tile; their fp32 partial tiles are summed in split order
 // (deterministic) by a fold kernel.
 #include <cudaTypedefs.h>
 
@@ -35,7 +36,7 @@ namespace hstu {
 
 namespace {
 
-constexpr int kGemmBM = 128, kGemmBN = 256, kGemmBK = 64, kGemmStages = 2;
+constexpr int kGemmBM = 128, kGemmBN = 256, kGemmBK = 64, kGemmStages = 4;
 constexpr int kMaxKSplits = 8;
 constexpr int kGradRows = 1024;  // rows of one chunk of the bias gradient's partial sums
 constexpr int kGemmThreads = 192;  // warps 0-3 epilogue, 4 TMA producer, 5 MMA issuer
@@ -58,7 +59,7 @@ struct GemmParams {
 struct GemmSmem {
   alignas(1024) uint8_t a[kGemmStages][kGemmBM * kGemmBK * 2];  // 16 KB a stage
   alignas(1024) uint8_t b[kGemmStages][kGemmBN * kGemmBK * 2];  // 32 KB a stage
-  alignas(8) uint64_t bar_full[kGemmStages], bar_empty[kGemmStages], bar_acc, bar_drain;
+  alignas(8) uint64_t bar_full[kGemmStages], bar_empty[kGemmStages], bar_acc_full[2], bar_acc_empty[2], bar_drain;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -98,17 +99,25 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t base, int kk) {
 }
 
 template <typename T, bool A_MN, bool B_MN, int EPI>
-__global__ void __launch_bounds__(kGemmThreads, 2) gemm_kernel(const __grid_constant__ GemmParams p) {
+__global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   GemmSmem& s = *reinterpret_cast<GemmSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m0 = blockIdx.x * kGemmBM, n0 = blockIdx.y * kGemmBN;
-  // This CTA's K blocks: split blockIdx.z of k_splits (all of K without a split).
+  const int tm = (p.M + kGemmBM - 1) / kGemmBM, tn = (p.N + kGemmBN - 1) / kGemmBN;
+  const int n_tiles = tm * tn * p.k_splits;
   const int nk_all = (p.K + kGemmBK - 1) / kGemmBK;
   const int per = (nk_all + p.k_splits - 1) / p.k_splits;
-  const int kb0 = static_cast<int>(blockIdx.z) * per;
-  const int kb1 = kb0 + per < nk_all ? kb0 + per : nk_all;
-  const int nk = kb1 > kb0 ? kb1 - kb0 : 0;
+  // Tile t: K split t / (tm tn), then n tile, then m tile (fastest). Its K
+  // blocks are [kb0, kb1) (empty only when k_splits exceeds the K blocks).
+  auto tile_of = [&](int t, int& m0, int& n0, int& split, int& kb0, int& kb1) {
+    split = t / (tm * tn);
+    const int rem = t - split * tm * tn;
+    n0 = (rem / tm) * kGemmBN;
+    m0 = (rem % tm) * kGemmBM;
+    kb0 = split * per;
+    kb1 = kb0 + per < nk_all ? kb0 + per : nk_all;
+    if (kb1 < kb0) kb1 = kb0;
+  };
   constexpr uint32_t kStageBytes = (kGemmBM + kGemmBN) * kGemmBK * 2;
   if (threadIdx.x == 0) {
     s.abort_flag = 0;
@@ -116,18 +125,21 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_kernel(const __grid_cons
       mbar_init(smem_u32(&s.bar_full[i]), 1);
       mbar_init(smem_u32(&s.bar_empty[i]), 1);
     }
-    mbar_init(smem_u32(&s.bar_acc), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&s.bar_acc_full[i]), 1);
+      mbar_init(smem_u32(&s.bar_acc_empty[i]), 128);  // the four epilogue warps
+    }
     mbar_init(smem_u32(&s.bar_drain), 1);
     fence_mbar_init();
   }
   if (warp == 5) {
-    tmem_alloc(smem_u32(&s.tmem_base), kGemmBN);
+    tmem_alloc(smem_u32(&s.tmem_base), 2 * kGemmBN);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tacc = s.tmem_base;
+  const uint32_t tbase = s.tmem_base;
   volatile int* abort_flag = &s.abort_flag;
 
   if (warp == 4) {
@@ -137,14 +149,23 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_kernel(const __grid_cons
       tma_prefetch_map(&p.tm_b);
       int last[kGemmStages];
       for (int st = 0; st < kGemmStages; ++st) last[st] = -1;
-      for (int kb = 0; kb < nk; ++kb) {
-        const int st = kb % kGemmStages, use = kb / kGemmStages;
-        if (use > 0 && !mbar_wait(smem_u32(&s.bar_empty[st]), (use - 1) & 1, abort_flag)) break;
-        const uint32_t bar = smem_u32(&s.bar_full[st]);
-        mbar_expect_tx(bar, kStageBytes);
-        load_operand<A_MN>(smem_u32(s.a[st]), &p.tm_a, bar, m0, (kb0 + kb) * kGemmBK);
-        load_operand<B_MN>(smem_u32(s.b[st]), &p.tm_b, bar, n0, (kb0 + kb) * kGemmBK);
-        last[st] = use;
+      int g = 0;  // K blocks over all tiles of this CTA
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
+        int m0, n0, split, kb0, kb1;
+        tile_of(t, m0, n0, split, kb0, kb1);
+        for (int kb = kb0; kb < kb1; ++kb, ++g) {
+          const int st = g % kGemmStages, use = g / kGemmStages;
+          if (use > 0 && !mbar_wait(smem_u32(&s.bar_empty[st]), (use - 1) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint32_t bar = smem_u32(&s.bar_full[st]);
+          mbar_expect_tx(bar, kStageBytes);
+          load_operand<A_MN>(smem_u32(s.a[st]), &p.tm_a, bar, m0, kb * kGemmBK);
+          load_operand<B_MN>(smem_u32(s.b[st]), &p.tm_b, bar, n0, kb * kGemmBK);
+          last[st] = use;
+        }
       }
       for (int st = 0; st < kGemmStages; ++st)  // never leave with a copy in flight
         if (last[st] >= 0) mbar_wait_drain(smem_u32(&s.bar_full[st]), last[st] & 1);
@@ -154,48 +175,62 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_kernel(const __grid_cons
     // ------------------------------------------------------------ MMA issuer
     if (elect_one_sync()) {
       constexpr uint32_t idesc = idesc_f16kind(kGemmBM, kGemmBN, A_MN, B_MN, Elem<T>::kUmma);
+      int g = 0;  // K blocks over all tiles of this CTA
+      int i = 0;  // tiles of this CTA
       bool ok = true;
-      for (int kb = 0; kb < nk; ++kb) {
-        const int st = kb % kGemmStages;
-        if (!mbar_wait(smem_u32(&s.bar_full[st]), (kb / kGemmStages) & 1, abort_flag)) {
-          ok = false;
-          break;
-        }
+      for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x, ++i) {
+        int m0, n0, split, kb0, kb1;
+        tile_of(t, m0, n0, split, kb0, kb1);
+        const int buf = i & 1;
+        // accumulator buf is free once the epilogue has read out tile i - 2
+        if (i >= 2 && !mbar_wait(smem_u32(&s.bar_acc_empty[buf]), ((i >> 1) - 1) & 1, abort_flag)) break;
         tc_fence_after();
+        const uint32_t tacc = tbase + buf * kGemmBN;
+        for (int kb = kb0; kb < kb1; ++kb, ++g) {
+          const int st = g % kGemmStages;
+          if (!mbar_wait(smem_u32(&s.bar_full[st]), (g / kGemmStages) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < kGemmBK / 16; ++kk)
-          umma_ss(tacc, operand_desc<A_MN>(smem_u32(s.a[st]), kk), operand_desc<B_MN>(smem_u32(s.b[st]), kk),
-                  idesc, (kb > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(smem_u32(&s.bar_empty[st]));
+          for (int kk = 0; kk < kGemmBK / 16; ++kk)
+            umma_ss(tacc, operand_desc<A_MN>(smem_u32(s.a[st]), kk), operand_desc<B_MN>(smem_u32(s.b[st]), kk),
+                    idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+          umma_commit(smem_u32(&s.bar_empty[st]));
+        }
+        if (ok) umma_commit(smem_u32(&s.bar_acc_full[buf]));
       }
-      if (ok) umma_commit(smem_u32(&s.bar_acc));
       umma_commit(smem_u32(&s.bar_drain));  // every MMA issued above has completed (also on abort)
       mbar_wait_drain(smem_u32(&s.bar_drain), 0);
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    // (a split with no K blocks -- only when k_splits exceeds them -- has
-    // nothing accumulated and writes zeros)
-    const bool ok = nk == 0 || mbar_wait(smem_u32(&s.bar_acc), 0, abort_flag);
-    if (__all_sync(0xffffffffu, ok)) {
+    const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
+    const T* bias = static_cast<const T*>(p.bias);
+    int i = 0;
+    for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++i) {
+      int m0, n0, split, kb0, kb1;
+      tile_of(t, m0, n0, split, kb0, kb1);
+      const int buf = i & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&s.bar_acc_full[buf]), (i >> 1) & 1, abort_flag))) break;
       tc_fence_after();
+      const bool empty = kb1 == kb0;  // nothing accumulated: zeros
       const int row = m0 + warp * 32 + lane;
-      const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
       T* out = static_cast<T*>(p.out) + static_cast<int64_t>(row) * p.ldo;
       T* out2 = p.out2 ? static_cast<T*>(p.out2) + static_cast<int64_t>(row) * p.ldo : nullptr;
-      const T* bias = static_cast<const T*>(p.bias);
       for (int c = 0; c < kGemmBN / 32; ++c) {
         const int col = n0 + c * 32;
         uint32_t a[32];
-        tmem_ld32(tacc + lane_addr + c * 32, a);
+        tmem_ld32(tbase + buf * kGemmBN + lane_addr + c * 32, a);
         tmem_ld_wait(a);
-        if (nk == 0)
+        if (empty)
 #pragma unroll
           for (int e = 0; e < 32; ++e) a[e] = 0u;
         if (row >= p.M || col >= p.N) continue;  // N is a multiple of 32
         if (EPI == kEpiPartial) {
-          float* dst = p.partial + (static_cast<int64_t>(blockIdx.z) * p.M + row) * p.N + col;
+          float* dst = p.partial + (static_cast<int64_t>(split) * p.M + row) * p.N + col;
 #pragma unroll
           for (int e = 0; e < 8; ++e)
             *reinterpret_cast<uint4*>(dst + 4 * e) = make_uint4(a[4 * e], a[4 * e + 1], a[4 * e + 2], a[4 * e + 3]);
@@ -229,13 +264,15 @@ __global__ void __launch_bounds__(kGemmThreads, 2) gemm_kernel(const __grid_cons
                 make_uint4(pz[4 * e], pz[4 * e + 1], pz[4 * e + 2], pz[4 * e + 3]);
         }
       }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&s.bar_acc_empty[buf]));
     }
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 5) {
     tc_fence_after();
-    tmem_dealloc(tacc, kGemmBN);
+    tmem_dealloc(tbase, 2 * kGemmBN);
   }
   if (threadIdx.x == 0 && s.abort_flag && p.err) atomicOr(p.err, kErrTimeout);
 }
@@ -382,8 +419,13 @@ cudaError_t launch_gemm(const GemmParams& p_in, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     if (bit) configured.fetch_or(bit);
   }
-  const dim3 grid((p.M + kGemmBM - 1) / kGemmBM, (p.N + kGemmBN - 1) / kGemmBN, p.k_splits);
-  if (grid.x == 0 || grid.y == 0) return cudaSuccess;
+  const long long tiles = static_cast<long long>((p.M + kGemmBM - 1) / kGemmBM) * ((p.N + kGemmBN - 1) / kGemmBN) *
+                          p.k_splits;
+  if (tiles <= 0) return cudaSuccess;
+  int sms = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const dim3 grid(static_cast<unsigned>(tiles < sms ? tiles : sms));  // persistent: one CTA per SM
   gemm_kernel<T, A_MN, B_MN, EPI><<<grid, kGemmThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
