@@ -72,7 +72,8 @@ typedef enum {
   HSTU_ERR_WORKSPACE = 3,    /* workspace null, too small or misaligned */
   HSTU_ERR_CUDA = 4,         /* a CUDA runtime call failed (launch, sync) */
   HSTU_ERR_DEVICE_INPUT = 5, /* device-side input check failed (offsets) */
-  HSTU_ERR_TIMEOUT = 6       /* a bounded in-kernel wait gave up */
+  HSTU_ERR_TIMEOUT = 6,      /* a bounded in-kernel wait gave up */
+  HSTU_ERR_DEVICE_CHECK = 7  /* checked build only: a work-list index check failed */
 } hstu_status_t;
 
 /* Input and output element types (all tensors of a call share one). */
@@ -306,8 +307,17 @@ HSTU_API hstu_status_t hstu_attn_build_func_candidates(const int32_t* seq_offset
                                                        int32_t* func_c, void* stream);
 
 /* Synchronises the stream, then returns the status recorded in the
- * workspace error word (HSTU_OK, HSTU_ERR_DEVICE_INPUT, HSTU_ERR_TIMEOUT) or
- * HSTU_ERR_CUDA if the synchronisation failed. */
+ * workspace error word (HSTU_OK, HSTU_ERR_DEVICE_INPUT, HSTU_ERR_TIMEOUT,
+ * and in the checked build HSTU_ERR_DEVICE_CHECK) or HSTU_ERR_CUDA if the
+ * synchronisation failed.
+ *
+ * Checked build: libhstu_attn_checked.so exports the same entry points,
+ * compiled with HSTU_CHECKED. Its attention kernels validate each entry of
+ * the plan's work lists (sequence inside the batch, tile inside the
+ * sequence) before any load or store goes through it; a bad entry ends that
+ * CTA's work and records HSTU_ERR_DEVICE_CHECK, and the workspace must be
+ * planned again. It is a debugging aid: results equal the release build's
+ * bit for bit. */
 HSTU_API hstu_status_t hstu_attn_get_device_status(const void* ws, void* stream);
 
 /* Static description of a status code. */

@@ -16,11 +16,14 @@ import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libhstu_attn.so")
+# The same entry points compiled with device-side index checks (see
+# hstu_attn.h); select_library() switches the wrappers below to it.
+CHECKED_LIB_PATH = os.path.join(_HERE, "libhstu_attn_checked.so")
 
 HSTU_OK = 0
 STATUS_NAMES = {
     0: "HSTU_OK", 1: "HSTU_ERR_INVALID_ARG", 2: "HSTU_ERR_UNSUPPORTED", 3: "HSTU_ERR_WORKSPACE",
-    4: "HSTU_ERR_CUDA", 5: "HSTU_ERR_DEVICE_INPUT", 6: "HSTU_ERR_TIMEOUT",
+    4: "HSTU_ERR_CUDA", 5: "HSTU_ERR_DEVICE_INPUT", 6: "HSTU_ERR_TIMEOUT", 7: "HSTU_ERR_DEVICE_CHECK",
 }
 WS_FULL = 0
 WS_TARGETS = 1
@@ -69,14 +72,24 @@ class Shape(ctypes.Structure):
     ]
 
 
-_lib = None
+_libs = {}
+_active = LIB_PATH
 
 
-def load(path: str = LIB_PATH) -> ctypes.CDLL:
-    """Loads the library (once). Raises if it has not been built."""
-    global _lib
-    if _lib is not None:
-        return _lib
+def select_library(path: str) -> str:
+    """Makes the wrappers of this module call the library at ``path`` (the
+    release or the checked build); returns the previously selected path."""
+    global _active
+    prev, _active = _active, path
+    return prev
+
+
+def load(path: str = None) -> ctypes.CDLL:
+    """Loads the selected library (once per path). Raises if it has not been
+    built."""
+    path = _active if path is None else path
+    if path in _libs:
+        return _libs[path]
     if not os.path.exists(path):
         raise RuntimeError(
             f"CUDA library {path} is missing: build it first "
@@ -115,7 +128,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         fn = getattr(lib, name)
         fn.restype = res
         fn.argtypes = args
-    _lib = lib
+    _libs[path] = lib
     return lib
 
 

@@ -1,8 +1,12 @@
-"""Builds the CUDA library ``libhstu_attn.so`` in-tree for sm_103a.
+"""Builds the CUDA libraries in-tree for sm_103a.
 
-Each translation unit is compiled by nvcc in parallel, then linked into one
-shared library next to this file (the CUDA runtime is linked statically).
-A rebuild is skipped when the library is newer than every source.
+``libhstu_attn.so`` is the release build. ``libhstu_attn_checked.so`` is the
+same sources compiled with ``HSTU_CHECKED``: its kernels validate every
+work-list entry before using it (a debugging aid, results bit-identical).
+Every translation unit of both is compiled by nvcc in one parallel pool, then
+each set is linked into one shared library next to this file (the CUDA
+runtime is linked statically). A library newer than every source is not
+rebuilt.
 """
 from __future__ import annotations
 
@@ -18,7 +22,12 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_NAME = "libhstu_attn.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
-
+CHECKED_LIB_PATH = os.path.join(PKG, "libhstu_attn_checked.so")
+# variant -> (library, object directory, extra nvcc flags)
+VARIANTS = {
+    "release": (LIB_PATH, BUILD_DIR, []),
+    "checked": (CHECKED_LIB_PATH, os.path.join(BUILD_DIR, "checked"), ["-DHSTU_CHECKED"]),
+}
 SOURCES = ["plan.cu", "attn_fwd_bf16.cu", "attn_fwd_f16.cu", "attn_bwd_bf16.cu", "attn_bwd_f16.cu", "targets_only.cu", "api.cu", "noalloc.cu", "selftest.cu", "func_build.cu", "project.cu",
            "shard.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -43,37 +52,45 @@ def _deps():
     return files
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB_PATH):
+def up_to_date(lib: str = LIB_PATH) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(f) <= t for f in _deps())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and up_to_date():
+def build(force: bool = False, verbose: bool = False, variants=("release", "checked")) -> str:
+    """Builds the requested variants; returns the release library's path."""
+    todo = [v for v in variants if force or not up_to_date(VARIANTS[v][0])]
+    if not todo:
         return LIB_PATH
-    os.makedirs(BUILD_DIR, exist_ok=True)
     nvcc = _nvcc()
 
-    def compile_one(src):
-        obj = os.path.join(BUILD_DIR, os.path.splitext(src)[0] + ".o")
-        cmd = [nvcc, *ARCH, *FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+    def compile_one(job):
+        variant, src = job
+        _, obj_dir, extra = VARIANTS[variant]
+        obj = os.path.join(obj_dir, os.path.splitext(src)[0] + ".o")
+        cmd = [nvcc, *ARCH, *FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             print(" ".join(cmd), flush=True)
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
-            raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
+            raise RuntimeError(f"nvcc failed on {src} ({variant}):\n{r.stdout}\n{r.stderr}")
         return obj
 
-    with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB_PATH + ".tmp"
-    cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
-    r = subprocess.run(cmd, capture_output=True, text=True)
-    if r.returncode != 0:
-        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
+    for v in todo:
+        os.makedirs(VARIANTS[v][1], exist_ok=True)
+    jobs = [(v, src) for v in todo for src in SOURCES]
+    with ThreadPoolExecutor(max_workers=min(len(jobs), max(os.cpu_count() or 1, len(SOURCES)))) as ex:
+        objs = list(ex.map(compile_one, jobs))
+    for v in todo:
+        lib = VARIANTS[v][0]
+        tmp = lib + ".tmp"
+        cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *[o for (vv, _), o in zip(jobs, objs) if vv == v]]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"link failed ({v}):\n{r.stdout}\n{r.stderr}")
+        os.replace(tmp, lib)
     return LIB_PATH
 
 

@@ -207,6 +207,7 @@ hstu_status_t hstu_attn_fwd(const void* q, const void* k, const void* v, void* o
   p.list = reinterpret_cast<const int32_t*>(base + l.fwd_list);
   p.header = reinterpret_cast<int32_t*>(base + l.header);
   p.total = shape->total;
+  p.batch = shape->batch;
   p.heads = shape->num_heads;
   p.dim = Dq;
   p.dim_v = Dv;
@@ -255,6 +256,7 @@ hstu_status_t hstu_attn_bwd(const void* dout, const void* q, const void* k, cons
   p.list = reinterpret_cast<const int32_t*>(base + l.bwd_list);
   p.header = reinterpret_cast<int32_t*>(base + l.header);
   p.total = shape->total;
+  p.batch = shape->batch;
   p.heads = shape->num_heads;
   p.dim = Dq;
   p.dim_v = Dv;
@@ -398,6 +400,7 @@ hstu_status_t hstu_attn_get_device_status(const void* ws, void* stream) {
   if (cudaMemcpy(&err, ws, sizeof(err), cudaMemcpyDeviceToHost) != cudaSuccess) return HSTU_ERR_CUDA;
   if (err & hstu::kErrInput) return HSTU_ERR_DEVICE_INPUT;
   if (err & hstu::kErrTimeout) return HSTU_ERR_TIMEOUT;
+  if (err & hstu::kErrCheck) return HSTU_ERR_DEVICE_CHECK;
   return HSTU_OK;
 }
 
@@ -410,6 +413,7 @@ const char* hstu_status_string(hstu_status_t status) {
     case HSTU_ERR_CUDA: return "CUDA runtime error";
     case HSTU_ERR_DEVICE_INPUT: return "device-side input check failed (seq_offsets)";
     case HSTU_ERR_TIMEOUT: return "bounded in-kernel wait timed out";
+    case HSTU_ERR_DEVICE_CHECK: return "index check of the checked build failed";
   }
   return "unknown status";
 }

@@ -287,7 +287,9 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
         if (lane == 0) w = fetch_work(p.header, kHdrBwdNext);
         w = __shfl_sync(0xffffffffu, w, 0);
       }
-      if (w >= n_work) {  // no more work: an item with nt = -1 tells the other roles
+      // No more work (or, in the checked build, a bad list entry): an item
+      // with nt = -1 tells the other roles.
+      if (w >= n_work || !list_entry_ok(p, p.list[w / p.heads], true)) {
         if (lane == 0) s.item[slot].nt = -1;
         __threadfence_block();
         __syncwarp();

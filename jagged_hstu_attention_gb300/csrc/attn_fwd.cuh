@@ -210,7 +210,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1) hstu_fwd_kernel(const __grid_c
         if (lane == 0) w = fetch_work(p.header, kHdrFwdNext);
         w = __shfl_sync(0xffffffffu, w, 0);
       }
-      if (w >= n_work) {  // no more work: an item with nt = -1 tells the other roles
+      // No more work (or, in the checked build, a bad list entry): an item
+      // with nt = -1 tells the other roles.
+      if (w >= n_work || !list_entry_ok(p, p.list[w / p.heads], false)) {
         if (lane == 0) s.item[slot].nt = -1;
         __threadfence_block();
         __syncwarp();

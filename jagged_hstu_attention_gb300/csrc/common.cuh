@@ -19,7 +19,7 @@ constexpr int kMaxTiles = kMaxSeqlen / kBlock;
 constexpr int kMaxIntervals = 5;   // nfunc <= 9
 
 // Workspace header (int32 words).
-constexpr int kHdrErr = 0;     // error bits (kErrInput | kErrTimeout)
+constexpr int kHdrErr = 0;     // error bits (kErrInput | kErrTimeout | kErrCheck)
 constexpr int kHdrNFwd = 1;    // entries of the forward work list
 constexpr int kHdrNBwd = 2;    // entries of the backward work list
 // Dynamic work distribution of the persistent attention kernels: the next
@@ -37,6 +37,16 @@ constexpr int kHdrUniform = 8;
 constexpr int kHdrWords = 64;  // 256 bytes
 constexpr int kErrInput = 1;
 constexpr int kErrTimeout = 2;
+constexpr int kErrCheck = 4;  // an index check of the checked build failed
+
+// The checked build (compiled with HSTU_CHECKED) validates every work-list
+// entry before anything is read or written through it; the release build
+// compiles the checks away.
+#ifdef HSTU_CHECKED
+constexpr bool kChecked = true;
+#else
+constexpr bool kChecked = false;
+#endif
 
 // Tile classes written by the plan (bits 0-1), with the dead 64-wide halves
 // of a partial pair: kv columns 0..63 / 64..127 seen by no row, q rows
@@ -134,13 +144,30 @@ struct AttnParams {
   const int32_t* list;
   int32_t* header;
   int64_t total;
-  int32_t heads, dim, dim_v, nt, max_seqlen;  // dim = D_qk, dim_v = D_v
+  int32_t batch, heads, dim, dim_v, nt, max_seqlen;  // dim = D_qk, dim_v = D_v
   float alpha, inv_n;
   // Limit of the MMA thread's wait for the epilogue to have read out the
   // previous item's accumulators (kWaitLimitNs unless a test shortens it to
   // make that wait run out with copies and MMAs in flight).
   uint64_t handoff_limit_ns;
 };
+
+// Checked builds only: a work-list entry must name a sequence of the batch
+// (and only the role bit besides it), and a tile inside that sequence. A bad
+// entry sets kErrCheck; the caller then ends its work as if the list had run
+// out. Every lane of the calling warp gets the same answer.
+__device__ __forceinline__ bool list_entry_ok(const AttnParams& p, int code, bool bwd) {
+  if (!kChecked) return true;
+  const int payload = bwd ? (code & ~kRoleDkdv) : code;
+  bool ok = payload >= 0 && (payload >> 8) < p.batch;
+  if (ok) {
+    const int b = payload >> 8;
+    const int L = p.seq_offsets[b + 1] - p.seq_offsets[b];
+    ok = (payload & 255) * kBlock < L;
+  }
+  if (!ok) atomicOr(p.header + kHdrErr, kErrCheck);
+  return ok;
+}
 
 struct TgtParams {
   const void* q_c;   // (C, H, dim), C = num_cand candidate rows

@@ -15,8 +15,10 @@
 // and B come from row-major 2-D tensors; an operand is K-major when K runs
 // along the tensor's rows (A = X_c, A = G, B = W in the forward) and
 // MN-major when K runs down its columns (B = W in dX_c; A = G and B = X_c in
-// dW). Persistent: one CTA per SM takes output tiles of 128 x 256 in turn
-// (M fastest, so CTAs running together share the B tile in L2); 64-deep K
+// dW). Persistent: one CTA per SM takes output tiles of 128 x 256 in turn,
+// N fastest: the CTAs running together cover every N tile of a few row
+// blocks, so the long A operand (X_c, G) comes from HBM once and W, which is
+// small, stays in L2 (with M fastest, A was read once per N tile); 64-deep K
 // blocks flow through a 4-stage TMA ring (48 KB a stage, 128-byte swizzle)
 // that runs on across tiles; one elected thread issues M=128, N=256, K=16
 // MMAs into one of two 256-column TMEM accumulators, so that four epilogue
@@ -38,7 +40,14 @@ namespace {
 
 constexpr int kGemmBM = 128, kGemmBN = 256, kGemmBK = 64, kGemmStages = 4;
 constexpr int kMaxKSplits = 8;
-constexpr int kGradRows = 1024;  // rows of one chunk of the bias gradient's partial sums
+// The SiLU gradient splits the rows into at most kGradChunks chunks of at
+// least kGradMinRows rows (one block each); a chunk's column sums are the
+// bias gradient's partials, folded in chunk order.
+constexpr int kGradChunks = 1216, kGradMinRows = 64, kGradThreads = 256;
+inline int grad_chunks(int64_t n) {
+  const int64_t c = (n + kGradMinRows - 1) / kGradMinRows;
+  return static_cast<int>(c < kGradChunks ? c : kGradChunks);
+}
 constexpr int kGemmThreads = 192;  // warps 0-3 epilogue, 4 TMA producer, 5 MMA issuer
 
 // Epilogues.
@@ -54,6 +63,7 @@ struct GemmParams {
   int32_t* err;  // error word (nullable): kErrTimeout on a timed-out wait
   float* partial;  // kEpiPartial: (k_splits, M, N) fp32
   int32_t M, N, K, ldo, k_splits;
+  int32_t wide;  // out, out2 and ldo allow 32-byte stores
 };
 
 struct GemmSmem {
@@ -91,6 +101,20 @@ __device__ __forceinline__ void load_operand(uint32_t dst, const CUtensorMap* ma
   else tma_load_2d(dst, map, bar, k0, mn0);
 }
 
+// Stores 32 bytes (eight words) at a 32-byte aligned address, or as two
+// 16-byte halves: a whole sector per store reaches L2 in one request.
+__device__ __forceinline__ void store_words8(void* dst, const uint32_t* w, bool wide) {
+  if (wide) {
+    asm volatile("st.global.L1::no_allocate.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(w[0]),
+                 "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+  } else {
+    uint4* d = static_cast<uint4*>(dst);
+    d[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    d[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  }
+}
+
 // Shared-memory descriptor of K-step kk (16 deep) of a stage tile.
 template <bool MN>
 __device__ __forceinline__ uint64_t operand_desc(uint32_t base, int kk) {
@@ -107,13 +131,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   const int n_tiles = tm * tn * p.k_splits;
   const int nk_all = (p.K + kGemmBK - 1) / kGemmBK;
   const int per = (nk_all + p.k_splits - 1) / p.k_splits;
-  // Tile t: K split t / (tm tn), then n tile, then m tile (fastest). Its K
+  // Tile t: K split t / (tm tn), then m tile, then n tile (fastest). Its K
   // blocks are [kb0, kb1) (empty only when k_splits exceeds the K blocks).
   auto tile_of = [&](int t, int& m0, int& n0, int& split, int& kb0, int& kb1) {
     split = t / (tm * tn);
     const int rem = t - split * tm * tn;
-    n0 = (rem / tm) * kGemmBN;
-    m0 = (rem % tm) * kGemmBM;
+    m0 = (rem / tn) * kGemmBM;
+    n0 = (rem % tn) * kGemmBN;
     kb0 = split * per;
     kb1 = kb0 + per < nk_all ? kb0 + per : nk_all;
     if (kb1 < kb0) kb1 = kb0;
@@ -229,11 +253,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
 #pragma unroll
           for (int e = 0; e < 32; ++e) a[e] = 0u;
         if (row >= p.M || col >= p.N) continue;  // N is a multiple of 32
-        if (EPI == kEpiPartial) {
+        if (EPI == kEpiPartial) {  // fp32 rows of the workspace: always 32-byte aligned
           float* dst = p.partial + (static_cast<int64_t>(split) * p.M + row) * p.N + col;
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            *reinterpret_cast<uint4*>(dst + 4 * e) = make_uint4(a[4 * e], a[4 * e + 1], a[4 * e + 2], a[4 * e + 3]);
+          for (int e = 0; e < 4; ++e) store_words8(dst + 8 * e, a + 8 * e, true);
           continue;
         }
         uint32_t pk[16], pz[16];
@@ -254,14 +277,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
             pk[e] = Elem<T>::pack2(x0, x1);
           }
         }
+        const bool wide = p.wide != 0;
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          *reinterpret_cast<uint4*>(out + col + 8 * e) = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+        for (int e = 0; e < 2; ++e) store_words8(out + col + 16 * e, pk + 8 * e, wide);
         if (EPI == kEpiBiasSilu && out2) {
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            *reinterpret_cast<uint4*>(out2 + col + 8 * e) =
-                make_uint4(pz[4 * e], pz[4 * e + 1], pz[4 * e + 2], pz[4 * e + 3]);
+          for (int e = 0; e < 2; ++e) store_words8(out2 + col + 16 * e, pz + 8 * e, wide);
         }
       }
       tc_fence_before();
@@ -291,24 +312,32 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
     xc[i * row_vecs + v] = ok ? x[static_cast<int64_t>(r) * row_vecs + v] : make_uint4(0, 0, 0, 0);
 }
 
-// G = dY * silu'(Z) for a chunk of kGradRows rows and 2048 columns (8 consecutive
-// columns a thread, 16-byte loads and stores), and the chunk's column sums of
-// G (the bias gradient's partials). cols is a multiple of 64.
+// G = dY * silu'(Z), eight consecutive columns a thread (16-byte loads and
+// stores), and the bias gradient's partials: block b takes the row chunk
+// [b R, (b + 1) R), R = ceil(rows / gridDim.x), and writes its column sums to
+// part[b]. The threads of a block cover rpi = 256 / (cols / 8) rows of all
+// columns per iteration when a row has at most 256 column groups, else one
+// row of the 256 groups that gridDim.y picks; two rows are in flight per
+// thread. Row lanes are summed in lane order through shared memory, so the
+// partials are deterministic. cols is a multiple of 64.
 template <typename T>
-__global__ void __launch_bounds__(256) silu_grad_kernel(const T* __restrict__ dy, const T* __restrict__ z,
-                                                        int64_t rows, int cols, T* __restrict__ g,
-                                                        float* __restrict__ part) {
-  const int col = (blockIdx.y * 256 + threadIdx.x) * 8;
-  if (col >= cols) return;
-  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * kGradRows;
-  const int64_t r1 = r0 + kGradRows < rows ? r0 + kGradRows : rows;
+__global__ void __launch_bounds__(kGradThreads) silu_grad_kernel(const T* __restrict__ dy, const T* __restrict__ z,
+                                                                 int64_t rows, int cols, T* __restrict__ g,
+                                                                 float* __restrict__ part) {
+  __shared__ float red[kGradThreads][8];
+  const int groups = cols / 8;
+  const int rpi = groups >= kGradThreads ? 1 : kGradThreads / groups;
+  const int gy = groups >= kGradThreads ? kGradThreads : groups;  // column groups a block covers
+  const int lane_row = threadIdx.x / gy, cg = blockIdx.y * gy + threadIdx.x % gy;
+  const bool active = lane_row < rpi && cg < groups;
+  const int col = cg * 8;
+  const int64_t per = (rows + gridDim.x - 1) / gridDim.x;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * per;
+  const int64_t r1 = r0 + per < rows ? r0 + per : rows;
   float sum[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) sum[e] = 0.0f;
-  for (int64_t r = r0; r < r1; ++r) {
-    const int64_t idx = r * cols + col;
-    const uint4 zv = *reinterpret_cast<const uint4*>(z + idx);
-    const uint4 dv = *reinterpret_cast<const uint4*>(dy + idx);
+  auto grad_row = [&](const uint4& zv, const uint4& dv, int64_t idx) {
     const uint32_t zw[4] = {zv.x, zv.y, zv.z, zv.w}, dw[4] = {dv.x, dv.y, dv.z, dv.w};
     uint32_t gw[4];
 #pragma unroll
@@ -327,21 +356,58 @@ __global__ void __launch_bounds__(256) silu_grad_kernel(const T* __restrict__ dy
       sum[2 * e + 1] += Elem<T>::hi(gw[e]);
     }
     *reinterpret_cast<uint4*>(g + idx) = make_uint4(gw[0], gw[1], gw[2], gw[3]);
+  };
+  if (active) {
+    int64_t r = r0 + lane_row;
+    for (; r + rpi < r1; r += 2 * rpi) {  // two rows in flight
+      const int64_t i0 = r * cols + col, i1 = (r + rpi) * cols + col;
+      const uint4 z0 = *reinterpret_cast<const uint4*>(z + i0), d0 = *reinterpret_cast<const uint4*>(dy + i0);
+      const uint4 z1 = *reinterpret_cast<const uint4*>(z + i1), d1 = *reinterpret_cast<const uint4*>(dy + i1);
+      grad_row(z0, d0, i0);
+      grad_row(z1, d1, i1);
+    }
+    if (r < r1) {
+      const int64_t i0 = r * cols + col;
+      grad_row(*reinterpret_cast<const uint4*>(z + i0), *reinterpret_cast<const uint4*>(dy + i0), i0);
+    }
   }
 #pragma unroll
-  for (int e = 0; e < 8; ++e) part[static_cast<int64_t>(blockIdx.x) * cols + col + e] = sum[e];
+  for (int e = 0; e < 8; ++e) red[threadIdx.x][e] = sum[e];
+  __syncthreads();
+  if (active && lane_row == 0) {
+    float tot[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) tot[e] = 0.0f;
+    for (int l = 0; l < rpi; ++l)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) tot[e] += red[l * gy + threadIdx.x][e];
+    float* dst = part + static_cast<int64_t>(blockIdx.x) * cols + col;
+    reinterpret_cast<float4*>(dst)[0] = make_float4(tot[0], tot[1], tot[2], tot[3]);
+    reinterpret_cast<float4*>(dst)[1] = make_float4(tot[4], tot[5], tot[6], tot[7]);
+  }
 }
 
-// db[col] = sum of the chunk partials in chunk order.
+// db[col] = sum of the chunk partials in chunk order: warp w of a block
+// sums chunks w, w + 8, ... of 32 columns (a lane a column), then lane l of
+// warp 0 adds the eight warps' sums in warp order.
 template <typename T>
 __global__ void __launch_bounds__(256) column_fold_kernel(const float* __restrict__ part, int chunks, int cols,
                                                           T* __restrict__ db) {
-  const int col = blockIdx.x * 256 + threadIdx.x;
-  if (col >= cols) return;
+  __shared__ float red[8][32];
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  const int col = blockIdx.x * 32 + l;
   float s = 0.0f;
-  for (int c = 0; c < chunks; ++c) s += part[static_cast<int64_t>(c) * cols + col];
-  const uint32_t w = Elem<T>::pack2(s, 0.0f);
-  reinterpret_cast<uint16_t*>(db)[col] = static_cast<uint16_t>(w & 0xffffu);
+  if (col < cols)
+    for (int c = w; c < chunks; c += 8) s += part[static_cast<int64_t>(c) * cols + col];
+  red[w][l] = s;
+  __syncthreads();
+  if (w == 0 && col < cols) {
+    float t = 0.0f;
+#pragma unroll
+    for (int x = 0; x < 8; ++x) t += red[x][l];
+    const uint32_t word = Elem<T>::pack2(t, 0.0f);
+    reinterpret_cast<uint16_t*>(db)[col] = static_cast<uint16_t>(word & 0xffffu);
+  }
 }
 
 // out = sum over splits (in order) of the fp32 partials, 8 elements a thread.
@@ -431,10 +497,11 @@ cudaError_t launch_gemm(const GemmParams& p_in, cudaStream_t stream) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
 
 // Workspace of the projection: a 256-byte header (error word), then the
 // gathered rows X_c (n x d_in), then (backward) G (n x d_out), the bias
-// partials (ceil(n / kGradRows) x d_out fp32) and the split-K partials of dW
+// partials (grad_chunks(n) x d_out fp32) and the split-K partials of dW
 // (kMaxKSplits x d_out x d_in fp32).
 struct ProjLayout {
   size_t xc = 0, g = 0, part = 0, dwp = 0, total = 0;
@@ -444,7 +511,7 @@ ProjLayout proj_layout(int64_t n, int d_in, int d_out, bool bwd) {
   l.xc = kHdrWords * 4;
   l.g = l.xc + align_up(static_cast<size_t>(n) * d_in * 2, 256);
   l.part = l.g + (bwd ? align_up(static_cast<size_t>(n) * d_out * 2, 256) : 0);
-  l.dwp = l.part + (bwd ? align_up(static_cast<size_t>((n + kGradRows - 1) / kGradRows) * d_out * 4, 256) : 0);
+  l.dwp = l.part + (bwd ? align_up(static_cast<size_t>(grad_chunks(n)) * d_out * 4, 256) : 0);
   l.total = l.dwp + (bwd ? align_up(static_cast<size_t>(kMaxKSplits) * d_out * d_in * 4, 256) : 0);
   return l;
 }
@@ -479,6 +546,7 @@ hstu_status_t project_fwd_t(const void* x, int64_t x_rows, const int32_t* rows, 
     return HSTU_ERR_CUDA;
   p.out = y;
   p.out2 = z;
+  p.wide = aligned32(y) && (!z || aligned32(z)) && (d_out * 2) % 32 == 0;
   p.bias = bias;
   p.err = err;
   p.M = static_cast<int32_t>(n);
@@ -504,12 +572,12 @@ hstu_status_t project_bwd_t(const void* dy, const void* z, const void* x, int64_
   }
   T* g = reinterpret_cast<T*>(base + l.g);
   float* part = reinterpret_cast<float*>(base + l.part);
-  const int chunks = static_cast<int>((n + kGradRows - 1) / kGradRows);
-  silu_grad_kernel<T><<<dim3(chunks, (d_out / 8 + 255) / 256), 256, 0, stream>>>(
+  const int chunks = grad_chunks(n);
+  silu_grad_kernel<T><<<dim3(chunks, (d_out / 8 + kGradThreads - 1) / kGradThreads), kGradThreads, 0, stream>>>(
       static_cast<const T*>(dy), static_cast<const T*>(z), n, d_out, g, part);
   if (cudaGetLastError() != cudaSuccess) return HSTU_ERR_CUDA;
   if (dbias) {
-    column_fold_kernel<T><<<(d_out + 255) / 256, 256, 0, stream>>>(part, chunks, d_out, static_cast<T*>(dbias));
+    column_fold_kernel<T><<<(d_out + 31) / 32, 256, 0, stream>>>(part, chunks, d_out, static_cast<T*>(dbias));
     if (cudaGetLastError() != cudaSuccess) return HSTU_ERR_CUDA;
   }
   const void* xc = x;
@@ -525,6 +593,7 @@ hstu_status_t project_bwd_t(const void* dy, const void* z, const void* x, int64_
       !operand_map(&p1.tm_b, w, d_out, d_in, dtype, true, kGemmBN))
     return HSTU_ERR_CUDA;
   p1.out = dx_c;
+  p1.wide = aligned32(dx_c) && (d_in * 2) % 32 == 0;
   p1.err = err;
   p1.M = static_cast<int32_t>(n);
   p1.N = d_in;
@@ -537,6 +606,7 @@ hstu_status_t project_bwd_t(const void* dy, const void* z, const void* x, int64_
       !operand_map(&p2.tm_b, xc, n, d_in, dtype, true, kGemmBN))
     return HSTU_ERR_CUDA;
   p2.out = dw;
+  p2.wide = aligned32(dw) && (d_in * 2) % 32 == 0;
   p2.err = err;
   p2.M = d_out;
   p2.N = d_in;

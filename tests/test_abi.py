@@ -39,6 +39,14 @@ def test_library_exports_every_declared_symbol(lib):
     assert set(_declared()) <= set(hb.EXPORTED) | set(_declared())
 
 
+def test_checked_build_exports_the_same_symbols(lib):
+    checked = hb.load(hb.CHECKED_LIB_PATH)
+    for name in _declared():
+        assert hasattr(checked, name), name
+    assert checked.hstu_status_string(7).decode() == lib.hstu_status_string(7).decode()
+    assert "checked build" in lib.hstu_status_string(7).decode()
+
+
 def _shape(**kw):
     s = dict(batch=4, total=1000, heads=2, dim=128, nfunc=5, max_seqlen=300, alpha=0.1, dim_v=0, dtype=0)
     s.update(kw)
@@ -117,10 +125,15 @@ def test_wait_timeout_hook_checks_its_arguments(lib):
     assert lib.hstu_attn_test_wait_timeout(vp(1 << 20), 2001, None) == 1  # limit too large
 
 
-def test_binding_fails_loudly_without_the_library(monkeypatch):
-    monkeypatch.setattr(hb, "_lib", None)
+def test_binding_fails_loudly_without_the_library():
     with pytest.raises(RuntimeError, match="missing"):
         hb.load(os.path.join(ROOT, "no_such_dir", "libhstu_attn.so"))
+    prev = hb.select_library(os.path.join(ROOT, "no_such_dir", "libhstu_attn.so"))
+    try:
+        with pytest.raises(RuntimeError, match="missing"):
+            hb.load()
+    finally:
+        hb.select_library(prev)
 
 
 def test_binding_has_no_cpu_path():

@@ -1,7 +1,8 @@
 """The candidate-row projection of the targets-only layer (tcgen05 GEMMs with
 a fused bias + SiLU epilogue) against the oracle: forward y and z,
 backward dx of the listed rows, dw and the bias gradient; M, N and K tails;
-all rows and a row list; bf16 and fp16.
+all rows and a row list; bf16 and fp16; more output tiles than SMs, and
+rows wider than one block of the SiLU-gradient kernel (d_out > 2048).
 
 Tolerances follow from the arithmetic: inputs in the 16-bit type, fp32
 accumulation, outputs rounded once to the 16-bit type (relative 2^-9 for
@@ -32,7 +33,7 @@ def _inputs(T, d_in, d_out, dtype, seed):
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
 @pytest.mark.parametrize("T,d_in,d_out,n_rows", [(300, 128, 192, 77), (1000, 512, 1024, 260), (50, 64, 64, 1),
-                                                  (700, 256, 320, None)])
+                                                  (700, 256, 320, None), (5000, 128, 2112, None)])
 def test_projection_matches_the_oracle(dtype, T, d_in, d_out, n_rows):
     x, w, b, dy_all = _inputs(T, d_in, d_out, dtype, seed=d_in + d_out)
     if n_rows is None:
