@@ -57,22 +57,27 @@ constexpr int kEpiPartial = 2;   // partial[split] = acc in fp32 (split K)
 
 struct GemmParams {
   CUtensorMap tm_a, tm_b;
+  CUtensorMap tm_out, tm_out2;  // 16-bit outputs (boxes of 64 columns x 32 rows), stored by TMA
   void* out;
   void* out2;
   const void* bias;
   int32_t* err;  // error word (nullable): kErrTimeout on a timed-out wait
   float* partial;  // kEpiPartial: (k_splits, M, N) fp32
   int32_t M, N, K, ldo, k_splits;
-  int32_t wide;  // out, out2 and ldo allow 32-byte stores
 };
 
 struct GemmSmem {
   alignas(1024) uint8_t a[kGemmStages][kGemmBM * kGemmBK * 2];  // 16 KB a stage
   alignas(1024) uint8_t b[kGemmStages][kGemmBN * kGemmBK * 2];  // 32 KB a stage
+  // Output staging of each epilogue warp: its 32 rows x 64 columns of out
+  // and of out2, 128-byte rows in the 128-byte swizzle the TMA store reads.
+  alignas(1024) uint8_t stage_out[4][32 * 128];
+  alignas(1024) uint8_t stage_out2[4][32 * 128];
   alignas(8) uint64_t bar_full[kGemmStages], bar_empty[kGemmStages], bar_acc_full[2], bar_acc_empty[2], bar_drain;
   uint32_t tmem_base;
   int abort_flag;
 };
+static_assert(sizeof(GemmSmem) + 1024 <= 232448, "GEMM shared memory over the per-CTA limit");
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
   asm volatile(
@@ -81,6 +86,29 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+// TMA store of a {64 columns, 32 rows} box from shared memory (bulk group).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(src)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Waits until the committed bulk stores have read their shared memory.
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Waits until the committed bulk stores have completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Makes this thread's generic-proxy shared-memory writes visible to TMA.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y,
                                             int z) {
   asm volatile(
@@ -231,8 +259,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
+    // Warp w reads TMEM lanes 32w.. (rows m0 + 32w + lane). fp32 partials
+    // leave as 32-byte row stores; 16-bit outputs go through the warp's
+    // staging buffers and leave as TMA stores of 32 rows x 64 columns, so
+    // the global writes are whole 128-byte lines instead of a row a thread.
     const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
     const T* bias = static_cast<const T*>(p.bias);
+    const uint32_t st_out = smem_u32(s.stage_out[warp]), st_out2 = smem_u32(s.stage_out2[warp]);
+    const bool want2 = EPI == kEpiBiasSilu && p.out2 != nullptr;
+    bool pending = false;  // lane 0: committed bulk stores may still read the staging buffers
     int i = 0;
     for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++i) {
       int m0, n0, split, kb0, kb1;
@@ -241,53 +276,77 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&s.bar_acc_full[buf]), (i >> 1) & 1, abort_flag))) break;
       tc_fence_after();
       const bool empty = kb1 == kb0;  // nothing accumulated: zeros
-      const int row = m0 + warp * 32 + lane;
-      T* out = static_cast<T*>(p.out) + static_cast<int64_t>(row) * p.ldo;
-      T* out2 = p.out2 ? static_cast<T*>(p.out2) + static_cast<int64_t>(row) * p.ldo : nullptr;
-      for (int c = 0; c < kGemmBN / 32; ++c) {
-        const int col = n0 + c * 32;
-        uint32_t a[32];
-        tmem_ld32(tbase + buf * kGemmBN + lane_addr + c * 32, a);
-        tmem_ld_wait(a);
-        if (empty)
+      const int row0 = m0 + warp * 32, row = row0 + lane;
+      if (EPI == kEpiPartial) {
+        for (int c = 0; c < kGemmBN / 32; ++c) {
+          const int col = n0 + c * 32;
+          uint32_t a[32];
+          tmem_ld32(tbase + buf * kGemmBN + lane_addr + c * 32, a);
+          tmem_ld_wait(a);
+          if (empty)
 #pragma unroll
-          for (int e = 0; e < 32; ++e) a[e] = 0u;
-        if (row >= p.M || col >= p.N) continue;  // N is a multiple of 32
-        if (EPI == kEpiPartial) {  // fp32 rows of the workspace: always 32-byte aligned
+            for (int e = 0; e < 32; ++e) a[e] = 0u;
+          if (row >= p.M || col >= p.N) continue;  // N is a multiple of 32
+          // fp32 rows of the workspace: always 32-byte aligned
           float* dst = p.partial + (static_cast<int64_t>(split) * p.M + row) * p.N + col;
 #pragma unroll
           for (int e = 0; e < 4; ++e) store_words8(dst + 8 * e, a + 8 * e, true);
-          continue;
         }
-        uint32_t pk[16], pz[16];
+      } else {
+        for (int c = 0; c < kGemmBN / 64; ++c) {
+          const int col = n0 + c * 64;
+          uint32_t a[32], b2[32];
+          tmem_ld32(tbase + buf * kGemmBN + lane_addr + c * 64, a);
+          tmem_ld32(tbase + buf * kGemmBN + lane_addr + c * 64 + 32, b2);
+          tmem_ld_wait(a);
+          tmem_ld_wait(b2);
+          if (col >= p.N || row0 >= p.M) continue;  // warp-uniform; N is a multiple of 64
+          uint32_t pk[32], pz[32];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          float x0 = __uint_as_float(a[2 * e]), x1 = __uint_as_float(a[2 * e + 1]);
-          if (EPI == kEpiBiasSilu) {
-            if (bias) {
-              const uint32_t bw = *reinterpret_cast<const uint32_t*>(bias + col + 2 * e);
-              x0 += Elem<T>::lo(bw);
-              x1 += Elem<T>::hi(bw);
+          for (int e = 0; e < 32; ++e) {
+            const uint32_t w0 = e < 16 ? a[2 * e] : b2[2 * e - 32];
+            const uint32_t w1 = e < 16 ? a[2 * e + 1] : b2[2 * e - 31];
+            float x0 = empty ? 0.0f : __uint_as_float(w0), x1 = empty ? 0.0f : __uint_as_float(w1);
+            if (EPI == kEpiBiasSilu) {
+              if (bias) {
+                const uint32_t bw = *reinterpret_cast<const uint32_t*>(bias + col + 2 * e);
+                x0 += Elem<T>::lo(bw);
+                x1 += Elem<T>::hi(bw);
+              }
+              pz[e] = Elem<T>::pack2(x0, x1);
+              // silu(x) = x/2 (1 + tanh(x/2)): one hardware tanh an element
+              const float h0 = 0.5f * x0, h1 = 0.5f * x1;
+              pk[e] = Elem<T>::pack2(fmaf(h0, tanh_approx(h0), h0), fmaf(h1, tanh_approx(h1), h1));
+            } else {
+              pk[e] = Elem<T>::pack2(x0, x1);
             }
-            pz[e] = Elem<T>::pack2(x0, x1);
-            // silu(x) = x/2 (1 + tanh(x/2)): one hardware tanh an element
-            const float h0 = 0.5f * x0, h1 = 0.5f * x1;
-            pk[e] = Elem<T>::pack2(fmaf(h0, tanh_approx(h0), h0), fmaf(h1, tanh_approx(h1), h1));
-          } else {
-            pk[e] = Elem<T>::pack2(x0, x1);
           }
-        }
-        const bool wide = p.wide != 0;
+          // The previous chunk's stores must have read the staging buffers.
+          if (lane == 0 && pending) bulk_wait_read_all();
+          __syncwarp();
+          // Row `lane`, 16-byte piece j lands at piece j ^ (lane & 7) of the
+          // row (128-byte swizzle: conflict-free across each 8-row group).
 #pragma unroll
-        for (int e = 0; e < 2; ++e) store_words8(out + col + 16 * e, pk + 8 * e, wide);
-        if (EPI == kEpiBiasSilu && out2) {
-#pragma unroll
-          for (int e = 0; e < 2; ++e) store_words8(out2 + col + 16 * e, pz + 8 * e, wide);
+          for (int j = 0; j < 8; ++j) {
+            const uint32_t off = static_cast<uint32_t>(lane * 128 + ((j ^ (lane & 7)) << 4));
+            st_shared_v4(st_out + off, pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+            if (want2) st_shared_v4(st_out2 + off, pz[4 * j], pz[4 * j + 1], pz[4 * j + 2], pz[4 * j + 3]);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {  // rows past M are clipped by the tensor map
+            tma_store_2d(&p.tm_out, st_out, col, row0);
+            if (want2) tma_store_2d(&p.tm_out2, st_out2, col, row0);
+            bulk_commit();
+            pending = true;
+          }
         }
       }
       tc_fence_before();
       mbar_arrive(smem_u32(&s.bar_acc_empty[buf]));
     }
+    if (lane == 0 && pending) bulk_wait_all();  // every store done before the CTA exits
+    __syncwarp();
   }
   tc_fence_before();
   __syncthreads();
@@ -497,7 +556,6 @@ cudaError_t launch_gemm(const GemmParams& p_in, cudaStream_t stream) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
 
 // Workspace of the projection: a 256-byte header (error word), then the
 // gathered rows X_c (n x d_in), then (backward) G (n x d_out), the bias
@@ -546,7 +604,9 @@ hstu_status_t project_fwd_t(const void* x, int64_t x_rows, const int32_t* rows, 
     return HSTU_ERR_CUDA;
   p.out = y;
   p.out2 = z;
-  p.wide = aligned32(y) && (!z || aligned32(z)) && (d_out * 2) % 32 == 0;
+  if (!operand_map(&p.tm_out, y, n, d_out, dtype, false, 32) ||
+      (z && !operand_map(&p.tm_out2, z, n, d_out, dtype, false, 32)))
+    return HSTU_ERR_CUDA;
   p.bias = bias;
   p.err = err;
   p.M = static_cast<int32_t>(n);
@@ -593,7 +653,7 @@ hstu_status_t project_bwd_t(const void* dy, const void* z, const void* x, int64_
       !operand_map(&p1.tm_b, w, d_out, d_in, dtype, true, kGemmBN))
     return HSTU_ERR_CUDA;
   p1.out = dx_c;
-  p1.wide = aligned32(dx_c) && (d_in * 2) % 32 == 0;
+  if (!operand_map(&p1.tm_out, dx_c, n, d_in, dtype, false, 32)) return HSTU_ERR_CUDA;
   p1.err = err;
   p1.M = static_cast<int32_t>(n);
   p1.N = d_in;
@@ -606,7 +666,7 @@ hstu_status_t project_bwd_t(const void* dy, const void* z, const void* x, int64_
       !operand_map(&p2.tm_b, xc, n, d_in, dtype, true, kGemmBN))
     return HSTU_ERR_CUDA;
   p2.out = dw;
-  p2.wide = aligned32(dw) && (d_in * 2) % 32 == 0;
+  if (!operand_map(&p2.tm_out, dw, d_out, d_in, dtype, false, 32)) return HSTU_ERR_CUDA;
   p2.err = err;
   p2.M = d_out;
   p2.N = d_in;
