@@ -201,6 +201,7 @@ HSTU_API hstu_status_t hstu_attn_bwd_targets(const void* dout_c, const void* q_c
  *          for every tensor
  *   ws     DEVICE, hstu_attn_project_workspace_size(rows ? num_rows : 0,
  *          d_in, d_out, 0) bytes, 256-byte aligned
+ * x, w, bias, y and z must be 16-byte aligned (else HSTU_ERR_INVALID_ARG).
  * A row index outside [0, x_rows) sets HSTU_ERR_DEVICE_INPUT in ws's error
  * word (read with hstu_attn_get_device_status) and gives a zero input row. */
 HSTU_API size_t hstu_attn_project_workspace_size(int64_t num_rows, int32_t d_in, int32_t d_out, int32_t backward);

@@ -295,12 +295,30 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       } else {
         for (int c = 0; c < kGemmBN / 64; ++c) {
           const int col = n0 + c * 64;
+          // The chunk's 64 bias values (the same for every row): eight
+          // 16-byte loads issued before the TMEM loads, so that both
+          // latencies overlap.
+          uint32_t bw[32];
+          const bool live = col < p.N && row0 < p.M;  // warp-uniform; N is a multiple of 64
+          if (EPI == kEpiBiasSilu && bias && live) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const uint4 v = *reinterpret_cast<const uint4*>(bias + col + 8 * q);
+              bw[4 * q] = v.x;
+              bw[4 * q + 1] = v.y;
+              bw[4 * q + 2] = v.z;
+              bw[4 * q + 3] = v.w;
+            }
+          } else {
+#pragma unroll
+            for (int q = 0; q < 32; ++q) bw[q] = 0u;
+          }
           uint32_t a[32], b2[32];
           tmem_ld32(tbase + buf * kGemmBN + lane_addr + c * 64, a);
           tmem_ld32(tbase + buf * kGemmBN + lane_addr + c * 64 + 32, b2);
           tmem_ld_wait(a);
           tmem_ld_wait(b2);
-          if (col >= p.N || row0 >= p.M) continue;  // warp-uniform; N is a multiple of 64
+          if (!live) continue;
           uint32_t pk[32], pz[32];
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
@@ -308,11 +326,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
             const uint32_t w1 = e < 16 ? a[2 * e + 1] : b2[2 * e - 31];
             float x0 = empty ? 0.0f : __uint_as_float(w0), x1 = empty ? 0.0f : __uint_as_float(w1);
             if (EPI == kEpiBiasSilu) {
-              if (bias) {
-                const uint32_t bw = *reinterpret_cast<const uint32_t*>(bias + col + 2 * e);
-                x0 += Elem<T>::lo(bw);
-                x1 += Elem<T>::hi(bw);
-              }
+              x0 += Elem<T>::lo(bw[e]);  // zero without a bias
+              x1 += Elem<T>::hi(bw[e]);
               pz[e] = Elem<T>::pack2(x0, x1);
               // silu(x) = x/2 (1 + tanh(x/2)): one hardware tanh an element
               const float h0 = 0.5f * x0, h1 = 0.5f * x1;
@@ -707,7 +722,7 @@ HSTU_API hstu_status_t hstu_attn_project_rows(const void* x, int64_t x_rows, con
   if (st != HSTU_OK) return st;
   if (!rows && num_rows != x_rows) return HSTU_ERR_INVALID_ARG;
   if (num_rows > 0 && (!hstu::aligned16(x) || !hstu::aligned16(w) || !hstu::aligned16(y) ||
-                       (z && !hstu::aligned16(z)) || (bias && (reinterpret_cast<uintptr_t>(bias) & 3u))))
+                       (z && !hstu::aligned16(z)) || (bias && !hstu::aligned16(bias))))
     return HSTU_ERR_INVALID_ARG;
   if (rows && (reinterpret_cast<uintptr_t>(rows) & 3u)) return HSTU_ERR_INVALID_ARG;
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) ||
