@@ -22,7 +22,9 @@
 // blocks flow through a 4-stage TMA ring (48 KB a stage, 128-byte swizzle)
 // that runs on across tiles; one elected thread issues M=128, N=256, K=16
 // MMAs into one of two 256-column TMEM accumulators, so that four epilogue
-// warps read one tile out (a row per thread) while the next accumulates.
+// warps read one tile out (a row per thread) while the next accumulates; the
+// 16-bit results leave through each warp's shared-memory staging buffer as
+// TMA stores of 32 rows x 64 columns.
 // dW, whose K is the number of rows, splits K over up to eight tiles per
 // output tile; their fp32 partial tiles are summed in split order
 // (deterministic) by a fold kernel.
@@ -129,18 +131,12 @@ __device__ __forceinline__ void load_operand(uint32_t dst, const CUtensorMap* ma
   else tma_load_2d(dst, map, bar, k0, mn0);
 }
 
-// Stores 32 bytes (eight words) at a 32-byte aligned address, or as two
-// 16-byte halves: a whole sector per store reaches L2 in one request.
-__device__ __forceinline__ void store_words8(void* dst, const uint32_t* w, bool wide) {
-  if (wide) {
-    asm volatile("st.global.L1::no_allocate.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(w[0]),
-                 "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
-                 : "memory");
-  } else {
-    uint4* d = static_cast<uint4*>(dst);
-    d[0] = make_uint4(w[0], w[1], w[2], w[3]);
-    d[1] = make_uint4(w[4], w[5], w[6], w[7]);
-  }
+// Stores 32 bytes (eight words) at a 32-byte aligned address: a whole
+// sector per store reaches L2 in one request.
+__device__ __forceinline__ void store_words8(void* dst, const uint32_t* w) {
+  asm volatile("st.global.L1::no_allocate.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(w[0]),
+               "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
 }
 
 // Shared-memory descriptor of K-step kk (16 deep) of a stage tile.
@@ -290,7 +286,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
           // fp32 rows of the workspace: always 32-byte aligned
           float* dst = p.partial + (static_cast<int64_t>(split) * p.M + row) * p.N + col;
 #pragma unroll
-          for (int e = 0; e < 4; ++e) store_words8(dst + 8 * e, a + 8 * e, true);
+          for (int e = 0; e < 4; ++e) store_words8(dst + 8 * e, a + 8 * e);
         }
       } else {
         for (int c = 0; c < kGemmBN / 64; ++c) {
