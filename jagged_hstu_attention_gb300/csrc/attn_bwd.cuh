@@ -4,10 +4,11 @@
 // early take the remaining items, and a CTA keeps its pipelines running
 // across items of either role.
 //
-// dK/dV role -- item (sequence b, kv tile kt, head h). K and V of the tile
-// stay in SMEM; the Q and dO tiles of every q tile that visits kt stream
-// through a ring of 64-row halves. Per half (TMEM lanes = kv rows):
-//     S^T  = K Q^T,  dP^T = V dO^T                      (SMEM x SMEM)
+// dK/dV role -- item (sequence b, kv tile kt, head h). K of the tile is
+// copied into TMEM and V stays in SMEM; the Q and dO tiles of every q tile
+// that visits kt stream through a ring of 64-row halves. Per half (TMEM
+// lanes = kv rows):
+//     S^T  = K Q^T   (TMEM x SMEM),  dP^T = V dO^T        (SMEM x SMEM)
 //     P^T  = silu(alpha S^T)/N,  dS^T = dP^T * silu'(alpha S^T) * alpha/N
 //            (masked on partial tiles, both packed bf16 in place over S^T;
 //            the common factor alpha/(2N) is applied once at the stores)
@@ -35,19 +36,20 @@
 // has read out the previous item's accumulators.
 //
 // TMEM (512 columns): acc0 [0,128) (dV or dQ), acc1 [128,256) (dK, or the
-// dQ role's Q and dO), three S slots at 256, 320 and 384, one dP slot at 448
-// (64 columns each).
+// dQ role's Q and dO), two S slots at 256 and 320, one dP slot at 384 (64
+// columns each), and the dK/dV role's K at 448.
 //
 // Half-step pipeline: every 128-wide tile is handled as two 64-column halves
 // ("half-steps", counted globally as v). S(v) and dP(v) are N=64 MMAs; S(v)
-// goes to S slot v % 3, dP(v) to the single dP slot. The epilogue warps form
+// goes to S slot v % 2, dP(v) to the single dP slot. The epilogue warps form
 // two groups of four (TMEM lanes 32(w%4)..); group h takes the half-steps with
-// v % 2 == h. A group first reads all of dP(v) and releases the dP slot, so
-// that dP(v+1) can be computed while it converts; it then packs P^T and dS^T
-// (or dS alone) as bf16 over the S columns it has read. Since S slots are
-// reused only every third half-step, S/dP of v + 3 are issued right after the
-// accumulating MMAs of v, and a group's conversion of v overlaps the tensor
-// work of two later half-steps instead of one.
+// v % 2 == h, always S slot h. A group first reads all of dP(v) and releases
+// the dP slot, so that dP(v+1) can be computed while it converts; it then
+// packs P^T and dS^T (or dS alone) as bf16 over the S columns it has read.
+// S/dP of v + 2 are issued right after the accumulating MMAs of v, so a
+// group's conversion of v overlaps the tensor work of the next half-step.
+// (Three S slots with K in SMEM measured 1.6% slower on DLRM: the dK/dV
+// role's S^T with both operands in SMEM is bound by shared-memory reads.)
 //
 // Partial-tile masks of the dK/dV role are built by transposition inside
 // each warp: lane l takes the two q rows of its half's chunks, computes which
@@ -99,11 +101,12 @@ struct BwdSmem {
   // TMEM slots of 64 columns after the two accumulators: kSSlots for S
   // (packed P/dS are written over them) and kDpSlots for dP. S/dP of step
   // v + kSSlots are issued right after the accumulating MMAs of step v.
-  // Two S and two dP slots measured the same as three and one on DLRM and
-  // OneRank and 3% slower on SLA.
-  static constexpr int kSSlots = 3;
+  static constexpr int kSSlots = 2;
   static constexpr int kDpSlots = 1;
-  static_assert(256 + 64 * (kSSlots + kDpSlots) <= 512, "TMEM holds 512 columns");
+  // The dK/dV role copies its resident K into TMEM after the S and dP
+  // slots (DPQ / 2 columns), so that S^T reads A from TMEM.
+  static constexpr int kKCols = 256 + 64 * (kSSlots + kDpSlots);
+  static_assert(kKCols + DPQ / 2 <= 512, "TMEM holds 512 columns");
   alignas(8) uint64_t bar_res_full, bar_res_empty, bar_full[kSlots], bar_empty[kSlots],
       bar_s_full[kSSlots], bar_p_full[kSSlots], bar_dp_free[kDpSlots], bar_acc_full, bar_acc_empty,
       bar_item_full[2], bar_item_empty[2], bar_drain;
@@ -252,6 +255,7 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
   const uint32_t t_acc1 = tbase + 128;  // dK (dK/dV role)
   const uint32_t tS = tbase + 256;      // S slot k at tS + 64 k
   const uint32_t tdP = tS + 64 * Smem::kSSlots;  // dP slot j at tdP + 64 j
+  const uint32_t tK = tbase + Smem::kKCols;       // dK/dV role: resident K
   volatile int* abort_flag = &s.abort_flag;
   const size_t nt_all = static_cast<size_t>(p.nt);
 
@@ -382,7 +386,7 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
     // ------------------------------------------------------------ MMA issuer
     if (elect_one_sync()) {
       // Half-step pipeline: step v covers the 64-column half (v & 1) of tile
-      // v >> 1. S/dP run three steps ahead of the accumulating MMAs.
+      // v >> 1. S/dP run kSSlots steps ahead of the accumulating MMAs.
       constexpr uint32_t idesc_s = idesc_f16kind(128, 64, false, false, Elem<T>::kUmma);
       // dV accumulates DPV columns (B = dO); dK and dQ DPQ columns (B = Q or K).
       constexpr uint32_t idesc_accv = idesc_f16kind(128, DPV, false, true, Elem<T>::kUmma);
@@ -440,12 +444,19 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
           for (int kk = 0; kk < DPV / 16; ++kk)
             tmem_cp_128x256b(tdOr + 8 * kk, sdesc_advance(dr1, (kk >> 2) * kChunkBytes + (kk & 3) * 32));
           umma_commit(smem_u32(&s.bar_res_empty));  // shared-memory residents free once copied
+        } else {
+          // K into TMEM for S^T = K Q^T. Its previous readers, the S MMAs of
+          // the previous dK/dV item, completed before that item's last
+          // accumulating MMAs were issued.
+#pragma unroll
+          for (int kk = 0; kk < DPQ / 16; ++kk)
+            tmem_cp_128x256b(tK + 8 * kk, sdesc_advance(dr0, (kk >> 2) * kChunkBytes + (kk & 3) * 32));
         }
         const int nsteps = s.item[slot].nhs;
         const int gv0 = ghs;  // global index of this item's first half-step
         // S/dP of step v (N = 64 MMAs): S (or S^T) = res0 . str0_h^T into S
-        // slot gv % 3, dP (or dP^T) = res1 . str1_h^T into the dP slot once
-        // the epilogue has read dP of step gv - 1 out of it.
+        // slot gv % kSSlots, dP (or dP^T) = res1 . str1_h^T into the dP slot
+        // once the epilogue has read dP of step gv - 1 out of it.
         auto issue_sdp = [&](int v) -> bool {
           const int gv = gv0 + v, st = gv % Smem::kSlots, k = gv % Smem::kSSlots, j = gv % Smem::kDpSlots;
           if (!mbar_wait(smem_u32(&s.bar_full[st]), (gv / Smem::kSlots) & 1, abort_flag)) return false;
@@ -454,9 +465,8 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
           if (dkdv) {
 #pragma unroll
             for (int kk = 0; kk < DPQ / 16; ++kk) {
-              const uint32_t aoff = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
               const uint32_t boff = (kk >> 2) * kHalfChunk + (kk & 3) * 32;
-              umma_ss(tS + 64 * k, sdesc_advance(dr0, aoff), sdesc_advance(b0, boff), idesc_s, kk > 0);
+              umma_ts(tS + 64 * k, tK + 8 * kk, sdesc_advance(b0, boff), idesc_s, kk > 0);
             }
           } else {
 #pragma unroll

@@ -57,8 +57,8 @@ def test_kernel_hash_ignores_comments_but_not_code(tmp_path, monkeypatch):
     text = p.read_text()
     p.write_text("// a new comment line\n" + text.replace("\n", "\n\n", 3) + "\n/* block\n comment */\n")
     assert bench.kernel_sources_sha() == base
-    assert "kSSlots = 3" in text
-    p.write_text(text.replace("kSSlots = 3", "kSSlots = 2", 1))
+    assert "kDpSlots = 1" in text
+    p.write_text(text.replace("kDpSlots = 1", "kDpSlots = 2", 1))
     assert bench.kernel_sources_sha() != base
 
 
