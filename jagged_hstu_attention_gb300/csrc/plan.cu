@@ -164,7 +164,8 @@ __device__ void block_exclusive_scan(int* cnt, int n) {
 // Q/dO) tiles in L2 instead of streaming every sequence's tiles from HBM at
 // once. Within a sequence the heaviest items come first: forward q tiles
 // last-first (the later rows of causal-like masks see the most columns);
-// backward dK/dV kv tiles first-first, then dQ q tiles last-first. Sequences
+// backward dK/dV kv tiles first-first and dQ q tiles last-first, the two
+// roles grouped in windows of list entries (below). Sequences
 // of equal length may come out in any order: every output element is
 // computed by exactly one CTA with a fixed internal order, so the order only
 // changes scheduling, never results.
@@ -173,6 +174,8 @@ __device__ void block_exclusive_scan(int* cnt, int n) {
 // [0, max_seqlen]) and writes the header: the error word (kErrInput, with
 // empty lists, if the check fails), the list lengths, the uniform flag and
 // the zeroed work counters.
+constexpr int kRoleWindow = 128;  // list entries (tile pairs) per role window
+
 __device__ void build_work_lists(const PlanParams& p) {
   __shared__ int hist[kMaxTiles + 1];
   __shared__ int n_items;
@@ -222,18 +225,27 @@ __device__ void build_work_lists(const PlanParams& p) {
   __syncthreads();
   block_exclusive_scan(p.seq_start, p.batch);
   __syncthreads();
+  if (tid == 0) n_items = p.seq_start[p.batch - 1] + tiles_of(p.seq_order[p.batch - 1]);
+  __syncthreads();
+  // Backward: entry e = st + t of the sequence-major order goes to window
+  // w = e / kRoleWindow; a window lists its dK/dV items first, then its dQ
+  // items (the dQ item paired with kv tile t is q tile n - 1 - t). A CTA
+  // then runs a few items of one role before the other, and a dQ item
+  // seldom follows a dK/dV item, whose accumulator read-out it would wait
+  // for; a window's sequences still fit in L2 together.
+  const int total = n_items;
   for (int pos = tid; pos < p.batch; pos += blockDim.x) {
     const int b = p.seq_order[pos];
     const int n = tiles_of(b);
     const int st = p.seq_start[pos];
     for (int t = 0; t < n; ++t) {
-      p.fwd_list[st + t] = (b << 8) | (n - 1 - t);
-      p.bwd_list[2 * st + t] = (b << 8) | t | kRoleDkdv;
-      p.bwd_list[2 * st + n + t] = (b << 8) | (n - 1 - t);
+      const int e = st + t, w0 = e / kRoleWindow * kRoleWindow;
+      const int len = min(kRoleWindow, total - w0);
+      p.fwd_list[e] = (b << 8) | (n - 1 - t);
+      p.bwd_list[2 * w0 + (e - w0)] = (b << 8) | t | kRoleDkdv;
+      p.bwd_list[2 * w0 + len + (e - w0)] = (b << 8) | (n - 1 - t);
     }
   }
-  if (tid == 0) n_items = p.seq_start[p.batch - 1] + tiles_of(p.seq_order[p.batch - 1]);
-  __syncthreads();
   if (tid == 0) {
     p.header[kHdrErr] = 0;
     p.header[kHdrNFwd] = n_items;
