@@ -129,6 +129,7 @@ hstu::PlanParams plan_params(const int32_t* seq_offsets, const int32_t* func,
   p.nfunc = s->nfunc;
   p.nt = l.nt;
   p.max_seqlen = s->max_seqlen;
+  p.role_window = hstu::role_window(s->num_heads, s->head_dim, dim_v(s));
   return p;
 }
 

@@ -126,7 +126,19 @@ struct PlanParams {
   uint8_t* cls;
   int64_t total;
   int32_t batch, nfunc, nt, max_seqlen;
+  int32_t role_window;  // backward list entries per role window (role_window())
 };
+
+// Backward list entries per role window: as many as keep a window's q, k, v
+// and dO rows (128 rows an entry, every head) within 32 MB, a quarter of L2,
+// at most 128 and at least 16. (With 64 MB the SLA B=16 S=2048 H=8 backward
+// re-read its tiles from HBM and ran 6% slower; with 32 MB every workload
+// measured here ran at least as fast as without windows.)
+inline int role_window(int heads, int dim, int dim_v) {
+  const long long per_entry = 128LL * heads * (2LL * dim + 2LL * dim_v) * 2;
+  const long long w = (32LL << 20) / (per_entry > 0 ? per_entry : 1);
+  return static_cast<int>(w < 16 ? 16 : (w > 128 ? 128 : w));
+}
 
 // Element types of q, k, v, dO and the outputs (one type for all of them).
 constexpr int kDtypeBf16 = 0, kDtypeF16 = 1;

@@ -174,8 +174,6 @@ __device__ void block_exclusive_scan(int* cnt, int n) {
 // [0, max_seqlen]) and writes the header: the error word (kErrInput, with
 // empty lists, if the check fails), the list lengths, the uniform flag and
 // the zeroed work counters.
-constexpr int kRoleWindow = 128;  // list entries (tile pairs) per role window
-
 __device__ void build_work_lists(const PlanParams& p) {
   __shared__ int hist[kMaxTiles + 1];
   __shared__ int n_items;
@@ -228,19 +226,19 @@ __device__ void build_work_lists(const PlanParams& p) {
   if (tid == 0) n_items = p.seq_start[p.batch - 1] + tiles_of(p.seq_order[p.batch - 1]);
   __syncthreads();
   // Backward: entry e = st + t of the sequence-major order goes to window
-  // w = e / kRoleWindow; a window lists its dK/dV items first, then its dQ
+  // w = e / role_window; a window lists its dK/dV items first, then its dQ
   // items (the dQ item paired with kv tile t is q tile n - 1 - t). A CTA
   // then runs a few items of one role before the other, and a dQ item
   // seldom follows a dK/dV item, whose accumulator read-out it would wait
-  // for; a window's sequences still fit in L2 together.
-  const int total = n_items;
+  // for; the window is sized so that its sequences' tiles stay in L2.
+  const int total = n_items, win = p.role_window;
   for (int pos = tid; pos < p.batch; pos += blockDim.x) {
     const int b = p.seq_order[pos];
     const int n = tiles_of(b);
     const int st = p.seq_start[pos];
     for (int t = 0; t < n; ++t) {
-      const int e = st + t, w0 = e / kRoleWindow * kRoleWindow;
-      const int len = min(kRoleWindow, total - w0);
+      const int e = st + t, w0 = e / win * win;
+      const int len = min(win, total - w0);
       p.fwd_list[e] = (b << 8) | (n - 1 - t);
       p.bwd_list[2 * w0 + (e - w0)] = (b << 8) | t | kRoleDkdv;
       p.bwd_list[2 * w0 + len + (e - w0)] = (b << 8) | (n - 1 - t);
