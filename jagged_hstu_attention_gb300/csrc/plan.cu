@@ -231,7 +231,13 @@ __device__ void build_work_lists(const PlanParams& p) {
   // then runs a few items of one role before the other, and a dQ item
   // seldom follows a dK/dV item, whose accumulator read-out it would wait
   // for; the window is sized so that its sequences' tiles stay in L2.
-  const int total = n_items, win = p.role_window;
+  // Batches whose sequences all have the same tile count n use windows of
+  // n, one sequence each (its dK/dV items, then its dQ items): their CTAs
+  // take items by a fixed stride, which balances that order by
+  // construction, and a window spanning sequences can unbalance it.
+  const int n_first = tiles_of(p.seq_order[0]);
+  const bool uniform = n_first == tiles_of(p.seq_order[p.batch - 1]);
+  const int total = n_items, win = uniform ? max(n_first, 1) : p.role_window;
   for (int pos = tid; pos < p.batch; pos += blockDim.x) {
     const int b = p.seq_order[pos];
     const int n = tiles_of(b);
