@@ -27,10 +27,10 @@
 //               factor alpha / (2N), applied once to O at the store), with
 //               the row's interval mask on partial tiles only (full tiles run
 //               no mask arithmetic), packed to bf16 in place over the first 64
-//               columns of the buffer. At the end of an item groups 0 and 1
+//               columns of the buffer. At the end of an item two groups
 //               each store half of O's columns (bf16, rows past L_b
-//               untouched; rows that see no column get zeros) while group 2
-//               goes on to the next item.
+//               untouched; rows that see no column get zeros) while the
+//               group that takes the next item's first tile goes on.
 //   warp 15     idle: 16 warps at 128 registers fill the register file, and
 //               a third epilogue group hides more TMEM and MUFU latency than
 //               two groups at 168 registers.
@@ -66,12 +66,17 @@ struct FwdSmem {
   alignas(1024) uint8_t k[kStages][kTileQ];
   alignas(1024) uint8_t v[kStages][kTileV];
   alignas(8) uint64_t bar_q_full, bar_q_empty, bar_k_full[kStages], bar_k_empty[kStages],
-      bar_v_full[kStages], bar_v_empty[kStages], bar_s_full[3], bar_p_full[3], bar_o_full,
+      bar_v_full[kStages], bar_v_empty[kStages], bar_s_full[3], bar_p_full[3], bar_o_full[2],
       bar_o_empty, bar_item_full[2], bar_item_empty[2], bar_drain;
   uint32_t tmem_base;
   int abort_flag;
   FwdItem item[2];
 };
+
+// 227 KB of dynamic shared memory per CTA, with 1 KB of alignment slack.
+static_assert(sizeof(FwdSmem<128, 128>) + 1024 <= 232448, "forward shared memory over the per-CTA limit");
+static_assert(sizeof(FwdSmem<128, 64>) + 1024 <= 232448, "forward shared memory over the per-CTA limit");
+static_assert(sizeof(FwdSmem<64, 128>) + 1024 <= 232448, "forward shared memory over the per-CTA limit");
 
 template <typename S>
 __device__ __forceinline__ S& fwd_smem_as(uint8_t* raw) {
@@ -163,8 +168,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1) hstu_fwd_kernel(const __grid_c
       mbar_init(smem_u32(&s.bar_s_full[i]), 1);
       mbar_init(smem_u32(&s.bar_p_full[i]), 128);
     }
-    mbar_init(smem_u32(&s.bar_o_full), 1);
-    mbar_init(smem_u32(&s.bar_o_empty), 256);  // epilogue groups 0 and 1 read O out
+    // O is final: one barrier per item slot. The groups that read an item's
+    // O out change from item to item; a group that skipped the previous
+    // items cannot be two phases behind a slot's barrier, because an item
+    // is published in its slot only after the read-out of the item two
+    // before it.
+    for (int i = 0; i < 2; ++i) mbar_init(smem_u32(&s.bar_o_full[i]), 1);
+    mbar_init(smem_u32(&s.bar_o_empty), 256);  // the two epilogue groups that read O out
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&s.bar_item_full[i]), 1);
       mbar_init(smem_u32(&s.bar_item_empty[i]), 2 + 384);  // MMA issuer, V producer, epilogue
@@ -413,7 +423,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) hstu_fwd_kernel(const __grid_c
           }
         }
         if (!ok) break;
-        umma_commit(smem_u32(&s.bar_o_full));
+        umma_commit(smem_u32(&s.bar_o_full[slot]));
         g += nt;
         ++q_uses;
       }
@@ -430,7 +440,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) hstu_fwd_kernel(const __grid_c
     const float out_scale = 0.5f * p.alpha * p.inv_n;  // hc = alpha / (2N)
     const bool wide = wide_rows_ok(p.out0, p.out0, p.out0, p.dim_v, p.dim_v);
     const int r = quarter * 32 + lane;                 // q row within the tile == TMEM lane
-    int g = 0, o_uses = 0;
+    int g = 0;
+    int o_cnt[2] = {0, 0};  // items that filled O, per item slot
     bool ok = true;
     int i = 0;
     for (; ok; ++i) {
@@ -464,13 +475,22 @@ __global__ void __launch_bounds__(kFwdThreads, 1) hstu_fwd_kernel(const __grid_c
         mbar_arrive(smem_u32(&s.bar_p_full[sbuf]));
       }
       if (!ok) break;
-      if (grp == 2) {  // groups 0 and 1 read O out; this one goes on to the next item
+      // The group that takes the next item's first tile (global tile index
+      // g + nt) goes on at once; the other two read O out, a column half
+      // each.
+      // Every group counts the items that fill O, whether or not it reads
+      // this one out: o_full[slot] completes a phase per such item.
+      const int o_phase = o_cnt[slot] & 1;
+      if (nt > 0) ++o_cnt[slot];
+      const int skip = (g + nt) % 3;
+      if (grp == skip) {
         mbar_arrive(smem_u32(&s.bar_item_empty[slot]));
         g += nt;
         continue;
       }
+      const int half = (grp - skip + 3) % 3 - 1;  // 0 or 1
       if (nt > 0) {
-        if (!warp_wait(smem_u32(&s.bar_o_full), o_uses & 1, abort_flag)) break;
+        if (!warp_wait(smem_u32(&s.bar_o_full[slot]), o_phase, abort_flag)) break;
         tc_fence_after();
       }
       if (*abort_flag) break;
@@ -480,7 +500,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) hstu_fwd_kernel(const __grid_c
       uint32_t v32[kNc][32];
       if (nt > 0) {
 #pragma unroll
-        for (int cc = 0; cc < kNc; ++cc) tmem_ld32(tO + lane_addr + grp * kHalfCols + cc * 32, v32[cc]);
+        for (int cc = 0; cc < kNc; ++cc) tmem_ld32(tO + lane_addr + half * kHalfCols + cc * 32, v32[cc]);
 #pragma unroll
         for (int cc = 0; cc < kNc; ++cc) tmem_ld_wait(v32[cc]);
       } else {
@@ -491,13 +511,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1) hstu_fwd_kernel(const __grid_c
       }
 #pragma unroll
       for (int cc = 0; cc < kNc; ++cc) {
-        const int col = grp * kHalfCols + cc * 32;
+        const int col = half * kHalfCols + cc * 32;
         if (valid && col < p.dim_v) store_row32<T>(dst + col, v32[cc], out_scale, wide);
       }
       if (nt > 0) {
         tc_fence_before();
         mbar_arrive(smem_u32(&s.bar_o_empty));
-        ++o_uses;
       }
       mbar_arrive(smem_u32(&s.bar_item_empty[slot]));
       g += nt;
