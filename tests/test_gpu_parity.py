@@ -44,6 +44,23 @@ def test_ragged_tails_all_masks(D, mask):
     compare(gb.run(), gb.oracle())
 
 
+def test_item_hand_offs_with_every_tile_count():
+    """Hundreds of short work items whose visited-tile counts run through
+    1..6 (with runs that are multiples of three) and empty sequences among
+    them: the forward's O read-out moves between epilogue groups from item
+    to item and the backward's roles alternate in windows, so every
+    hand-off order occurs; the whole batch is compared with the oracle."""
+    rng = np.random.default_rng(7)
+    pattern = [384, 384, 384, 0, 128, 1, 768, 640, 256, 0, 512, 130, 384, 384, 700, 3]
+    lens = np.array([pattern[i % len(pattern)] if i % 5 else int(rng.integers(1, 769))
+                     for i in range(96)])
+    cfg = wl.Config("h", len(lens), 0, 0, 2, 64, "causal", 1)
+    func = wl.build_func(cfg, lens, 1)
+    q, k, v, do = _gen(lens, 2, 64, seed=5)
+    gb = GpuBatch(lens, func, q, k, v, do, max_seqlen=768)
+    compare(gb.run(), gb.oracle())
+
+
 @pytest.mark.parametrize("nfunc", [1, 3, 5, 7, 9])
 def test_random_intervals(nfunc):
     """Arbitrary (also negative, out-of-range, reversed) func values."""
