@@ -64,8 +64,15 @@ __device__ void classify_tile(const PlanParams& p, int b, int qt) {
   nonempty = __reduce_or_sync(0xffffffffu, nonempty);
   if (lane == 0 && nonempty) atomicOr(&active_iv, nonempty);
 
+  // No row of this warp sees a column at or past its largest interval end:
+  // the kv tiles from there on are skip for the warp (their bits stay 0).
+  int hi_row = 0;
+#pragma unroll
+  for (int t = 0; t < NINT; ++t) hi_row = max(hi_row, hi[t]);
+  const int hi_warp = __reduce_max_sync(0xffffffffu, hi_row);
+  const int jmax = min(ntiles, (hi_warp + kBlock - 1) / kBlock);
   int count = 0;
-  for (int j = 0; j < ntiles; ++j) {
+  for (int j = 0; j < jmax; ++j) {
     // Most tiles lie wholly inside one interval or outside all of them (an
     // empty interval is [0,0) and never meets a tile); only the others need
     // the row's column bits.
