@@ -740,7 +740,12 @@ def main():
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
     from jagged_hstu_attention_gb300 import build_ext
-    build_ext.build()
+    # One rank per node compiles (the ranks share the object files and the
+    # library's path); the others wait for it.
+    if local == 0:
+        build_ext.build()
+    if world > 1:
+        dist.barrier(device_ids=[local])
     from jagged_hstu_attention_gb300 import binding as hb
     hb.load()
     if args.mode == "targets":
