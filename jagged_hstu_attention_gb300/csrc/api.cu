@@ -120,8 +120,6 @@ hstu::PlanParams plan_params(const int32_t* seq_offsets, const int32_t* func,
   p.header = reinterpret_cast<int32_t*>(base + l.header);
   p.fwd_list = reinterpret_cast<int32_t*>(base + l.fwd_list);
   p.bwd_list = reinterpret_cast<int32_t*>(base + l.bwd_list);
-  p.seq_order = reinterpret_cast<int32_t*>(base + l.seq_order);
-  p.seq_start = reinterpret_cast<int32_t*>(base + l.seq_start);
   p.ivmask = base + l.ivmask;
   p.cls = base + l.cls;
   p.total = s->total;

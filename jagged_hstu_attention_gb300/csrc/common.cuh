@@ -64,8 +64,7 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // the kernels read; every other region is fully written before it is read.
 struct FullLayout {
   int nt = 0;  // tiles per sequence at max_seqlen
-  size_t header = 0, header_bytes = 0, fwd_list = 0, bwd_list = 0, seq_order = 0, seq_start = 0,
-         ivmask = 0, cls = 0, total = 0;
+  size_t header = 0, header_bytes = 0, fwd_list = 0, bwd_list = 0, ivmask = 0, cls = 0, total = 0;
 };
 inline FullLayout full_layout(int batch, int max_seqlen) {
   FullLayout l;
@@ -75,9 +74,7 @@ inline FullLayout full_layout(int batch, int max_seqlen) {
   l.header_bytes = kHdrWords * 4;
   l.fwd_list = l.header_bytes;
   l.bwd_list = l.fwd_list + align_up(items * 4, 256);
-  l.seq_order = l.bwd_list + align_up(2 * items * 4, 256);
-  l.seq_start = l.seq_order + align_up(static_cast<size_t>(batch) * 4, 256);
-  l.ivmask = l.seq_start + align_up(static_cast<size_t>(batch) * 4, 256);
+  l.ivmask = l.bwd_list + align_up(2 * items * 4, 256);
   l.cls = l.ivmask + align_up(items, 256);
   l.total = l.cls + align_up(items * l.nt, 256);
   return l;
@@ -120,8 +117,6 @@ struct PlanParams {
   int32_t* header;
   int32_t* fwd_list;
   int32_t* bwd_list;
-  int32_t* seq_order;  // sequences, longest first
-  int32_t* seq_start;  // first work item of each sorted sequence
   uint8_t* ivmask;     // per q tile: bit t set iff interval t is non-empty for some row
   uint8_t* cls;
   int64_t total;

@@ -127,73 +127,79 @@ __device__ void classify_tile(const PlanParams& p, int b, int qt) {
   if (tid == 0) p.ivmask[static_cast<size_t>(b) * p.nt + qt] = static_cast<uint8_t>(active_iv);
 }
 
-// Exclusive scan of cnt[0..n) in place, by one block (any multiple of 32
-// threads up to 1024), in chunks of blockDim.x entries.
-__device__ void block_exclusive_scan(int* cnt, int n) {
-  __shared__ int carry;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  __shared__ int warp_sums[32];
-  if (tid == 0) carry = 0;
-  __syncthreads();
-  for (int base = 0; base < n; base += blockDim.x) {
-    const int idx = base + tid;
-    const int x = idx < n ? cnt[idx] : 0;
-    int incl = x;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, d);
-      if (lane >= d) incl += y;
-    }
-    if (lane == 31) warp_sums[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-      const int ws = lane < (blockDim.x >> 5) ? warp_sums[lane] : 0;
-      int wincl = ws;
-#pragma unroll
-      for (int d = 1; d < 32; d <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, wincl, d);
-        if (lane >= d) wincl += y;
-      }
-      warp_sums[lane] = wincl - ws;
-    }
-    __syncthreads();
-    const int excl = carry + warp_sums[warp] + incl - x;
-    __syncthreads();
-    if (idx < n) cnt[idx] = excl;
-    if (tid == blockDim.x - 1) carry = excl + x;
-    __syncthreads();
-  }
-}
-
-// Work lists. Sequences are ordered longest first (counting sort on their
+// Work lists. Sequences are ordered longest first (a counting sort on their
 // tile count) and every sequence's items are contiguous, so the CTAs that
 // run at the same time work on one or two sequences and share their K/V (or
 // Q/dO) tiles in L2 instead of streaming every sequence's tiles from HBM at
 // once. Within a sequence the heaviest items come first: forward q tiles
 // last-first (the later rows of causal-like masks see the most columns);
 // backward dK/dV kv tiles first-first and dQ q tiles last-first, the two
-// roles grouped in windows of list entries (below). Sequences
-// of equal length may come out in any order: every output element is
-// computed by exactly one CTA with a fixed internal order, so the order only
-// changes scheduling, never results.
+// roles grouped in windows of list entries (below). Sequences of equal tile
+// count may come out in any order: every output element is computed by
+// exactly one CTA with a fixed internal order, so the order only changes
+// scheduling, never results.
 //
-// Before that it checks seq_offsets (first 0, last = total, every length in
-// [0, max_seqlen]) and writes the header: the error word (kErrInput, with
-// empty lists, if the check fails), the list lengths, the uniform flag and
-// the zeroed work counters.
+// Block 0 does this in two passes over the sequences, each thread keeping
+// kListUnroll sequences' offset loads in flight:
+//   1. check seq_offsets (first 0, last = total, every length in
+//      [0, max_seqlen]) and count the sequences of each tile count (bin
+//      nt - tiles, so that bins run longest first), one shared atomic per
+//      bin and warp;
+//   2. give each sequence its position within its bin (again one atomic per
+//      bin and warp) and write its items. The sequences before it are the
+//      earlier bins and the earlier positions of its own bin, so its first
+//      list entry follows from the bins' prefix sums without a scan over
+//      the batch.
+// It writes the header: the error word (kErrInput, with empty lists, if the
+// check fails), the list lengths, the uniform flag and the zeroed work
+// counters.
+constexpr int kListUnroll = 8;
+
 __device__ void build_work_lists(const PlanParams& p) {
-  __shared__ int hist[kMaxTiles + 1];
-  __shared__ int n_items;
-  __shared__ int bad;
-  const int tid = threadIdx.x;
+  __shared__ int hist[kMaxTiles + 1];      // sequences per bin
+  __shared__ int bin_pos[kMaxTiles + 1];   // first sorted position of each bin
+  __shared__ int bin_item[kMaxTiles + 1];  // first list entry of each bin
+  __shared__ int cursor[kMaxTiles + 1];    // next free position of each bin
+  __shared__ int n_items, n_first, uniform_s, bad;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int nt = p.nt;
+  const int step = kListUnroll * static_cast<int>(blockDim.x);
+  // The sequences of this thread in one round of a pass, their offsets, and
+  // their bins (-1 past the batch).
+  auto load_round = [&](int base, int (&o0)[kListUnroll], int (&o1)[kListUnroll]) {
+#pragma unroll
+    for (int u = 0; u < kListUnroll; ++u) {
+      const int b = base + u * static_cast<int>(blockDim.x) + tid;
+      o0[u] = b < p.batch ? p.seq_offsets[b] : 0;
+      o1[u] = b < p.batch ? p.seq_offsets[b + 1] : 0;
+    }
+  };
+  auto bin_of = [&](int o0, int o1) {
+    int64_t L = static_cast<int64_t>(o1) - o0;
+    L = L < 0 ? 0 : (L > p.max_seqlen ? p.max_seqlen : L);
+    return nt - static_cast<int>((L + kBlock - 1) / kBlock);
+  };
+
   if (tid == 0)
     bad = (p.seq_offsets[0] != 0 || static_cast<int64_t>(p.seq_offsets[p.batch]) != p.total) ? 1 : 0;
+  for (int x = tid; x <= nt; x += blockDim.x) hist[x] = 0;
   __syncthreads();
-  for (int b = tid; b < p.batch; b += blockDim.x) {
-    const int o0 = p.seq_offsets[b], o1 = p.seq_offsets[b + 1];
-    const int64_t L = static_cast<int64_t>(o1) - o0;
-    if (o0 < 0 || static_cast<int64_t>(o1) > p.total || L < 0 || L > p.max_seqlen)
-      bad = 1;  // every writer stores the same value
+  for (int base = 0; base < p.batch; base += step) {
+    int o0[kListUnroll], o1[kListUnroll];
+    load_round(base, o0, o1);
+#pragma unroll
+    for (int u = 0; u < kListUnroll; ++u) {
+      const int b = base + u * static_cast<int>(blockDim.x) + tid;
+      int bin = -1;
+      if (b < p.batch) {
+        const int64_t L = static_cast<int64_t>(o1[u]) - o0[u];
+        if (o0[u] < 0 || static_cast<int64_t>(o1[u]) > p.total || L < 0 || L > p.max_seqlen)
+          bad = 1;  // every writer stores the same value
+        bin = bin_of(o0[u], o1[u]);
+      }
+      const unsigned same = __match_any_sync(0xffffffffu, bin);
+      if (bin >= 0 && lane == __ffs(same) - 1) atomicAdd(&hist[bin], __popc(same));
+    }
   }
   __syncthreads();
   if (tid == 0) {
@@ -211,26 +217,23 @@ __device__ void build_work_lists(const PlanParams& p) {
     }
     return;
   }
-  const int nt = p.nt;
-  auto tiles_of = [&](int b) {
-    int L = p.seq_offsets[b + 1] - p.seq_offsets[b];
-    L = min(max(L, 0), p.max_seqlen);
-    return (L + kBlock - 1) / kBlock;
-  };
-  for (int x = tid; x <= nt; x += blockDim.x) hist[x] = 0;
-  __syncthreads();
-  for (int b = tid; b < p.batch; b += blockDim.x) atomicAdd(&hist[nt - tiles_of(b)], 1);
-  __syncthreads();
-  block_exclusive_scan(hist, nt + 1);
-  __syncthreads();
-  for (int b = tid; b < p.batch; b += blockDim.x)
-    p.seq_order[atomicAdd(&hist[nt - tiles_of(b)], 1)] = b;
-  __syncthreads();
-  for (int pos = tid; pos < p.batch; pos += blockDim.x) p.seq_start[pos] = tiles_of(p.seq_order[pos]);
-  __syncthreads();
-  block_exclusive_scan(p.seq_start, p.batch);
-  __syncthreads();
-  if (tid == 0) n_items = p.seq_start[p.batch - 1] + tiles_of(p.seq_order[p.batch - 1]);
+  if (tid == 0) {
+    int pos = 0, item = 0, first = -1, last = -1;
+    for (int x = 0; x <= nt; ++x) {
+      bin_pos[x] = pos;
+      cursor[x] = pos;
+      bin_item[x] = item;
+      if (hist[x] > 0) {
+        if (first < 0) first = x;
+        last = x;
+      }
+      pos += hist[x];
+      item += hist[x] * (nt - x);
+    }
+    n_items = item;
+    n_first = nt - first;           // the longest sequence's tile count (batch >= 1)
+    uniform_s = first == last ? 1 : 0;  // every sequence has that many tiles
+  }
   __syncthreads();
   // Backward: entry e = st + t of the sequence-major order goes to window
   // w = e / role_window; a window lists its dK/dV items first, then its dQ
@@ -242,27 +245,43 @@ __device__ void build_work_lists(const PlanParams& p) {
   // n, one sequence each (its dK/dV items, then its dQ items): their CTAs
   // take items by a fixed stride, which balances that order by
   // construction, and a window spanning sequences can unbalance it.
-  const int n_first = tiles_of(p.seq_order[0]);
-  const bool uniform = n_first == tiles_of(p.seq_order[p.batch - 1]);
-  const int total = n_items, win = uniform ? max(n_first, 1) : p.role_window;
-  for (int pos = tid; pos < p.batch; pos += blockDim.x) {
-    const int b = p.seq_order[pos];
-    const int n = tiles_of(b);
-    const int st = p.seq_start[pos];
-    for (int t = 0; t < n; ++t) {
-      const int e = st + t, w0 = e / win * win;
-      const int len = min(win, total - w0);
-      p.fwd_list[e] = (b << 8) | (n - 1 - t);
-      p.bwd_list[2 * w0 + (e - w0)] = (b << 8) | t | kRoleDkdv;
-      p.bwd_list[2 * w0 + len + (e - w0)] = (b << 8) | (n - 1 - t);
+  const int total = n_items, win = uniform_s ? max(n_first, 1) : p.role_window;
+  for (int base = 0; base < p.batch; base += step) {
+    int o0[kListUnroll], o1[kListUnroll];
+    load_round(base, o0, o1);
+#pragma unroll
+    for (int u = 0; u < kListUnroll; ++u) {
+      const int b = base + u * static_cast<int>(blockDim.x) + tid;
+      const int bin = b < p.batch ? bin_of(o0[u], o1[u]) : -1;
+      const unsigned same = __match_any_sync(0xffffffffu, bin);
+      const int leader = __ffs(same) - 1;
+      int first_pos = 0;
+      if (bin >= 0 && lane == leader) first_pos = atomicAdd(&cursor[bin], __popc(same));
+      first_pos = __shfl_sync(0xffffffffu, first_pos, leader);
+      if (bin < 0) continue;
+      const int pos = first_pos + __popc(same & ((1u << lane) - 1u));
+      const int n = nt - bin;
+      const int st = bin_item[bin] + (pos - bin_pos[bin]) * n;
+      // Entry e = st + t lies at r = e - w0 in the window starting at w0,
+      // which holds len entries of each role; both advance with e.
+      int w0 = st / win * win, r = st - w0, len = min(win, total - w0);
+      for (int t = 0; t < n; ++t) {
+        p.fwd_list[st + t] = (b << 8) | (n - 1 - t);
+        p.bwd_list[2 * w0 + r] = (b << 8) | t | kRoleDkdv;
+        p.bwd_list[2 * w0 + len + r] = (b << 8) | (n - 1 - t);
+        if (++r == win) {
+          w0 += win;
+          r = 0;
+          len = min(win, total - w0);
+        }
+      }
     }
   }
   if (tid == 0) {
     p.header[kHdrErr] = 0;
     p.header[kHdrNFwd] = n_items;
     p.header[kHdrNBwd] = 2 * n_items;
-    // seq_order is sorted by tile count: equal ends mean equal counts.
-    p.header[kHdrUniform] = tiles_of(p.seq_order[0]) == tiles_of(p.seq_order[p.batch - 1]) ? 1 : 0;
+    p.header[kHdrUniform] = uniform_s;
   }
 }
 

@@ -224,6 +224,39 @@ def test_small_batches_never_reach_a_wait_limit(lens):
     compare(out, gb.oracle())
 
 
+def test_many_short_sequences_all_items_run():
+    """Eight thousand sequences of mixed length (zero included): the plan's
+    list builder takes several rounds per thread, and its warps hold
+    sequences of several tile counts at once. Every row of every output is
+    written (the outputs start as NaN), the visible counts are exactly
+    i + 1 (causal), and sampled sequences match the oracle."""
+    rng = np.random.default_rng(11)
+    lens = rng.integers(1, 300, size=8000)
+    lens[rng.choice(len(lens), 400, replace=False)] = 0
+    H, D = 1, 32
+    q, k, v, do = _gen(lens, H, D, seed=11)
+    gb = GpuBatch(lens, wl.build_func(wl.Config("many", len(lens), 0, 0, H, D, "causal", 1), lens, 1),
+                  q, k, v, do)
+    T = gb.total
+    shape = hb.make_shape(len(lens), T, H, D, 1, gb.max_seqlen, gb.alpha)
+    ws = hb.alloc_workspace(shape)
+    counts = torch.full((T,), -1, dtype=torch.int32, device="cuda")
+    o = torch.full_like(gb.q, float("nan"))
+    grads = tuple(torch.full_like(gb.q, float("nan")) for _ in range(3))
+    hb.fwd(gb.q, gb.k, gb.v, gb.d_off, gb.d_func, gb.max_seqlen, gb.alpha, ws=ws, row_counts=counts, out=o)
+    hb.bwd(gb.do, gb.q, gb.k, gb.v, gb.d_off, gb.d_func, gb.max_seqlen, gb.alpha, ws=ws, reuse_plan=True,
+           outs=grads)
+    torch.cuda.synchronize()
+    assert hb.device_status(ws) == hb.HSTU_OK
+    for name, t in zip(("o", "dq", "dk", "dv"), (o,) + grads):
+        assert not torch.isnan(t).any(), f"{name}: rows left unwritten"
+    local = np.arange(T) - np.repeat(gb.offsets[:-1], lens)
+    assert np.array_equal(counts.cpu().numpy(), local + 1)
+    nz = np.nonzero(lens)[0]
+    seqs = [int(nz[0]), int(np.argmax(lens)), int(nz[np.argmin(lens[nz])]), int(nz[-1]), int(nz[len(nz) // 2])]
+    compare({"o": o, "dq": grads[0], "dk": grads[1], "dv": grads[2], "counts": counts}, gb.oracle(seqs))
+
+
 def test_batch_of_empty_sequences():
     """No rows at all: every entry point accepts it, writes nothing, and the
     targets-only candidates (which see no key) get zeros."""
