@@ -80,6 +80,12 @@ typedef enum {
 #define HSTU_DTYPE_BF16 0
 #define HSTU_DTYPE_F16 1
 
+/* Size limits of a shape:
+ *   - T < 2^31, since seq_offsets are int32 (else HSTU_ERR_INVALID_ARG);
+ *   - B < 2^22, since the work lists pack the sequence index in 22 bits
+ *     (else HSTU_ERR_UNSUPPORTED);
+ *   - 2 min(B ceil(N/128), T/128 + B) H < 2^30: the backward's work items,
+ *     which the kernels number in int32 (else HSTU_ERR_UNSUPPORTED). */
 typedef struct {
   int32_t batch;      /* B, number of sequences (>= 1) */
   int64_t total;      /* T = seq_offsets[B], rows of k and v (and of q, o) */

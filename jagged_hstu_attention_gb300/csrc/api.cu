@@ -43,6 +43,14 @@ hstu_status_t check_shape(const hstu_attn_shape_t* s) {
   if (!dim_ok(s->head_dim) || (s->head_dim_v != 0 && !dim_ok(s->head_dim_v))) return HSTU_ERR_UNSUPPORTED;
   if (s->dtype != HSTU_DTYPE_BF16 && s->dtype != HSTU_DTYPE_F16) return HSTU_ERR_UNSUPPORTED;
   if (!(s->alpha == s->alpha)) return HSTU_ERR_INVALID_ARG;  // NaN
+  // The kernels number their work (list entry x heads + head) in int32, and
+  // their counters run past the end by up to a grid: keep it below 2^30. The
+  // backward list has 2 sum_b ceil(L_b / 128) <= 2 min(B NT, T / 128 + B)
+  // entries.
+  const int64_t nt = (static_cast<int64_t>(s->max_seqlen) + hstu::kBlock - 1) / hstu::kBlock;
+  const int64_t entries =
+      2 * std::min<int64_t>(static_cast<int64_t>(s->batch) * nt, s->total / hstu::kBlock + s->batch);
+  if (entries * s->num_heads >= (int64_t{1} << 30)) return HSTU_ERR_UNSUPPORTED;
   return HSTU_OK;
 }
 

@@ -83,6 +83,22 @@ def test_workspace_size(lib):
     assert hb.workspace_size(_shape(), 7) == 0
 
 
+def test_work_index_bound(lib):
+    """Backward list entries x heads must stay below 2^30 (the kernels' int32
+    work index, plus a grid of overrun): 2 min(B NT, T/128 + B) entries."""
+    # 2 * min(1000 * 256, 2**20 // 128 + 1000) = 18384 entries
+    ok = _shape(batch=1000, total=1 << 20, max_seqlen=32768, heads=(1 << 30) // 18384)
+    assert hb.workspace_size(ok, hb.WS_FULL) > 0
+    bad = _shape(batch=1000, total=1 << 20, max_seqlen=32768, heads=(1 << 30) // 18384 + 1)
+    assert hb.workspace_size(bad, hb.WS_FULL) == 0
+    # here T / 128 + B decides: 2 * min(4 * 3, 1000 // 128 + 4) = 22 entries
+    assert hb.workspace_size(_shape(max_seqlen=300, heads=(1 << 30) // 22), hb.WS_FULL) > 0
+    assert hb.workspace_size(_shape(max_seqlen=300, heads=(1 << 30) // 22 + 1), hb.WS_FULL) == 0
+    # and B NT for a small maximum: 2 * min(4 * 1, 7 + 4) = 8 entries
+    assert hb.workspace_size(_shape(max_seqlen=100, heads=(1 << 30) // 8 - 1), hb.WS_FULL) > 0
+    assert hb.workspace_size(_shape(max_seqlen=100, heads=(1 << 30) // 8), hb.WS_FULL) == 0
+
+
 def _fwd(lib, shape, q=1 << 20, k=1 << 20, v=1 << 20, o=1 << 20, off=1 << 20, func=1 << 20,
          ws=1 << 20, ws_bytes=1 << 30):
     vp = ctypes.c_void_p
