@@ -314,7 +314,8 @@ template <typename T, int DQ, int DV, bool BWD>
 static cudaError_t launch_tgt_t(const TgtParams& p, cudaStream_t stream) {
   constexpr int DM = DQ > DV ? DQ : DV;
   const long long blocks = static_cast<long long>(p.num_cand) * p.nc;
-  if (blocks > 0x7fffffffLL || static_cast<long long>(p.batch) * p.nc > 0x7fffffffLL)
+  if (blocks > 0x7fffffffLL || static_cast<long long>(p.batch) * p.nc > 0x7fffffffLL ||
+      static_cast<long long>(p.num_cand) * p.heads > 0x7fffffffLL || p.heads > 65535)
     return cudaErrorInvalidConfiguration;
   const bool multi = p.cand_offsets != nullptr;
   if (BWD && multi) {
