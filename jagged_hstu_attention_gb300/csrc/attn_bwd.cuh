@@ -132,30 +132,33 @@ __device__ __forceinline__ bool warp_wait_b(uint32_t bar, uint32_t parity, volat
   return __all_sync(0xffffffffu, ok);
 }
 
-// Writes this warp's half of TMEM columns [taddr, taddr + DP) of its lane (or
-// zeros), times `scale`, into a row of `dim` elements of T. Both 32-column
-// chunks are read before the first store.
-template <typename T, int DP>
-__device__ __forceinline__ void store_acc_half(uint32_t taddr, int half, bool have, bool valid, T* dst,
-                                               int dim, float scale, bool wide) {
-  constexpr int kNc = DP / 64;
-  uint32_t a[kNc][32];
+// Reads NC 32-column accumulator chunks (TMEM addresses ta[c], this warp's
+// lanes) with a single wait, or zeros when `have` is false.
+template <int NC>
+__device__ __forceinline__ void load_acc_chunks(const uint32_t (&ta)[NC], bool have, uint32_t (&a)[NC][32]) {
   if (have) {
 #pragma unroll
-    for (int c = 0; c < kNc; ++c) tmem_ld32(taddr + half * (DP / 2) + c * 32, a[c]);
+    for (int c = 0; c < NC; ++c) tmem_ld32(ta[c], a[c]);
 #pragma unroll
-    for (int c = 0; c < kNc; ++c) tmem_ld_wait(a[c]);
+    for (int c = 0; c < NC; ++c) tmem_ld_wait(a[c]);
   } else {
 #pragma unroll
-    for (int c = 0; c < kNc; ++c)
+    for (int c = 0; c < NC; ++c)
 #pragma unroll
       for (int e = 0; e < 32; ++e) a[c][e] = 0u;
   }
+}
+
+// Writes chunk c of `a`, times `scale`, as columns [col[c], col[c] + 32) of
+// the row dst[c] of dim[c] elements (nothing for an invalid row or columns
+// past dim[c]).
+template <typename T, int NC>
+__device__ __forceinline__ void store_acc_chunks(const uint32_t (&a)[NC][32], T* const (&dst)[NC],
+                                                 const int (&col)[NC], const int (&dim)[NC], bool valid,
+                                                 float scale, bool wide) {
 #pragma unroll
-  for (int c = 0; c < kNc; ++c) {
-    const int col = half * (DP / 2) + c * 32;
-    if (valid && col < dim) store_row32<T>(dst + col, a[c], scale, wide);
-  }
+  for (int c = 0; c < NC; ++c)
+    if (valid && col[c] < dim[c]) store_row32<T>(dst[c] + col[c], a[c], scale, wide);
 }
 
 // 16 columns [C0, C0 + 16) of 32 loaded S and dP columns -> packed T
@@ -654,19 +657,56 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
       }
       if (*abort_flag) break;
       const int64_t row = static_cast<int64_t>(o0 + own_loc) * p.heads + h;
+      // This warp's half of the accumulators (dV and dK, or dQ) is loaded
+      // with one wait and released before the rows are stored, so that the
+      // next item may overwrite those columns meanwhile.
       if (dkdv) {
-        store_acc_half<T, DPV>(t_acc0 + lane_addr, half, nt > 0, valid, static_cast<T*>(p.out2) + row * p.dim_v,
-                               p.dim_v, out_scale, wide);  // dV
-        store_acc_half<T, DPQ>(t_acc1 + lane_addr, half, nt > 0, valid, static_cast<T*>(p.out1) + row * p.dim,
-                               p.dim, out_scale, wide);  // dK
+        constexpr int kV = DPV / 64, kQ = DPQ / 64;  // chunks per half of dV / dK
+        uint32_t ta[kV + kQ];
+        T* dst[kV + kQ];
+        int col[kV + kQ], dim[kV + kQ];
+#pragma unroll
+        for (int c = 0; c < kV; ++c) {
+          col[c] = half * (DPV / 2) + 32 * c;
+          ta[c] = t_acc0 + lane_addr + col[c];
+          dst[c] = static_cast<T*>(p.out2) + row * p.dim_v;
+          dim[c] = p.dim_v;
+        }
+#pragma unroll
+        for (int c = 0; c < kQ; ++c) {
+          col[kV + c] = half * (DPQ / 2) + 32 * c;
+          ta[kV + c] = t_acc1 + lane_addr + col[kV + c];
+          dst[kV + c] = static_cast<T*>(p.out1) + row * p.dim;
+          dim[kV + c] = p.dim;
+        }
+        uint32_t a[kV + kQ][32];
+        load_acc_chunks<kV + kQ>(ta, nt > 0, a);
+        if (nt > 0) {
+          tc_fence_before();
+          mbar_arrive(smem_u32(&s.bar_acc_empty));
+          ++acc_uses;
+        }
+        store_acc_chunks<T, kV + kQ>(a, dst, col, dim, valid, out_scale, wide);
       } else {
-        store_acc_half<T, DPQ>(t_acc0 + lane_addr, half, nt > 0, valid, static_cast<T*>(p.out0) + row * p.dim,
-                               p.dim, out_scale, wide);  // dQ
-      }
-      if (nt > 0) {
-        tc_fence_before();
-        mbar_arrive(smem_u32(&s.bar_acc_empty));
-        ++acc_uses;
+        constexpr int kC = DPQ / 64;  // chunks per half of dQ
+        uint32_t ta[kC];
+        T* dst[kC];
+        int col[kC], dim[kC];
+#pragma unroll
+        for (int c = 0; c < kC; ++c) {
+          col[c] = half * (DPQ / 2) + 32 * c;
+          ta[c] = t_acc0 + lane_addr + col[c];
+          dst[c] = static_cast<T*>(p.out0) + row * p.dim;
+          dim[c] = p.dim;
+        }
+        uint32_t a[kC][32];
+        load_acc_chunks<kC>(ta, nt > 0, a);
+        if (nt > 0) {
+          tc_fence_before();
+          mbar_arrive(smem_u32(&s.bar_acc_empty));
+          ++acc_uses;
+        }
+        store_acc_chunks<T, kC>(a, dst, col, dim, valid, out_scale, wide);
       }
       mbar_arrive(smem_u32(&s.bar_item_empty[slot]));
       g0 += lhs;

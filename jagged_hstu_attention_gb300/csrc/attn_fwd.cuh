@@ -509,14 +509,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1) hstu_fwd_kernel(const __grid_c
 #pragma unroll
           for (int e = 0; e < 32; ++e) v32[cc][e] = 0u;
       }
+      // O is in registers: the next item's first PV may overwrite it while
+      // the rows are stored.
+      if (nt > 0) {
+        tc_fence_before();
+        mbar_arrive(smem_u32(&s.bar_o_empty));
+      }
 #pragma unroll
       for (int cc = 0; cc < kNc; ++cc) {
         const int col = half * kHalfCols + cc * 32;
         if (valid && col < p.dim_v) store_row32<T>(dst + col, v32[cc], out_scale, wide);
-      }
-      if (nt > 0) {
-        tc_fence_before();
-        mbar_arrive(smem_u32(&s.bar_o_empty));
       }
       mbar_arrive(smem_u32(&s.bar_item_empty[slot]));
       g += nt;
