@@ -428,6 +428,7 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
         const int nt = s.item[slot].nt;
         if (nt < 0) break;  // no more work
         const bool dkdv = s.item[slot].dkdv != 0;
+        const int nsteps = s.item[slot].nhs;  // every field this thread reads, before the slot is released
         mbar_arrive(smem_u32(&s.bar_item_empty[slot]));
         if (nt == 0) continue;
         if (!mbar_wait(smem_u32(&s.bar_res_full), res_uses & 1, abort_flag)) break;
@@ -455,7 +456,6 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
           for (int kk = 0; kk < DPQ / 16; ++kk)
             tmem_cp_128x256b(tK + 8 * kk, sdesc_advance(dr0, (kk >> 2) * kChunkBytes + (kk & 3) * 32));
         }
-        const int nsteps = s.item[slot].nhs;
         const int gv0 = ghs;  // global index of this item's first half-step
         // S/dP of step v (N = 64 MMAs): S (or S^T) = res0 . str0_h^T into S
         // slot gv % kSSlots, dP (or dP^T) = res1 . str1_h^T into the dP slot
@@ -651,6 +651,9 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
         mbar_arrive(smem_u32(&s.bar_p_full[k]));
       }
       if (!ok) break;
+      // The item's fields are in registers from here on: its slot may take
+      // the item after next while the accumulators are read out.
+      mbar_arrive(smem_u32(&s.bar_item_empty[slot]));
       if (nt > 0) {
         if (!warp_wait_b(smem_u32(&s.bar_acc_full), acc_uses & 1, abort_flag)) break;
         tc_fence_after();
@@ -708,7 +711,6 @@ __global__ void __launch_bounds__(320, 1) hstu_bwd_kernel(const __grid_constant_
         }
         store_acc_chunks<T, kC>(a, dst, col, dim, valid, out_scale, wide);
       }
-      mbar_arrive(smem_u32(&s.bar_item_empty[slot]));
       g0 += lhs;
     }
   }
