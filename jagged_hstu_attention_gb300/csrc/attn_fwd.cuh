@@ -494,6 +494,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) hstu_fwd_kernel(const __grid_c
         tc_fence_after();
       }
       if (*abort_flag) break;
+      // O is complete: the MMA thread has read the item's tile list for its
+      // last PV, and this group needs only registers from here on, so the
+      // slot may take the item after next during the read-out.
+      mbar_arrive(smem_u32(&s.bar_item_empty[slot]));
       constexpr int kHalfCols = DPV / 2;
       constexpr int kNc = kHalfCols / 32;
       T* dst = static_cast<T*>(p.out0) + (static_cast<int64_t>(o0 + qt * kBlock + r) * p.heads + h) * p.dim_v;
@@ -520,7 +524,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1) hstu_fwd_kernel(const __grid_c
         const int col = half * kHalfCols + cc * 32;
         if (valid && col < p.dim_v) store_row32<T>(dst + col, v32[cc], out_scale, wide);
       }
-      mbar_arrive(smem_u32(&s.bar_item_empty[slot]));
       g += nt;
     }
   }
